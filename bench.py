@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark of the per-rank hot path of context-parallel causal attention
+over packed THD (libcpthd on one GB300).
+
+One *step* runs the whole path for one packed workload: for every strategy
+the workload names and every context-parallel rank (sequentially, on one
+GPU): partition index -> reorder of the Q slice and of the int64
+input_ids / labels / position_ids -> causal THD attention forward (tile
+metadata + attention kernel).
+
+The headline metric is attention TFLOPS over unmasked pairs only
+(4 * d * pairs * Hq per step, pairs counted from the rank's index list)
+divided by the device time of the step, measured with CUDA events on the
+launching stream. L2 (129 MB) is flushed between timed steps by writing a
+256 MB buffer outside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the float64 CPU oracle, timed on host cores
+
+Under torchrun (N > 1) every rank runs an independent replica of the step
+(weak scaling; the path has no collective), the slowest rank's time counts,
+and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "causal-THD attn fwd TFLOPS (unmasked pairs) & % BF16 peak; reorder GB/s"
+DEFAULT_WORKLOAD = W.CONFIGS[1].name
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def rank_pairs(idx: np.ndarray, lay: W.Layout) -> int:
+    """Unmasked (query, key) pairs of one rank's slice, per head: a row at
+    position pos of a document sees pos + 1 keys; pad rows see none."""
+    cup = lay.cu_seqlens_padded.astype(np.int64)
+    j = np.searchsorted(cup, idx, side="right") - 1
+    pos = idx - cup[j]
+    valid = pos < lay.lengths[j]
+    return int((pos[valid] + 1).sum())
+
+
+# ----------------------------------------------------------------------------
+# clocks sampling (nvidia-smi during the timed region)
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the CUDA path
+# ----------------------------------------------------------------------------
+class Strategy:
+    """Device-resident inputs, outputs and workspaces of one strategy."""
+
+    def __init__(self, cp, cfg, strategy, dev):
+        self.name = strategy
+        inp = W.make_attn_inputs(cfg, strategy)
+        lay = inp.layout
+        self.lay = lay
+        self.T = lay.T
+        self.cpsize = cfg.cp
+        self.t_local = cp.cp_local_tokens(strategy, lay.T, cfg.cp)
+        ids, labels, pos = W.make_ids_logical(cfg.seed, lay)
+        host = {
+            "q": inp.q, "k": inp.k, "v": inp.v,
+            "cu": torch.from_numpy(lay.cu_seqlens), "cup": torch.from_numpy(lay.cu_seqlens_padded),
+            "ids": W.to_physical(ids, lay, -1), "labels": W.to_physical(labels, lay, -1),
+            "pos": W.to_physical(pos, lay, -1),
+        }
+        self.host = {k: v.contiguous().pin_memory() for k, v in host.items()}
+        self.dev = {k: v.to(dev) for k, v in self.host.items()}
+        tl, hq, d = self.t_local, cfg.hq, cfg.d
+        self.idx = [torch.empty(tl, dtype=torch.int32, device=dev) for _ in range(cfg.cp)]
+        self.q_loc = [torch.empty((tl, hq, d), dtype=torch.bfloat16, device=dev) for _ in range(cfg.cp)]
+        self.ids_loc = [[torch.empty(tl, dtype=torch.int64, device=dev) for _ in range(3)] for _ in range(cfg.cp)]
+        self.out = [torch.empty((tl, hq, d), dtype=torch.bfloat16, device=dev) for _ in range(cfg.cp)]
+        self.lse = [torch.empty((hq, tl), dtype=torch.float32, device=dev) for _ in range(cfg.cp)]
+        self.ws = torch.empty(cp.thd_causal_attn_workspace_size(tl, hq, cfg.hkv, d), dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(2, dtype=torch.int32, device=dev)
+        self.out_host = [torch.empty_like(o, device="cpu").pin_memory() for o in self.out]
+        self.lse_host = [torch.empty_like(x, device="cpu").pin_memory() for x in self.lse]
+        # algorithmic work, from the index lists the library itself returns
+        self.pairs = []
+        for r in range(cfg.cp):
+            cp.cp_partition_index(strategy, self.dev["cup"], self.T, cfg.cp, r, out=self.idx[r], err=self.err)
+            self.pairs.append(rank_pairs(self.idx[r].cpu().numpy().astype(np.int64), lay))
+        self.flops = [4.0 * d * p * hq for p in self.pairs]
+        # reorder bytes per rank: read + write of every gathered row, plus the index list
+        rb = hq * d * 2 + 3 * 8
+        self.reorder_bytes = tl * (2 * rb + 4)
+
+    # launches per rank: partition (offset check + index) 2, Q reorder 1,
+    # ids reorder 1, attention (doc check, tile metadata, tile order, attention) 4
+    LAUNCHES_PER_RANK = 8
+
+    def run_rank(self, cp, r, ev=None):
+        d = self.dev
+        if ev is not None:
+            ev[0].record()
+        cp.cp_partition_index(self.name, d["cup"], self.T, self.cpsize, r, out=self.idx[r], err=self.err)
+        cp.cp_reorder(d["q"], self.idx[r], out=self.q_loc[r], err=self.err)
+        cp.cp_reorder_multi([d["ids"], d["labels"], d["pos"]], self.idx[r], outs=self.ids_loc[r], err=self.err)
+        if ev is not None:
+            ev[1].record()
+        cp.thd_causal_attn_fwd(self.idx[r], self.q_loc[r], d["k"], d["v"], d["cu"], d["cup"], out=self.out[r],
+                               lse=self.lse[r], workspace=self.ws, err=self.err)
+        if ev is not None:
+            ev[2].record()
+
+
+def run_cuda(args):
+    import context_packed_thd_gb300 as cp
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = W.CONFIG_BY_NAME[args.workload]
+    strategies = [Strategy(cp, cfg, s, dev) for s in cfg.strategies]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        k = 0
+        for st in strategies:
+            for r in range(cfg.cp):
+                st.run_rank(cp, r, None if evs is None else evs[k])
+                k += 1
+
+    n_ranks = cfg.cp * len(strategies)
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    for st in strategies:
+        e = st.err.cpu().tolist()
+        if e[0] != 0:
+            raise RuntimeError(f"device check failed during warm-up: {cp.cpthd_status_string(e[0])} ({e})")
+
+    # ---- device-timed region -------------------------------------------------
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    rank_ev = [[tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(n_ranks)]
+               for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()
+        step_ev[i][0].record(stream)
+        step(rank_ev[i])
+        step_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    total_ms = sum(step_ms)
+    attn_ms = [[rank_ev[i][k][1].elapsed_time(rank_ev[i][k][2]) for k in range(n_ranks)] for i in range(args.steps)]
+    prep_ms = [[rank_ev[i][k][0].elapsed_time(rank_ev[i][k][1]) for k in range(n_ranks)] for i in range(args.steps)]
+    flops_step = sum(sum(st.flops) for st in strategies)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+
+    # per-rank attention times (median over steps) and the dominant-kernel roofline
+    med_attn = [statistics.median(attn_ms[i][k] for i in range(args.steps)) for k in range(n_ranks)]
+    per_strategy = {}
+    k = 0
+    for st in strategies:
+        ms = med_attn[k:k + cfg.cp]
+        per_strategy[st.name] = {
+            "attn_ms_per_rank_max": max(ms), "attn_ms_per_rank_min": min(ms),
+            "attn_tflops": sum(st.flops) / (sum(ms) * 1e-3) / 1e12,
+            "pairs_per_rank_max": max(st.pairs), "pairs_per_rank_min": min(st.pairs),
+        }
+        k += cfg.cp
+    attn_total_ms = sum(sum(x) for x in attn_ms)
+    achieved = flops_step * args.steps / (attn_total_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    reorder_bytes = sum(st.reorder_bytes * cfg.cp for st in strategies)
+    prep_total_ms = sum(sum(x) for x in prep_ms)
+
+    # ---- end to end: pinned host inputs -> step -> host results --------------
+    e2e_steps = max(1, min(args.steps, 10))
+    h2d = sum(sum(t.numel() * t.element_size() for t in st.host.values()) for st in strategies)
+    d2h = sum(sum(o.numel() * o.element_size() + l.numel() * l.element_size() for o, l in zip(st.out, st.lse))
+              for st in strategies)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for st in strategies:
+            for key, h in st.host.items():
+                st.dev[key].copy_(h, non_blocking=True)
+        step()
+        for st in strategies:
+            for r in range(cfg.cp):
+                st.out_host[r].copy_(st.out[r], non_blocking=True)
+                st.lse_host[r].copy_(st.lse[r], non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * flops_step / e2e_s / 1e12
+
+    for st in strategies:
+        e = st.err.cpu().tolist()
+        if e[0] != 0:
+            raise RuntimeError(f"device check failed: {cp.cpthd_status_string(e[0])} ({e})")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "T": int(sum(cfg.lengths)), "docs": len(cfg.lengths), "Hq": cfg.hq,
+                       "Hkv": cfg.hkv, "d": cfg.d, "cp_size": cfg.cp, "strategies": list(cfg.strategies),
+                       "ranks_per_step": n_ranks, "flops_per_step": flops_step,
+                       "l2": "flushed between timed steps (256 MB write, untimed)",
+                       "parallelism": f"replicas{world}"},
+            "per_strategy": per_strategy,
+            "reorder": {"GB/s": round(reorder_bytes * args.steps / (prep_total_ms * 1e-3) / 1e9, 2),
+                        "bytes_per_step": reorder_bytes,
+                        "note": "partition + Q/ids reorder launches, timed together per rank"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "thd_causal_attn_fwd (timed per call: tile metadata + attention)",
+                         "peak_source": f"{peak_src} bf16_tflops (burst)"},
+            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": Strategy.LAUNCHES_PER_RANK * n_ranks * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# the float64 oracle on host cores
+# ----------------------------------------------------------------------------
+def _oracle_rank(cfg, strategy, r, cache):
+    from oracle import attention as A
+    from oracle import partition as P
+    if strategy not in cache:
+        cache[strategy] = W.make_attn_inputs(cfg, strategy)
+    inp = cache[strategy]
+    lay = inp.layout
+    t0 = time.perf_counter()
+    idx = np.asarray(P.partition_index(strategy, lay.cu_seqlens_padded.tolist(), cfg.cp, r), dtype=np.int64)
+    q_loc = inp.q[torch.from_numpy(idx)]
+    A.attention_fwd(q_loc, inp.k, inp.v, lay.cu_seqlens, lay.cu_seqlens_padded, idx)
+    dt = time.perf_counter() - t0
+    return dt, 4.0 * cfg.d * cfg.hq * rank_pairs(idx, lay)
+
+
+def cpu_baseline(cfg, seconds):
+    """Time the oracle as it stands on a bounded sample: whole rank slices in
+    (strategy, rank) order until about ``seconds`` of CPU work."""
+    cache = {}
+    t_sum, f_sum, done = 0.0, 0.0, []
+    for s in cfg.strategies:
+        for r in range(cfg.cp):
+            dt, f = _oracle_rank(cfg, s, r, cache)
+            t_sum += dt
+            f_sum += f
+            done.append(f"{s}:{r}")
+            if t_sum >= seconds:
+                break
+        if t_sum >= seconds:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(f_sum / t_sum / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{cfg.name}: rank slices {','.join(done)} (all heads, float64 numpy), {t_sum:.1f} s"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = W.CONFIG_BY_NAME[args.workload]
+    order = [(s, r) for s in cfg.strategies for r in range(cfg.cp)]
+    cache = {}
+    for i in range(args.warmup):
+        _oracle_rank(cfg, *order[i % len(order)], cache)
+    t_sum, f_sum = 0.0, 0.0
+    for i in range(args.steps):
+        dt, f = _oracle_rank(cfg, *order[i % len(order)], cache)
+        t_sum += dt
+        f_sum += f
+    value = f_sum / t_sum / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = f"{cfg.name}: one rank slice per step, cycling {len(order)} (strategy, rank) slices, float64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_sum / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "T": int(sum(cfg.lengths)), "Hq": cfg.hq, "Hkv": cfg.hkv, "d": cfg.d,
+                   "cp_size": cfg.cp, "strategies": list(cfg.strategies)},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.CONFIG_BY_NAME))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "cuda":
+        print("note: --warmup below 3 is not a valid measurement", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

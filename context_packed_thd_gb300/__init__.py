@@ -1,0 +1,204 @@
+"""Python binding of libcpthd (context-parallel causal attention over packed THD).
+
+The functions keep the C ABI's names (include/cpthd.h) and only marshal
+arguments: torch tensors in, device pointers and the current CUDA stream out.
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback. Importing the package builds libcpthd.so in-tree when
+it is missing or stale (nvcc, sm_103a) and fails loudly when it cannot.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+__all__ = [
+    "DUAL_CHUNK_SWAP", "NO_LOAD_BALANCE", "CpthdError", "LIB_PATH", "lib",
+    "cpthd_status_string", "cp_local_tokens", "cp_partition_index", "cp_reorder", "cp_reorder_multi",
+    "thd_causal_attn_workspace_size", "thd_causal_attn_fwd", "get_batch_on_this_cp_rank", "strategy_code",
+]
+
+DUAL_CHUNK_SWAP = 0
+NO_LOAD_BALANCE = 1
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcpthd.so")
+
+
+def _load_library():
+    """Load libcpthd.so, building it in-tree with nvcc on first use. There is
+    no fallback: without the library (or nvcc to build it) the import fails."""
+    from . import build as _build
+    try:
+        _build.build()
+    except Exception as e:  # no nvcc, compile error ...
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libcpthd.so is missing and could not be built: {e}") from e
+    return ctypes.CDLL(LIB_PATH)
+
+
+lib = _load_library()
+
+_i32 = ctypes.c_int
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_f32 = ctypes.c_float
+_sz = ctypes.c_size_t
+
+lib.cpthd_status_string.argtypes = [_i32]
+lib.cpthd_status_string.restype = ctypes.c_char_p
+lib.cp_local_tokens.argtypes = [_i32, _i64, _i32, ctypes.POINTER(_i64)]
+lib.cp_local_tokens.restype = _i32
+lib.cp_partition_index.argtypes = [_i32, _vp, _i32, _i64, _i32, _i32, _vp, _vp, _vp]
+lib.cp_partition_index.restype = _i32
+lib.cp_reorder.argtypes = [_vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp]
+lib.cp_reorder.restype = _i32
+lib.cp_reorder_multi.argtypes = [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_i64), _i64, _vp,
+                                 _i64, _vp, _vp]
+lib.cp_reorder_multi.restype = _i32
+lib.thd_causal_attn_workspace_size.argtypes = [_i64, _i32, _i32, _i32, ctypes.POINTER(_sz)]
+lib.thd_causal_attn_workspace_size.restype = _i32
+lib.thd_causal_attn_fwd.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _f32, _vp,
+                                    _vp, _vp, _sz, _vp, _vp]
+lib.thd_causal_attn_fwd.restype = _i32
+
+
+class CpthdError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {cpthd_status_string(status)} (status {status})")
+
+
+def cpthd_status_string(status: int) -> str:
+    return lib.cpthd_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise CpthdError(status, where)
+
+
+def strategy_code(strategy) -> int:
+    if isinstance(strategy, str):
+        s = strategy.lower()
+        if s in ("dcs", "dual_chunk_swap"):
+            return DUAL_CHUNK_SWAP
+        if s in ("nlb", "no_load_balance"):
+            return NO_LOAD_BALANCE
+        raise ValueError(f"unknown strategy {strategy!r}")
+    return int(strategy)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libcpthd takes CUDA tensors only")
+
+
+def cp_local_tokens(strategy, T: int, cp_size: int) -> int:
+    out = _i64(0)
+    _check(lib.cp_local_tokens(strategy_code(strategy), int(T), int(cp_size), ctypes.byref(out)), "cp_local_tokens")
+    return int(out.value)
+
+
+def cp_partition_index(strategy, cu_seqlens_padded: torch.Tensor, T: int, cp_size: int, rank: int,
+                       out: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """int32 physical indices owned by ``rank`` (rank = -1: all ranks, rank-major)."""
+    _need_cuda(cu_seqlens_padded, out, err)
+    assert cu_seqlens_padded.dtype == torch.int32 and cu_seqlens_padded.is_contiguous()
+    n = cp_local_tokens(strategy, T, cp_size) * (cp_size if rank < 0 else 1)
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=cu_seqlens_padded.device)
+    assert out.numel() >= n and out.dtype == torch.int32
+    _check(lib.cp_partition_index(strategy_code(strategy), _ptr(cu_seqlens_padded), cu_seqlens_padded.numel() - 1,
+                                  int(T), int(cp_size), int(rank), _ptr(out), _ptr(err), _stream(stream)),
+           "cp_partition_index")
+    return out
+
+
+def cp_reorder(src: torch.Tensor, idx: torch.Tensor, out: Optional[torch.Tensor] = None,
+               err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[i] = src[idx[i]] along dim 0, bit exact."""
+    _need_cuda(src, idx, out, err)
+    assert src.is_contiguous() and idx.dtype == torch.int32 and idx.is_contiguous()
+    if out is None:
+        out = torch.empty((idx.numel(),) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    rb = int(src[0].numel() * src.element_size()) if src.dim() > 1 else src.element_size()
+    _check(lib.cp_reorder(_ptr(src), src.shape[0], rb, _ptr(idx), idx.numel(), _ptr(out), _ptr(err),
+                          _stream(stream)), "cp_reorder")
+    return out
+
+
+def cp_reorder_multi(srcs: Sequence[torch.Tensor], idx: torch.Tensor, outs=None,
+                     err: Optional[torch.Tensor] = None, stream=None):
+    """Gather several tensors (same row count) by one index list in one launch."""
+    srcs = list(srcs)
+    _need_cuda(idx, err, *srcs)
+    n = len(srcs)
+    rows = srcs[0].shape[0]
+    assert all(s.shape[0] == rows and s.is_contiguous() for s in srcs)
+    if outs is None:
+        outs = [torch.empty((idx.numel(),) + tuple(s.shape[1:]), dtype=s.dtype, device=s.device) for s in srcs]
+    sp = (_vp * n)(*[s.data_ptr() for s in srcs])
+    dp = (_vp * n)(*[o.data_ptr() for o in outs])
+    rb = (_i64 * n)(*[int(s[0].numel() * s.element_size()) if s.dim() > 1 else s.element_size() for s in srcs])
+    _check(lib.cp_reorder_multi(n, sp, dp, rb, rows, _ptr(idx), idx.numel(), _ptr(err), _stream(stream)),
+           "cp_reorder_multi")
+    return outs
+
+
+def thd_causal_attn_workspace_size(t_local: int, Hq: int, Hkv: int, d: int) -> int:
+    out = _sz(0)
+    _check(lib.thd_causal_attn_workspace_size(int(t_local), int(Hq), int(Hkv), int(d), ctypes.byref(out)),
+           "thd_causal_attn_workspace_size")
+    return int(out.value)
+
+
+def thd_causal_attn_fwd(q_slice_idx: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                        cu_seqlens: torch.Tensor, cu_seqlens_padded: Optional[torch.Tensor] = None,
+                        softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                        lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        err: Optional[torch.Tensor] = None, stream=None):
+    """Causal THD attention of a rank's query slice q [t_local, Hq, d] against
+    the full k, v [T, Hkv, d]. Returns (out bf16 [t_local, Hq, d], lse fp32 [Hq, t_local])."""
+    _need_cuda(q_slice_idx, q, k, v, cu_seqlens, cu_seqlens_padded, out, lse, workspace, err)
+    t_local, Hq, d = q.shape
+    T, Hkv, _ = k.shape
+    for t in (q, k, v):
+        assert t.dtype == torch.bfloat16 and t.is_contiguous()
+    assert q_slice_idx.dtype == torch.int32 and q_slice_idx.numel() == t_local
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, t_local), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(thd_causal_attn_workspace_size(t_local, Hq, Hkv, d), dtype=torch.uint8,
+                                device=q.device)
+    _check(lib.thd_causal_attn_fwd(_ptr(q_slice_idx), t_local, _ptr(q), _ptr(k), _ptr(v), T, _ptr(cu_seqlens),
+                                   _ptr(cu_seqlens_padded), cu_seqlens.numel() - 1, Hq, Hkv, d,
+                                   float(softmax_scale) if softmax_scale else 0.0, _ptr(out), _ptr(lse),
+                                   _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)),
+           "thd_causal_attn_fwd")
+    return out, lse
+
+
+def get_batch_on_this_cp_rank(cu_seqlens_padded: torch.Tensor, *tensors: torch.Tensor, cp_size: int, rank: int,
+                              strategy=DUAL_CHUNK_SWAP, err: Optional[torch.Tensor] = None):
+    """Slice THD tensors (input_ids, labels, position_ids, activations ...)
+    to ``rank``'s tokens in one reorder launch. Returns (idx, [slices])."""
+    T = int(tensors[0].shape[0])
+    idx = cp_partition_index(strategy, cu_seqlens_padded, T, cp_size, rank, err=err)
+    outs = cp_reorder_multi(tensors, idx, err=err) if tensors else []
+    return idx, outs

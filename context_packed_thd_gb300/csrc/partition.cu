@@ -1,0 +1,99 @@
+// Partition index kernels: which physical THD tokens a context-parallel rank
+// owns.
+//
+// TransformerEngine PR #3221 ("Why", "What changed"): the default
+// DualChunkSwap partition cuts every document into 2*cp_size chunks and
+// rank r owns chunks r and 2*cp_size-1-r (the head-tail split, torchtitan
+// PR #2144 "Summary"); NO_LOAD_BALANCE cuts the complete physical buffer into
+// cp_size contiguous chunks, rank-major. Within a DualChunkSwap rank the
+// documents keep pack order and chunk r precedes chunk 2*cp_size-1-r, so the
+// rank-local offsets are cu_seqlens_padded / cp_size: output position t is
+// found by a binary search over those local offsets.
+#include "common.cuh"
+
+namespace cpthd {
+
+__global__ void validate_offsets_kernel(const int32_t* __restrict__ cup, int num_docs, long long T,
+                                        int cp, int dcs, int32_t* err) {
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j <= num_docs; j += gridDim.x * blockDim.x) {
+    int32_t a = cup[j];
+    if (j == 0 && a != 0) record_error(err, CPTHD_ERR_BAD_OFFSETS, 0);
+    if (j == num_docs && a != T) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
+    if (j < num_docs) {
+      int32_t b = cup[j + 1];
+      if (b < a) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
+      else if (dcs && ((b - a) % (2 * cp)) != 0) record_error(err, CPTHD_ERR_NOT_DIVISIBLE, j);
+    }
+  }
+}
+
+__global__ void dual_chunk_swap_index_kernel(const int32_t* __restrict__ cup, int num_docs, int cp,
+                                             int rank, long long t_local, long long total,
+                                             int32_t* __restrict__ idx) {
+  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
+       o += (long long)gridDim.x * blockDim.x) {
+    int r = rank;
+    long long t = o;
+    if (rank < 0) { r = static_cast<int>(o / t_local); t = o - (long long)r * t_local; }
+    // local offsets lp[j] = cup[j] / cp; find the document holding local slot t
+    int lo = 0, hi = num_docs;
+    while (hi - lo > 1) {
+      int mid = (lo + hi) >> 1;
+      if (static_cast<long long>(__ldg(cup + mid) / cp) <= t) lo = mid; else hi = mid;
+    }
+    long long start = __ldg(cup + lo);
+    long long chunk = (static_cast<long long>(__ldg(cup + lo + 1)) - start) / (2 * cp);
+    long long u = t - start / cp;
+    long long p = (u < chunk) ? start + r * chunk + u
+                              : start + (2LL * cp - 1 - r) * chunk + (u - chunk);
+    idx[o] = static_cast<int32_t>(p);
+  }
+}
+
+__global__ void no_load_balance_index_kernel(int rank, long long t_local, long long total,
+                                             int32_t* __restrict__ idx) {
+  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
+       o += (long long)gridDim.x * blockDim.x) {
+    long long p = (rank < 0) ? o : rank * t_local + o;
+    idx[o] = static_cast<int32_t>(p);
+  }
+}
+
+}  // namespace cpthd
+
+extern "C" int cp_local_tokens(int strategy, int64_t T, int cp_size, int64_t* t_local_host) {
+  if (t_local_host == nullptr || cp_size < 1 || T < 0) return CPTHD_ERR_INVALID_ARG;
+  if (strategy != CPTHD_DUAL_CHUNK_SWAP && strategy != CPTHD_NO_LOAD_BALANCE) return CPTHD_ERR_INVALID_ARG;
+  if (T % cp_size != 0) return CPTHD_ERR_NOT_DIVISIBLE;
+  *t_local_host = T / cp_size;
+  return CPTHD_OK;
+}
+
+extern "C" int cp_partition_index(int strategy, const int32_t* cu_seqlens_padded_dev, int num_docs,
+                                  int64_t T, int cp_size, int rank, int32_t* idx_out_dev,
+                                  int32_t* err_dev, cpthd_stream_t stream) {
+  int64_t t_local = 0;
+  int st = cp_local_tokens(strategy, T, cp_size, &t_local);
+  if (st != CPTHD_OK) return st;
+  if (rank < -1 || rank >= cp_size) return CPTHD_ERR_INVALID_ARG;
+  if (num_docs < 0 || T > INT32_MAX) return CPTHD_ERR_INVALID_ARG;
+  if (cu_seqlens_padded_dev == nullptr) return CPTHD_ERR_INVALID_ARG;
+  const long long total = (rank < 0) ? (long long)cp_size * t_local : t_local;
+  if (total > 0 && idx_out_dev == nullptr) return CPTHD_ERR_INVALID_ARG;
+  if (total > 0 && num_docs == 0) return CPTHD_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int dcs = (strategy == CPTHD_DUAL_CHUNK_SWAP);
+  cpthd::validate_offsets_kernel<<<cpthd::grid_for(num_docs + 1, 256, 64), 256, 0, s>>>(
+      cu_seqlens_padded_dev, num_docs, T, cp_size, dcs, err_dev);
+  CPTHD_TRY_CUDA(cudaGetLastError());
+  if (total == 0) return CPTHD_OK;
+  const int grid = cpthd::grid_for(total, 256, 152 * 16);
+  if (dcs) {
+    cpthd::dual_chunk_swap_index_kernel<<<grid, 256, 0, s>>>(cu_seqlens_padded_dev, num_docs, cp_size,
+                                                             rank, t_local, total, idx_out_dev);
+  } else {
+    cpthd::no_load_balance_index_kernel<<<grid, 256, 0, s>>>(rank, t_local, total, idx_out_dev);
+  }
+  CPTHD_TRY_CUDA(cudaGetLastError());
+  return CPTHD_OK;
+}

@@ -1,0 +1,175 @@
+// Reorder (row gather) kernels: dst[i, :] = src[idx[i], :], bit exact.
+//
+// This is the slicing of THD tensors into a context-parallel rank's token
+// order (TransformerEngine PR #3221, "How to use": get_batch_on_this_cp_rank
+// over input_ids, labels, position_ids; the same gather applies to
+// activations). It is a pure copy, bound by HBM bandwidth for wide rows and
+// by launch latency for the 8-byte id rows.
+//
+// Layout: one warp copies one row per step; its lanes move 16-byte vectors
+// (8- or 4-byte when the row or a base pointer is less aligned, bytes
+// otherwise) with UNROLL independent loads in flight before the stores, so
+// the SMs keep enough bytes outstanding to cover HBM latency. Narrow rows
+// (fewer than 32 vectors) use one thread per vector instead. Loads and stores
+// use the streaming cache hints: every byte is touched once.
+#include "common.cuh"
+
+namespace cpthd {
+
+struct ReorderTensor {
+  const void* src;
+  void* dst;
+  long long row_bytes;
+  int vec;  // bytes per vector: 16, 8, 4 or 1
+};
+
+struct ReorderBatch {
+  ReorderTensor t[8];
+};
+
+template <typename V>
+__device__ __forceinline__ V load_stream(const V* p) { return __ldcs(p); }
+template <>
+__device__ __forceinline__ uint8_t load_stream<uint8_t>(const uint8_t* p) { return *p; }
+template <typename V>
+__device__ __forceinline__ void store_stream(V* p, V v) { __stcs(p, v); }
+template <>
+__device__ __forceinline__ void store_stream<uint8_t>(uint8_t* p, uint8_t v) { *p = v; }
+
+constexpr int kUnroll = 4;
+
+template <typename V>
+__device__ __forceinline__ void gather_wide(const V* __restrict__ src, long long src_rows, long long vpr,
+                                            const int32_t* __restrict__ idx, long long n_rows,
+                                            V* __restrict__ dst, int32_t* err, long long warp,
+                                            long long nwarps, int lane) {
+  for (long long row = warp; row < n_rows; row += nwarps) {
+    const int32_t s = __ldg(idx + row);
+    if (s < 0 || s >= src_rows) {
+      if (lane == 0) record_error(err, CPTHD_ERR_INDEX_RANGE, row);
+      continue;
+    }
+    const V* sp = src + static_cast<long long>(s) * vpr;
+    V* dp = dst + row * vpr;
+    long long c = lane;
+    for (; c + (kUnroll - 1) * 32 < vpr; c += kUnroll * 32) {
+      V tmp[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) tmp[u] = load_stream(sp + c + u * 32);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) store_stream(dp + c + u * 32, tmp[u]);
+    }
+    for (; c < vpr; c += 32) store_stream(dp + c, load_stream(sp + c));
+  }
+}
+
+template <typename V>
+__device__ __forceinline__ void gather_narrow(const V* __restrict__ src, long long src_rows, int vpr,
+                                              const int32_t* __restrict__ idx, long long n_rows,
+                                              V* __restrict__ dst, int32_t* err, long long tid,
+                                              long long nthreads) {
+  const long long total = n_rows * vpr;
+  for (long long v = tid; v < total; v += nthreads) {
+    const long long row = (vpr == 1) ? v : v / vpr;
+    const int col = static_cast<int>(v - row * vpr);
+    const int32_t s = __ldg(idx + row);
+    if (s < 0 || s >= src_rows) {
+      if (col == 0) record_error(err, CPTHD_ERR_INDEX_RANGE, row);
+      continue;
+    }
+    dst[v] = src[static_cast<long long>(s) * vpr + col];
+  }
+}
+
+template <typename V>
+__device__ __forceinline__ void gather_one(const ReorderTensor& t, long long src_rows,
+                                           const int32_t* idx, long long n_rows, int32_t* err) {
+  const long long vpr = t.row_bytes / static_cast<long long>(sizeof(V));
+  const V* src = static_cast<const V*>(t.src);
+  V* dst = static_cast<V*>(t.dst);
+  if (vpr >= 32) {
+    const long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    gather_wide<V>(src, src_rows, vpr, idx, n_rows, dst, err, warp, nwarps, threadIdx.x & 31);
+  } else {
+    const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    const long long nthreads = (long long)gridDim.x * blockDim.x;
+    gather_narrow<V>(src, src_rows, static_cast<int>(vpr), idx, n_rows, dst, err, tid, nthreads);
+  }
+}
+
+// blockIdx.y selects the tensor of the batch.
+__global__ void __launch_bounds__(256) reorder_kernel(ReorderBatch batch, long long src_rows,
+                                                      const int32_t* __restrict__ idx, long long n_rows,
+                                                      int32_t* err) {
+  const ReorderTensor& t = batch.t[blockIdx.y];
+  if (t.row_bytes == 0) return;
+  switch (t.vec) {
+    case 16: gather_one<uint4>(t, src_rows, idx, n_rows, err); break;
+    case 8: gather_one<uint2>(t, src_rows, idx, n_rows, err); break;
+    case 4: gather_one<uint32_t>(t, src_rows, idx, n_rows, err); break;
+    default: gather_one<uint8_t>(t, src_rows, idx, n_rows, err); break;
+  }
+}
+
+static int vector_bytes(const void* src, const void* dst, long long row_bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
+                      static_cast<uintptr_t>(row_bytes);
+  if ((a & 15) == 0) return 16;
+  if ((a & 7) == 0) return 8;
+  if ((a & 3) == 0) return 4;
+  return 1;
+}
+
+static int launch_reorder(int n, const void* const* src, void* const* dst, const int64_t* row_bytes,
+                          int64_t src_rows, const int32_t* idx, int64_t n_rows, int32_t* err,
+                          cudaStream_t s) {
+  if (n < 1 || n > 8 || src_rows < 0 || n_rows < 0) return CPTHD_ERR_INVALID_ARG;
+  if (src_rows > INT32_MAX) return CPTHD_ERR_INVALID_ARG;
+  ReorderBatch b{};
+  long long max_bytes = 0;
+  for (int i = 0; i < n; ++i) {
+    if (row_bytes[i] < 0) return CPTHD_ERR_INVALID_ARG;
+    if (row_bytes[i] > 0 && n_rows > 0 && (src[i] == nullptr || dst[i] == nullptr)) return CPTHD_ERR_INVALID_ARG;
+    b.t[i].src = src[i];
+    b.t[i].dst = dst[i];
+    b.t[i].row_bytes = row_bytes[i];
+    b.t[i].vec = vector_bytes(src[i], dst[i], row_bytes[i]);
+    max_bytes = row_bytes[i] > max_bytes ? row_bytes[i] : max_bytes;
+  }
+  if (n_rows == 0 || max_bytes == 0) return CPTHD_OK;
+  if (idx == nullptr) return CPTHD_ERR_INVALID_ARG;
+  // a warp per row for wide rows, a thread per vector for narrow rows;
+  // capped at 8 resident 256-thread blocks on each of the 152 SMs
+  long long work = 0;
+  for (int i = 0; i < n; ++i) {
+    const long long vpr = b.t[i].row_bytes / b.t[i].vec;
+    const long long w = (vpr >= 32) ? n_rows * 32 : n_rows * vpr;
+    work = w > work ? w : work;
+  }
+  const int grid = grid_for(work, 256, 152 * 8);
+  dim3 g(grid, n);
+  reorder_kernel<<<g, 256, 0, s>>>(b, src_rows, idx, n_rows, err);
+  CPTHD_TRY_CUDA(cudaGetLastError());
+  return CPTHD_OK;
+}
+
+}  // namespace cpthd
+
+extern "C" int cp_reorder(const void* src_dev, int64_t src_rows, int64_t row_bytes, const int32_t* idx_dev,
+                          int64_t n_rows, void* dst_dev, int32_t* err_dev, cpthd_stream_t stream) {
+  const void* srcs[1] = {src_dev};
+  void* dsts[1] = {dst_dev};
+  const int64_t rb[1] = {row_bytes};
+  return cpthd::launch_reorder(1, srcs, dsts, rb, src_rows, idx_dev, n_rows, err_dev,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int cp_reorder_multi(int n_tensors, const void* const* src_dev_host, void* const* dst_dev_host,
+                                const int64_t* row_bytes_host, int64_t src_rows, const int32_t* idx_dev,
+                                int64_t n_rows, int32_t* err_dev, cpthd_stream_t stream) {
+  if (src_dev_host == nullptr || dst_dev_host == nullptr || row_bytes_host == nullptr)
+    return CPTHD_ERR_INVALID_ARG;
+  return cpthd::launch_reorder(n_tensors, src_dev_host, dst_dev_host, row_bytes_host, src_rows, idx_dev,
+                               n_rows, err_dev, reinterpret_cast<cudaStream_t>(stream));
+}

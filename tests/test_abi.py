@@ -1,0 +1,86 @@
+"""The C ABI without a GPU: libcpthd.so loads, exports every entry point
+include/cpthd.h declares, and its host-only calls validate their arguments
+(no kernel is launched by any call in this file)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names += re.findall(r"CPTHD_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def cp():
+    from context_packed_thd_gb300 import build
+    build.build()
+    import context_packed_thd_gb300 as cp
+    return cp
+
+
+def test_every_declared_symbol_is_exported(cp):
+    names = _declared()
+    assert {"cp_partition_index", "cp_reorder", "cp_reorder_multi", "thd_causal_attn_fwd",
+            "thd_causal_attn_workspace_size", "cp_local_tokens", "cpthd_status_string"} <= set(names)
+    raw = ctypes.CDLL(cp.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_binding_names_match_abi(cp):
+    for n in _declared():
+        assert callable(getattr(cp, n)), n
+
+
+def test_local_tokens(cp):
+    assert cp.cp_local_tokens("dcs", 132, 2) == 66
+    assert cp.cp_local_tokens("nlb", 131072, 16) == 8192
+    with pytest.raises(cp.CpthdError) as e:
+        cp.cp_local_tokens("nlb", 130, 4)
+    assert e.value.status == -2
+    with pytest.raises(cp.CpthdError) as e:
+        cp.cp_local_tokens("nlb", 128, 0)
+    assert e.value.status == -1
+    with pytest.raises(cp.CpthdError):
+        cp.cp_local_tokens(7, 128, 2)
+
+
+def test_status_strings(cp):
+    for s in range(0, -10, -1):
+        assert cp.cpthd_status_string(s) not in ("", "unknown status")
+    assert cp.cpthd_status_string(-99) == "unknown status"
+
+
+def test_host_validation_launches_nothing(cp):
+    L = cp.lib
+    st = cp._i32
+    # rank out of range, bad cp_size, null offsets: rejected on the host
+    assert L.cp_partition_index(0, ctypes.c_void_p(16), 1, 8, 2, 5, ctypes.c_void_p(16), None, None) == -1
+    assert L.cp_partition_index(0, None, 1, 8, 2, 0, ctypes.c_void_p(16), None, None) == -1
+    assert L.cp_partition_index(1, ctypes.c_void_p(16), 1, 9, 2, 0, ctypes.c_void_p(16), None, None) == -2
+    # reorder: too many tensors, negative rows
+    assert L.cp_reorder(ctypes.c_void_p(16), -1, 16, ctypes.c_void_p(16), 4, ctypes.c_void_p(16), None, None) == -1
+    # attention: unsupported head dim, GQA mismatch, missing workspace
+    f = L.thd_causal_attn_fwd
+    p = ctypes.c_void_p(256)
+    assert f(p, 4, p, p, p, 8, p, None, 1, 2, 2, 96, 0.0, p, p, p, 1 << 20, None, None) == -3
+    assert f(p, 4, p, p, p, 8, p, None, 1, 3, 2, 64, 0.0, p, p, p, 1 << 20, None, None) == -3
+    assert f(p, 4, p, p, p, 8, p, None, 1, 2, 2, 64, 0.0, p, p, None, 0, None, None) == -4
+    # empty slice: nothing to do
+    assert f(None, 0, None, None, None, 8, None, None, 1, 2, 2, 64, 0.0, None, None, None, 0, None, None) == 0
+
+
+def test_workspace_size(cp):
+    a = cp.thd_causal_attn_workspace_size(128, 8, 8, 128)
+    b = cp.thd_causal_attn_workspace_size(129, 8, 8, 128)
+    assert 0 < a < b
+    assert cp.thd_causal_attn_workspace_size(0, 8, 8, 128) >= 0

@@ -1,0 +1,65 @@
+"""GPU partition index vs the oracle: bit exact, every workload, every rank,
+both strategies; rank = -1 gives all ranks rank-major; device-side checks of
+malformed offsets land in the error word."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import partition as P
+import workloads as W
+from gpu_common import cuda_or_skip, load_lib, new_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("cfg", W.CONFIGS, ids=lambda c: c.name)
+def test_partition_every_config(cfg):
+    dev = cuda_or_skip(); cp = load_lib()
+    for s in cfg.strategies:
+        lay = W.layout_for(cfg, s)
+        cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
+        err = new_err(dev)
+        for r in range(cfg.cp):
+            got = cp.cp_partition_index(s, cup, lay.T, cfg.cp, r, err=err).cpu().numpy()
+            ref = np.asarray(P.partition_index(s, lay.cu_seqlens_padded.tolist(), cfg.cp, r), dtype=np.int32)
+            assert np.array_equal(got, ref), (s, r)
+        allr = cp.cp_partition_index(s, cup, lay.T, cfg.cp, -1, err=err).cpu().numpy()
+        ref = np.concatenate([P.partition_index(s, lay.cu_seqlens_padded.tolist(), cfg.cp, r)
+                              for r in range(cfg.cp)]).astype(np.int32)
+        assert np.array_equal(allr, ref)
+        assert err.cpu().tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("cpsize", [1, 2, 3, 5, 8])
+def test_partition_random_packs(cpsize):
+    dev = cuda_or_skip(); cp = load_lib()
+    rng = np.random.default_rng(cpsize)
+    for _ in range(8):
+        lay = W.random_layout(rng, int(rng.integers(1, 40)), 300, 2 * cpsize, allow_empty=True)
+        cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
+        for s in ("dcs", "nlb"):
+            if lay.T % cpsize:
+                continue
+            for r in range(cpsize):
+                got = cp.cp_partition_index(s, cup, lay.T, cpsize, r).cpu().numpy()
+                ref = np.asarray(P.partition_index(s, lay.cu_seqlens_padded.tolist(), cpsize, r), dtype=np.int32)
+                assert np.array_equal(got, ref)
+
+
+def test_partition_device_checks():
+    dev = cuda_or_skip(); cp = load_lib()
+    # document 1 has padded length 6, not divisible by 2*cp_size = 4
+    cup = torch.tensor([0, 8, 14, 16], dtype=torch.int32, device=dev)
+    err = new_err(dev)
+    cp.cp_partition_index("dcs", cup, 16, 2, 0, err=err)
+    assert err.cpu().tolist() == [-2, 1]
+    # last offset differs from T
+    cup = torch.tensor([0, 8, 12], dtype=torch.int32, device=dev)
+    err = new_err(dev)
+    cp.cp_partition_index("nlb", cup, 16, 2, 1, err=err)
+    assert err.cpu().tolist()[0] == -6
+    # decreasing offsets
+    cup = torch.tensor([0, 8, 4, 16], dtype=torch.int32, device=dev)
+    err = new_err(dev)
+    cp.cp_partition_index("dcs", cup, 16, 2, 0, err=err)
+    assert err.cpu().tolist()[0] == -6
