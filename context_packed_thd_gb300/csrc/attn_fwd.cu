@@ -15,8 +15,9 @@
 //               then O += P_{i-1} V_{i-1} into the TMEM O accumulator.
 //  * warps 2..5 -- softmax: each thread owns one query row (its TMEM lane),
 //               reads S_i with tcgen05.ld, masks by the row's key interval
-//               [doc start, own position] (only on blocks that the tile's
-//               bounds do not cover fully), keeps the fp32 running max / sum
+//               [doc start, own position] clipped to the end of the tile
+//               interval the block belongs to (only on blocks that the
+//               tile's bounds do not cover fully), keeps the fp32 running max / sum
 //               in base 2, rescales O in TMEM only when the max grows by more
 //               than 2^8 (the result is exact either way), writes P as bf16
 //               into swizzled shared memory and hands it to the MMA lane.
@@ -249,7 +250,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     cur.init(tile_iv, n_iv);
     bool ok = true;
     for (int i = 0; i < n_blocks; ++i) {
+      // a block never reaches past its interval's end: the next interval may
+      // start inside it, and its keys must be counted there only
       const int kstart = cur.start;
+      const int kend = cur.end;
       cur.next();
       const int b = i & 1;
       if (!warp_wait(&s_full[b], (i >> 1) & 1, &abort_flag)) { ok = false; break; }
@@ -267,12 +271,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[b]);
 
-      const bool full = (kstart >= ti.max_lo) && (kstart + kBlockN - 1 <= ti.min_hi);
+      const int row_end = min(hi, kend);
+      const bool full = (kstart >= ti.max_lo) && (kstart + kBlockN - 1 <= min(ti.min_hi, kend));
       if (!full) {
 #pragma unroll
         for (int j = 0; j < kBlockN; ++j) {
           const int key = kstart + j;
-          if (key < lo || key > hi) s[j] = -INFINITY;
+          if (key < lo || key > row_end) s[j] = -INFINITY;
         }
       }
       float mx = s[0];
