@@ -168,17 +168,17 @@ class Strategy:
         rb = hq * d * 2 + 3 * 8
         self.reorder_bytes = tl * (2 * rb + 4)
 
-    # launches per rank: partition (offset check + index) 2, Q reorder 1,
-    # ids reorder 1, attention (doc check, tile metadata, tile order, attention) 4
-    LAUNCHES_PER_RANK = 8
+    # launches per rank: partition index 1, one reorder of Q and the three id
+    # tensors 1, attention (row-group metadata, group order, attention) 3
+    LAUNCHES_PER_RANK = 5
 
     def run_rank(self, cp, r, ev=None):
         d = self.dev
         if ev is not None:
             ev[0].record()
         cp.cp_partition_index(self.name, d["cup"], self.T, self.cpsize, r, out=self.idx[r], err=self.err)
-        cp.cp_reorder(d["q"], self.idx[r], out=self.q_loc[r], err=self.err)
-        cp.cp_reorder_multi([d["ids"], d["labels"], d["pos"]], self.idx[r], outs=self.ids_loc[r], err=self.err)
+        cp.cp_reorder_multi([d["q"], d["ids"], d["labels"], d["pos"]], self.idx[r],
+                            outs=[self.q_loc[r]] + self.ids_loc[r], err=self.err)
         if ev is not None:
             ev[1].record()
         cp.thd_causal_attn_fwd(self.idx[r], self.q_loc[r], d["k"], d["v"], d["cu"], d["cup"], out=self.out[r],
@@ -199,18 +199,22 @@ def run_cuda(args):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     cfg = W.CONFIG_BY_NAME[args.workload]
-    strategies = [Strategy(cp, cfg, s, dev) for s in cfg.strategies]
+    names = [s for s in cfg.strategies if args.strategy in (None, s)]
+    if not names:
+        raise SystemExit(f"workload {cfg.name} does not run strategy {args.strategy}")
+    strategies = [Strategy(cp, cfg, s, dev) for s in names]
+    ranks = list(range(cfg.cp)) if args.rank is None else [args.rank]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(evs=None):
         k = 0
         for st in strategies:
-            for r in range(cfg.cp):
+            for r in ranks:
                 st.run_rank(cp, r, None if evs is None else evs[k])
                 k += 1
 
-    n_ranks = cfg.cp * len(strategies)
+    n_ranks = len(ranks) * len(strategies)
     for _ in range(args.warmup):
         step()
         flush.zero_()
@@ -244,7 +248,7 @@ def run_cuda(args):
     total_ms = sum(step_ms)
     attn_ms = [[rank_ev[i][k][1].elapsed_time(rank_ev[i][k][2]) for k in range(n_ranks)] for i in range(args.steps)]
     prep_ms = [[rank_ev[i][k][0].elapsed_time(rank_ev[i][k][1]) for k in range(n_ranks)] for i in range(args.steps)]
-    flops_step = sum(sum(st.flops) for st in strategies)
+    flops_step = sum(st.flops[r] for st in strategies for r in ranks)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -256,25 +260,27 @@ def run_cuda(args):
     per_strategy = {}
     k = 0
     for st in strategies:
-        ms = med_attn[k:k + cfg.cp]
+        ms = med_attn[k:k + len(ranks)]
+        fl = [st.flops[r] for r in ranks]
+        pr = [st.pairs[r] for r in ranks]
         per_strategy[st.name] = {
             "attn_ms_per_rank_max": max(ms), "attn_ms_per_rank_min": min(ms),
-            "attn_tflops": sum(st.flops) / (sum(ms) * 1e-3) / 1e12,
-            "pairs_per_rank_max": max(st.pairs), "pairs_per_rank_min": min(st.pairs),
+            "attn_tflops": sum(fl) / (sum(ms) * 1e-3) / 1e12,
+            "pairs_per_rank_max": max(pr), "pairs_per_rank_min": min(pr),
         }
-        k += cfg.cp
+        k += len(ranks)
     attn_total_ms = sum(sum(x) for x in attn_ms)
     achieved = flops_step * args.steps / (attn_total_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    reorder_bytes = sum(st.reorder_bytes * cfg.cp for st in strategies)
+    reorder_bytes = sum(st.reorder_bytes * len(ranks) for st in strategies)
     prep_total_ms = sum(sum(x) for x in prep_ms)
 
     # ---- end to end: pinned host inputs -> step -> host results --------------
     e2e_steps = max(1, min(args.steps, 10))
     h2d = sum(sum(t.numel() * t.element_size() for t in st.host.values()) for st in strategies)
-    d2h = sum(sum(o.numel() * o.element_size() + l.numel() * l.element_size() for o, l in zip(st.out, st.lse))
-              for st in strategies)
+    d2h = sum(st.out[r].numel() * st.out[r].element_size() + st.lse[r].numel() * st.lse[r].element_size()
+              for st in strategies for r in ranks)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
@@ -283,7 +289,7 @@ def run_cuda(args):
                 st.dev[key].copy_(h, non_blocking=True)
         step()
         for st in strategies:
-            for r in range(cfg.cp):
+            for r in ranks:
                 st.out_host[r].copy_(st.out[r], non_blocking=True)
                 st.lse_host[r].copy_(st.lse[r], non_blocking=True)
         torch.cuda.synchronize()
@@ -311,15 +317,17 @@ def run_cuda(args):
             "config": {"workload": cfg.name, "T": int(sum(cfg.lengths)), "docs": len(cfg.lengths), "Hq": cfg.hq,
                        "Hkv": cfg.hkv, "d": cfg.d, "cp_size": cfg.cp, "strategies": list(cfg.strategies),
                        "ranks_per_step": n_ranks, "flops_per_step": flops_step,
+                       "subset": None if (args.strategy is None and args.rank is None)
+                       else {"strategy": args.strategy, "rank": args.rank},
                        "l2": "flushed between timed steps (256 MB write, untimed)",
                        "parallelism": f"replicas{world}"},
             "per_strategy": per_strategy,
             "reorder": {"GB/s": round(reorder_bytes * args.steps / (prep_total_ms * 1e-3) / 1e9, 2),
                         "bytes_per_step": reorder_bytes,
-                        "note": "partition + Q/ids reorder launches, timed together per rank"},
+                        "note": "partition index + one reorder launch of Q and the int64 ids, timed together per rank"},
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": "thd_causal_attn_fwd (timed per call: tile metadata + attention)",
+                         "kernel": "thd_causal_attn_fwd (timed per call: row-group metadata, group order, attention kernel)",
                          "peak_source": f"{peak_src} bf16_tflops (burst)"},
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
@@ -410,6 +418,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.CONFIG_BY_NAME))
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--strategy", choices=list(W.STRATEGIES), default=None,
+                    help="time one strategy only (profiling); the headline runs every strategy")
+    ap.add_argument("--rank", type=int, default=None,
+                    help="time one context-parallel rank only (profiling); the headline runs every rank")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "cuda":
         print("note: --warmup below 3 is not a valid measurement", file=sys.stderr)

@@ -6,25 +6,41 @@
 // buffer, documents isolated through cu_seqlens / cu_seqlens_padded. Output
 // O in bf16 and the natural-log LSE in fp32 ([Hq, t_local]).
 //
-// Kernel design (one CTA per (128-row query tile, query head)):
-//  * warp 0  -- TMA producer: Q tile once, then K and V 128-key blocks into a
-//               two-stage shared-memory ring (128-byte swizzle, the layout the
-//               UMMA descriptors read).
-//  * warp 1  -- owns the 512-column TMEM allocation; one lane issues the
-//               tcgen05 MMAs: S_i = Q K_i^T into one of two TMEM S buffers,
-//               then O += P_{i-1} V_{i-1} into the TMEM O accumulator.
-//  * warps 2..5 -- softmax: each thread owns one query row (its TMEM lane),
-//               reads S_i with tcgen05.ld, masks by the row's key interval
-//               [doc start, own position] clipped to the end of the tile
-//               interval the block belongs to (only on blocks that the
-//               tile's bounds do not cover fully), keeps the fp32 running max / sum
-//               in base 2, rescales O in TMEM only when the max grows by more
-//               than 2^8 (the result is exact either way), writes P as bf16
-//               into swizzled shared memory and hands it to the MMA lane.
-//               At the end it normalises O and writes out and LSE.
-// Key blocks start at the tile's interval starts (document starts), so
-// whole documents that a tile does not see are never loaded or multiplied.
-// The grid runs the tiles in decreasing-cost order.
+// Kernel design. A CTA owns two 128-row query tiles A and B that read the
+// same K/V blocks: one row tile under two query heads that share a KV head
+// (GQA group sizes divisible by 2), or two consecutive row tiles under one
+// head. Twelve warps in three warpgroups; warpgroup 0 gives registers to the
+// softmax warpgroups (setmaxnreg: 56 vs 224 per thread; 56*128 + 224*256 equals
+// the 168 * 384 the launch allocates):
+//  * warp 0      TMA producer: both Q tiles once, then K and V 128-key blocks
+//                into a two-stage shared-memory ring (128-byte swizzle, the
+//                layout the UMMA shared-memory descriptors read).
+//  * warp 1      owns the 512-column TMEM allocation (S_A, S_B, O_A, O_B);
+//                one lane issues the tcgen05 MMAs in the order
+//                  S_A(0), S_B(0), then per block j:
+//                  O_A += P_A(j) V_j, S_A(j+1), O_B += P_B(j) V_j, S_B(j+1)
+//                so that each softmax warpgroup works while the tensor core
+//                runs the other tile's two MMAs. P_x(j) is written by the
+//                softmax into the first 64 columns of S_x (bf16 pairs) and is
+//                read from TMEM by the MMA. Because MMAs complete in issue
+//                order, the commit that reports S_x(j+1) also reports that
+//                O_x += P_x(j) V_j is done, so the softmax may then rescale O_x
+//                and overwrite P_x without further waits.
+//  * warps 2-3   idle.
+//  * warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: each thread
+//                owns one query row (its TMEM lane). It reads S with one
+//                tcgen05.ld, masks by the row's key interval [document
+//                start, own position] clipped to the end of the block's
+//                interval (only on blocks the tile's bounds do not cover
+//                fully), keeps the fp32 running max / sum in base 2, rescales
+//                O in TMEM only when the max grows by more than 2^8 (exact
+//                either way), and writes P back into TMEM. At the end it
+//                normalises O and writes out and LSE.
+// Key blocks start at the group's interval starts (document starts), so
+// documents the group does not see are never loaded or multiplied. The grid
+// runs the groups in decreasing-cost order. Every wait is bounded; a wait
+// that times out makes the CTA drain its copies and MMAs, free TMEM, record
+// CPTHD_ERR_TIMEOUT and return.
 #include <cuda_bf16.h>
 
 #include "attn_meta.cuh"
@@ -35,22 +51,23 @@ namespace cpthd {
 
 using namespace sm100;
 
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 384;
+constexpr int kRegsControl = 56;   // warpgroup 0: producer, MMA issuer
+constexpr int kRegsSoftmax = 224;  // warpgroups 1 and 2
+static_assert(kRegsControl * 128 + kRegsSoftmax * 256 <= 168 * kAttnThreads, "register split exceeds the launch");
 constexpr int kStages = 2;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 256x
 
 template <int D>
 struct AttnSmem {
-  static constexpr int kChunk = kBlockM * 64 * 2;      // one 128-row x 64-column bf16 swizzle panel
+  static constexpr int kChunk = kBlockM * 64 * 2;  // one 128-row x 64-column bf16 swizzle panel
   static constexpr int kChunks = D / 64;
-  static constexpr int kQ = kChunks * kChunk;          // Q tile
-  static constexpr int kKV = kChunks * kChunk;         // one K or V block
-  static constexpr int kP = 2 * kChunk;                // P: 128 rows x 128 keys
-  static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQ;
+  static constexpr int kQ = kChunks * kChunk;      // one Q tile
+  static constexpr int kKV = kChunks * kChunk;     // one K or V block
+  static constexpr int kQOff = 0;                  // Q_A, Q_B
+  static constexpr int kKOff = 2 * kQ;
   static constexpr int kVOff = kKOff + kStages * kKV;
-  static constexpr int kPOff = kVOff + kStages * kKV;
-  static constexpr int kBytes = kPOff + kP;
+  static constexpr int kBytes = kVOff + kStages * kKV;
   // request at least this much so that one CTA holds an SM (TMEM is taken whole)
   static constexpr int kLaunchBytes = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
 };
@@ -58,7 +75,7 @@ struct AttnSmem {
 struct AttnParams {
   const int32_t* row_lo;
   const int32_t* row_hi;
-  const TileInfo* tile_info;
+  const GroupInfo* group_info;
   const int2* intervals;
   const int32_t* order;
   __nv_bfloat16* out;
@@ -66,12 +83,14 @@ struct AttnParams {
   long long t_local;
   int Hq;
   int Hkv;
-  int max_blocks;  // upper bound on blocks per tile, guards malformed metadata
+  int head_pairs;  // 1: tiles A/B = heads 2u, 2u+1 of one row tile; 0: row tiles 2g, 2g+1 of one head
+  int group_rows;  // 128 with head pairs, 256 with tile pairs
+  int max_blocks;  // upper bound on blocks per group, guards malformed metadata
   float scale_log2;
   int32_t* err;
 };
 
-// Walks the key blocks of a tile: interval by interval, 128 keys at a time.
+// Walks the key blocks of a group: interval by interval, 128 keys at a time.
 struct BlockCursor {
   const int2* iv;
   int n_iv;
@@ -112,23 +131,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sQ = smem + L::kQOff;
   uint8_t* sK = smem + L::kKOff;
   uint8_t* sV = smem + L::kVOff;
-  uint8_t* sP = smem + L::kPOff;
 
   __shared__ uint64_t q_full, k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
-  __shared__ uint64_t s_full[2], s_free[2], p_full, o_done, drain;
+  __shared__ uint64_t s_full[2], p_full[2], o_final, drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int units = p.head_pairs ? (p.Hq >> 1) : p.Hq;
   const int item = blockIdx.x;
-  const int tile = __ldg(p.order + item / p.Hq);
-  const int h = item % p.Hq;
-  const int kvh = h / (p.Hq / p.Hkv);
-  const TileInfo ti = p.tile_info[tile];
-  const int n_blocks = min(max(ti.n_blocks, 0), p.max_blocks);
-  const int2* tile_iv = p.intervals + static_cast<long long>(tile) * kBlockM;
-  const int n_iv = min(max(ti.n_intervals, 0), kBlockM);
+  const int group = __ldg(p.order + item / units);
+  const int unit = item % units;
+  const int head0 = p.head_pairs ? 2 * unit : unit;
+  const int kvh = head0 / (p.Hq / p.Hkv);
+  const GroupInfo gi = p.group_info[group];
+  const int n_blocks = min(max(gi.n_blocks, 0), p.max_blocks);
+  const int2* group_iv = p.intervals + static_cast<long long>(group) * p.group_rows;
+  const int n_iv = min(max(gi.n_intervals, 0), p.group_rows);
+  const long long group_row0 = static_cast<long long>(group) * p.group_rows;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -139,12 +160,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 4);
     }
-    mbar_init(&p_full, 4);
-    mbar_init(&o_done, 1);
+    mbar_init(&o_final, 1);
     mbar_init(&drain, 1);
     fence_mbar_init();
   }
@@ -156,19 +176,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t tmem_s0 = tmem;         // S buffers: columns [0,128) and [128,256)
-  const uint32_t tmem_o = tmem + 256;    // O accumulator: columns [256, 256 + D)
+  // columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D, 256+2D)
 
-  if (warp == 0) {
+  if (warp < 4) {
+   setmaxnreg_dec<kRegsControl>();
+   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_blocks > 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&q_full, L::kQ);
-      for (int c = 0; c < L::kChunks; ++c) tma_load_3d(sQ + c * L::kChunk, &tm_q, &q_full, c * 64, h, tile * kBlockM);
+      mbar_arrive_expect_tx(&q_full, 2 * L::kQ);
+      for (int x = 0; x < 2; ++x) {
+        const int qh = p.head_pairs ? head0 + x : head0;
+        const int qrow = static_cast<int>(group_row0) + (p.head_pairs ? 0 : x * kBlockM);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sQ + x * L::kQ + c * L::kChunk, &tm_q, &q_full, c * 64, qh, qrow);
+      }
       BlockCursor cur;
-      cur.init(tile_iv, n_iv);
+      cur.init(group_iv, n_iv);
       int issued = 0;
       for (int i = 0; i < n_blocks; ++i) {
         const int st = i & 1;
@@ -177,7 +203,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive_expect_tx(&k_full[st], L::kKV);
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(sK + st * L::kKV + c * L::kChunk, &tm_k, &k_full[st], c * 64, kvh, cur.start);
-        if (i >= kStages && !mbar_wait(&v_empty[st], par, &abort_flag)) { issued = 2 * i + 1; break; }
+        issued = 2 * i + 1;
+        if (i >= kStages && !mbar_wait(&v_empty[st], par, &abort_flag)) break;
         mbar_arrive_expect_tx(&v_full[st], L::kKV);
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(sV + st * L::kKV + c * L::kChunk, &tm_v, &v_full[st], c * 64, kvh, cur.start);
@@ -193,97 +220,122 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_blocks > 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kBlockM, D, 0, 1);
-      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV), p0 = smem_u32(sP);
-      bool ok = mbar_wait(&q_full, 0, &abort_flag);
-      tc_fence_after_sync();
-      for (int i = 0; ok && i <= n_blocks; ++i) {
-        if (i < n_blocks) {
-          const int st = i & 1, b = i & 1;
-          if (!mbar_wait(&k_full[st], (i >> 1) & 1, &abort_flag)) break;
-          if (i >= 2 && !mbar_wait(&s_free[b], ((i >> 1) + 1) & 1, &abort_flag)) break;
-          tc_fence_after_sync();
-          const uint32_t kb = k0 + st * L::kKV;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::kChunk + (kk & 3) * 32;
-            umma_ss(tmem_s0 + b * kBlockN, smem_desc_sw128(q0 + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                    kIdescS, kk > 0);
-          }
-          umma_commit(&s_full[b]);
-          umma_commit(&k_empty[st]);
+      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
+      // Descriptors differ only in their start-address field (bits 0-13,
+      // address >> 4), so each one is a base descriptor plus an offset >> 4;
+      // shared-memory addresses stay below 256 KB, so the field never carries.
+      const uint64_t dq = smem_desc_sw128(q0, 16, 1024);
+      const uint64_t dk = smem_desc_sw128(k0, 16, 1024);
+      const uint64_t dv = smem_desc_sw128(v0, L::kChunk, 1024);
+      auto issue_s = [&](int x, int j) {  // S_x = Q_x K_j^T
+        const uint32_t qoff = (x * L::kQ) >> 4, koff = ((j & 1) * L::kKV) >> 4;
+#pragma unroll 1
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + x * kBlockN, dq + qoff + off, dk + koff + off, kIdescS, kk > 0);
         }
-        if (i >= 1) {
-          const int j = i - 1, st = j & 1;
-          if (!mbar_wait(&v_full[st], (j >> 1) & 1, &abort_flag)) break;
-          if (!mbar_wait(&p_full, j & 1, &abort_flag)) break;
+      };
+      auto issue_pv = [&](int x, int j) {  // O_x += P_x V_j, P_x read from TMEM
+        const uint32_t voff = ((j & 1) * L::kKV) >> 4;
+#pragma unroll 1
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          umma_ts(tmem + 256 + x * D, tmem + x * kBlockN + kk * 8, dv + voff + ((kk * 16 * 128) >> 4), kIdescO,
+                  (j > 0 || kk > 0));
+        }
+      };
+      bool ok = mbar_wait(&q_full, 0, &abort_flag) && mbar_wait(&k_full[0], 0, &abort_flag);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_s(0, 0);
+        umma_commit(&s_full[0]);
+        issue_s(1, 0);
+        umma_commit(&s_full[1]);
+        umma_commit(&k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_blocks; ++j) {
+        const int st = j & 1;
+        const bool more = (j + 1 < n_blocks);
+        if (!mbar_wait(&v_full[st], (j >> 1) & 1, &abort_flag)) break;
+        if (!mbar_wait(&p_full[0], j & 1, &abort_flag)) break;
+        tc_fence_after_sync();
+        issue_pv(0, j);
+        if (more) {
+          if (!mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, &abort_flag)) break;
           tc_fence_after_sync();
-          const uint32_t vb = v0 + st * L::kKV;
-#pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            const uint32_t poff = (kk >> 2) * L::kChunk + (kk & 3) * 32;
-            umma_ss(tmem_o, smem_desc_sw128(p0 + poff, 16, 1024),
-                    smem_desc_sw128(vb + kk * 16 * 128, L::kChunk, 1024), kIdescO, (j > 0 || kk > 0));
-          }
-          umma_commit(&o_done);
-          umma_commit(&v_empty[st]);
+          issue_s(0, j + 1);
+          umma_commit(&s_full[0]);
+        }
+        if (!mbar_wait(&p_full[1], j & 1, &abort_flag)) break;
+        tc_fence_after_sync();
+        issue_pv(1, j);
+        umma_commit(&v_empty[st]);
+        if (more) {
+          issue_s(1, j + 1);
+          umma_commit(&s_full[1]);
+          umma_commit(&k_empty[(j + 1) & 1]);
         }
       }
+      umma_commit(&o_final);
       umma_commit(&drain);
       mbar_wait_drain(&drain, 0);
     }
+   }
   } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
-    const int quarter = warp & 3;
+    const int x = (warp - 4) >> 2;  // tile of this warpgroup
+    const int quarter = warp & 3;   // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;
-    const long long grow = static_cast<long long>(tile) * kBlockM + r;
+    const long long grow = group_row0 + (p.head_pairs ? 0 : x * kBlockM) + r;
+    const int qh = p.head_pairs ? head0 + x : head0;
     const int lo = p.row_lo[grow];
     const int hi = p.row_hi[grow];
     const bool valid = (grow < p.t_local) && (lo <= hi);
+    const int tmax_lo = gi.max_lo[x], tmin_hi = gi.min_hi[x];
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float m = -INFINITY, l = 0.f;
+    const uint32_t t_s = tmem + lane_off + x * kBlockN;
+    const uint32_t t_o = tmem + lane_off + 256 + x * D;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;  // running max of scale*log2(e)*s
+    float l = 0.f;
     BlockCursor cur;
-    cur.init(tile_iv, n_iv);
+    cur.init(group_iv, n_iv);
     bool ok = true;
-    for (int i = 0; i < n_blocks; ++i) {
+    for (int j = 0; j < n_blocks; ++j) {
       // a block never reaches past its interval's end: the next interval may
       // start inside it, and its keys must be counted there only
       const int kstart = cur.start;
       const int kend = cur.end;
       cur.next();
-      const int b = i & 1;
-      if (!warp_wait(&s_full[b], (i >> 1) & 1, &abort_flag)) { ok = false; break; }
+      if (!warp_wait(&s_full[x], j & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after_sync();
-      float s[kBlockN];
-#pragma unroll
-      for (int c = 0; c < kBlockN / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tmem_s0 + lane_off + b * kBlockN + c * 32, rr);
-        tmem_ld_wait(rr);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) s[c * 32 + j] = __uint_as_float(rr[j]) * p.scale_log2;
-      }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[b]);
-
+      uint32_t sr[kBlockN];
+      tmem_ld128(t_s, sr);
+      tmem_ld_wait128(sr);
       const int row_end = min(hi, kend);
-      const bool full = (kstart >= ti.max_lo) && (kstart + kBlockN - 1 <= min(ti.min_hi, kend));
+      const bool full = (kstart >= tmax_lo) && (kstart + kBlockN - 1 <= min(tmin_hi, kend));
       if (!full) {
 #pragma unroll
-        for (int j = 0; j < kBlockN; ++j) {
-          const int key = kstart + j;
-          if (key < lo || key > row_end) s[j] = -INFINITY;
+        for (int c = 0; c < kBlockN; ++c) {
+          const int key = kstart + c;
+          if (key < lo || key > row_end) sr[c] = __float_as_uint(-INFINITY);
         }
       }
-      float mx = s[0];
+      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
 #pragma unroll
-      for (int j = 1; j < kBlockN; ++j) mx = fmaxf(mx, s[j]);
-      const float m_new = fmaxf(m, mx);
+      for (int c = 4; c < kBlockN; c += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+      }
+      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
       const bool grow_o = (m != -INFINITY) && (m_new > m + kRescaleThreshold);
       float alpha = 1.f;
       if (m == -INFINITY) {
@@ -293,79 +345,69 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         l *= alpha;
         m = m_new;
       }
-      bool o_ready = false;
+      const float mref = (m == -INFINITY) ? 0.f : m;
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float e0 = ex2(fmaf(__uint_as_float(sr[64 * h2 + 2 * c]), sl2, -mref));
+          const float e1 = ex2(fmaf(__uint_as_float(sr[64 * h2 + 2 * c + 1]), sl2, -mref));
+          rs0 += e0;
+          rs1 += e1;
+          pk[c] = pack_bf16x2(e0, e1);
+        }
+        tmem_st32(t_s + 32 * h2, pk);
+      }
+      l += rs0 + rs1;
       if (__any_sync(0xffffffffu, grow_o)) {
-        if (i > 0) {
-          if (!warp_wait(&o_done, (i - 1) & 1, &abort_flag)) { ok = false; break; }
-          tc_fence_after_sync();
-          o_ready = true;
+        // O_x holds P_x(j-1) V_{j-1} (complete before S_x(j) was reported) and
+        // nothing newer: rescale it before O_x += P_x(j) V_j is issued
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t rr[32];
-            tmem_ld32(tmem_o + lane_off + c * 32, rr);
-            tmem_ld_wait(rr);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(t_o + c * 32, orr);
+          tmem_ld_wait(orr);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
-            tmem_st32(tmem_o + lane_off + c * 32, rr);
-          }
-          tmem_st_wait();
+          for (int q = 0; q < 32; ++q) orr[q] = __float_as_uint(__uint_as_float(orr[q]) * alpha);
+          tmem_st32(t_o + c * 32, orr);
         }
       }
-      const float mref = (m == -INFINITY) ? 0.f : m;
-      uint32_t pk[kBlockN / 2];
-      float rs = 0.f;
-#pragma unroll
-      for (int j = 0; j < kBlockN / 2; ++j) {
-        const float e0 = ex2(s[2 * j] - mref);
-        const float e1 = ex2(s[2 * j + 1] - mref);
-        rs += e0 + e1;
-        pk[j] = pack_bf16x2(e0, e1);
-      }
-      l += rs;
-      // the single P buffer is free once O += P_{i-1} V_{i-1} has completed
-      if (i > 0 && !o_ready) {
-        if (!warp_wait(&o_done, (i - 1) & 1, &abort_flag)) { ok = false; break; }
-      }
-#pragma unroll
-      for (int u = 0; u < kBlockN / 8; ++u) {
-        const int region = u >> 3, uu = u & 7;
-        uint4* dst = reinterpret_cast<uint4*>(sP + region * L::kChunk + r * 128 + ((uu ^ (r & 7)) << 4));
-        *dst = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full);
+      if (lane == 0) mbar_arrive(&p_full[x]);
     }
     // ---------------------------------------------------------- epilogue
-    if (ok && n_blocks > 0) ok = warp_wait(&o_done, (n_blocks - 1) & 1, &abort_flag);
+    if (ok && n_blocks > 0) ok = warp_wait(&o_final, 0, &abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after_sync();
     if (ok) {
       const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.out + (grow * p.Hq + h) * D;
+      __nv_bfloat16* orow = p.out + (grow * p.Hq + qh) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rr[32];
         if (n_blocks > 0) {
-          tmem_ld32(tmem_o + lane_off + c * 32, rr);
+          tmem_ld32(t_o + c * 32, rr);
           tmem_ld_wait(rr);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) rr[j] = 0u;
         }
         uint32_t ob[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          ob[j] = pack_bf16x2(__uint_as_float(rr[2 * j]) * inv, __uint_as_float(rr[2 * j + 1]) * inv);
+        for (int q = 0; q < 16; ++q)
+          ob[q] = (valid && n_blocks > 0)
+                      ? pack_bf16x2(__uint_as_float(rr[2 * q]) * inv, __uint_as_float(rr[2 * q + 1]) * inv)
+                      : 0u;
         if (grow < p.t_local) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(ob[4 * q4], ob[4 * q4 + 1], ob[4 * q4 + 2], ob[4 * q4 + 3]);
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[q4] = make_uint4(ob[4 * q4], ob[4 * q4 + 1], ob[4 * q4 + 2], ob[4 * q4 + 3]);
         }
       }
       if (grow < p.t_local)
-        p.lse[static_cast<long long>(h) * p.t_local + grow] =
+        p.lse[static_cast<long long>(qh) * p.t_local + grow] =
             (valid && l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
   }
@@ -407,10 +449,14 @@ static bool make_rows_heads_map(EncodeTiledFn enc, CUtensorMap* m, const void* b
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Two query tiles per CTA: two heads of one KV head when the GQA group size is
+// even, else two consecutive 128-row tiles of one head.
+static int group_rows_for(int Hq, int Hkv) { return ((Hq / Hkv) % 2 == 0) ? kBlockM : 2 * kBlockM; }
+
 template <int D>
 static int launch_attn(const void* q, const void* k, const void* v, long long t_local, long long T, int Hq, int Hkv,
-                       float scale_log2, const AttnWorkspace& ws, long long ntiles, void* out, float* lse,
-                       int32_t* err, cudaStream_t s) {
+                       float scale_log2, const AttnWorkspace& ws, long long ngroups, int group_rows, void* out,
+                       float* lse, int32_t* err, cudaStream_t s) {
   EncodeTiledFn enc = get_encode_tiled();
   if (enc == nullptr) return CPTHD_ERR_CUDA;
   CUtensorMap mq, mk, mv;
@@ -420,7 +466,7 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
   AttnParams p;
   p.row_lo = ws.row_lo;
   p.row_hi = ws.row_hi;
-  p.tile_info = ws.tile_info;
+  p.group_info = ws.group_info;
   p.intervals = ws.intervals;
   p.order = ws.order;
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -428,12 +474,14 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
   p.t_local = t_local;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.max_blocks = static_cast<int>((T + kBlockN - 1) / kBlockN + kBlockM);
+  p.head_pairs = (group_rows == kBlockM) ? 1 : 0;
+  p.group_rows = group_rows;
+  p.max_blocks = static_cast<int>((T + kBlockN - 1) / kBlockN + group_rows);
   p.scale_log2 = scale_log2;
   p.err = err;
   const int smem = AttnSmem<D>::kLaunchBytes;
   CPTHD_TRY_CUDA(cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-  const long long items = ntiles * Hq;
+  const long long items = ngroups * (p.head_pairs ? Hq / 2 : Hq);
   if (items > INT32_MAX) return CPTHD_ERR_UNSUPPORTED;
   attn_fwd_tc_kernel<D><<<static_cast<unsigned>(items), kAttnThreads, smem, s>>>(mq, mk, mv, p);
   CPTHD_TRY_CUDA(cudaGetLastError());
@@ -444,9 +492,11 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
 
 extern "C" int thd_causal_attn_workspace_size(int64_t t_local, int Hq, int Hkv, int d, size_t* bytes_host) {
   if (bytes_host == nullptr || t_local < 0 || Hq < 1 || Hkv < 1) return CPTHD_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return CPTHD_ERR_UNSUPPORTED;
   (void)d;
-  const long long ntiles = (t_local + cpthd::kBlockM - 1) / cpthd::kBlockM;
-  *bytes_host = cpthd::attn_workspace_bytes(ntiles);
+  const int rows = cpthd::group_rows_for(Hq, Hkv);
+  const long long ngroups = (t_local + rows - 1) / rows;
+  *bytes_host = cpthd::attn_workspace_bytes(ngroups, rows);
   return CPTHD_OK;
 }
 
@@ -468,8 +518,9 @@ extern "C" int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loc
   const uintptr_t align = reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(k_dev) |
                           reinterpret_cast<uintptr_t>(v_dev) | reinterpret_cast<uintptr_t>(out_dev);
   if (align & 15) return CPTHD_ERR_UNSUPPORTED;
-  const long long ntiles = (t_local + kBlockM - 1) / kBlockM;
-  if (workspace_dev == nullptr || workspace_bytes < attn_workspace_bytes(ntiles) ||
+  const int rows = group_rows_for(Hq, Hkv);
+  const long long ngroups = (t_local + rows - 1) / rows;
+  if (workspace_dev == nullptr || workspace_bytes < attn_workspace_bytes(ngroups, rows) ||
       (reinterpret_cast<uintptr_t>(workspace_dev) & 255))
     return CPTHD_ERR_WORKSPACE;
   const int32_t* cup = cu_seqlens_padded_dev ? cu_seqlens_padded_dev : cu_seqlens_dev;
@@ -477,15 +528,19 @@ extern "C" int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loc
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
   const float scale_log2 = scale * 1.4426950408889634f;
 
-  AttnWorkspace ws = carve_workspace(workspace_dev, ntiles);
-  attn_validate_docs_kernel<<<grid_for(num_docs + 1, 256, 64), 256, 0, s>>>(cu_seqlens_dev, cup, num_docs, T,
-                                                                            err_dev);
-  attn_tile_meta_kernel<<<static_cast<unsigned>(ntiles), kBlockM, 0, s>>>(
-      q_slice_idx_dev, t_local, cu_seqlens_dev, cup, num_docs, T, ws, err_dev);
-  attn_tile_order_kernel<<<1, 1024, 0, s>>>(static_cast<int>(ntiles), ws);
+  AttnWorkspace ws = carve_workspace(workspace_dev, ngroups, rows);
+  if (rows == kBlockM) {
+    attn_group_meta_kernel<kBlockM><<<static_cast<unsigned>(ngroups), kBlockM, 0, s>>>(
+        q_slice_idx_dev, t_local, cu_seqlens_dev, cup, num_docs, T, ws, err_dev);
+  } else {
+    attn_group_meta_kernel<2 * kBlockM><<<static_cast<unsigned>(ngroups), 2 * kBlockM, 0, s>>>(
+        q_slice_idx_dev, t_local, cu_seqlens_dev, cup, num_docs, T, ws, err_dev);
+  }
+  attn_group_order_kernel<<<1, 1024, 0, s>>>(static_cast<int>(ngroups), ws);
   CPTHD_TRY_CUDA(cudaGetLastError());
-  if (d == 128) return launch_attn<128>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ntiles, out_dev,
-                                        lse_dev, err_dev, s);
-  return launch_attn<64>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ntiles, out_dev, lse_dev,
+  if (d == 128)
+    return launch_attn<128>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ngroups, rows, out_dev,
+                            lse_dev, err_dev, s);
+  return launch_attn<64>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ngroups, rows, out_dev, lse_dev,
                          err_dev, s);
 }

@@ -1,4 +1,4 @@
-// Per-row and per-tile metadata of the causal packed-THD attention.
+// Per-row and per-group metadata of the causal packed-THD attention.
 //
 // Document isolation and causality (TransformerEngine PR #3221, "Scope and
 // constraints": causal, window_size = (-1, 0); "What changed": logical
@@ -8,13 +8,17 @@
 // real query of j, so they never fall inside an interval. A pad query row
 // gets the empty interval.
 //
-// For every tile of kBlockM consecutive local rows the metadata kernel
-// stores the union of its rows' intervals (one interval per document present
-// in the tile, sorted by document), the number of kBlockN-key blocks that
-// covers them (the tile's cost), and the largest interval start / smallest
-// interval end over its real rows: a key block inside [maxLo, minHi] needs no
-// mask. A second kernel orders the tiles by decreasing cost, so that a grid
-// launched in that order hands the longest work to the SMs first.
+// The attention kernel gives each CTA two 128-row query tiles that read the
+// same K/V blocks: either one row tile under two query heads of the same KV
+// head (a "row group" of 128 rows), or two consecutive row tiles under one
+// head (a row group of 256 rows). For every row group the metadata kernel
+// stores the union of its rows' intervals (one interval per document present,
+// sorted by document), the number of kBlockN-key blocks that covers them (the
+// group's cost), and for each 128-row tile the largest interval start and
+// smallest interval end over its real rows: a key block inside
+// [max_lo, min_hi] needs no mask. A second kernel orders the groups by
+// decreasing cost, so that a grid launched in that order hands the longest
+// work to the SMs first.
 #pragma once
 
 #include "common.cuh"
@@ -23,51 +27,68 @@ namespace cpthd {
 
 constexpr int kBlockM = 128;  // query rows per tile
 constexpr int kBlockN = 128;  // keys per key block
-constexpr int kMaxSortTiles = 8192;
+constexpr int kMaxSortGroups = 8192;
 
-struct TileInfo {
+struct GroupInfo {
   int n_intervals;
   int n_blocks;
-  int max_lo;  // over real rows; INT_MIN when the tile has none
-  int min_hi;  // over real rows; INT_MAX when the tile has none
+  int max_lo[2];  // per tile, over real rows; INT_MIN when the tile has none
+  int min_hi[2];  // per tile, over real rows; INT_MAX when the tile has none
 };
 
 struct AttnWorkspace {
-  int32_t* row_lo;      // [ntiles * kBlockM]
-  int32_t* row_hi;      // [ntiles * kBlockM]
-  TileInfo* tile_info;  // [ntiles]
-  int2* intervals;      // [ntiles * kBlockM] (start, end) inclusive
-  int32_t* order;       // [ntiles]
+  int32_t* row_lo;        // [ngroups * group_rows]
+  int32_t* row_hi;        // [ngroups * group_rows]
+  GroupInfo* group_info;  // [ngroups]
+  int2* intervals;        // [ngroups * group_rows] (start, end) inclusive
+  int32_t* order;         // [ngroups]
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-inline size_t attn_workspace_bytes(long long ntiles) {
+inline size_t attn_workspace_bytes(long long ngroups, int group_rows) {
+  const long long rows = ngroups * group_rows;
   size_t b = 0;
-  b += align256(sizeof(int32_t) * ntiles * kBlockM);
-  b += align256(sizeof(int32_t) * ntiles * kBlockM);
-  b += align256(sizeof(TileInfo) * ntiles);
-  b += align256(sizeof(int2) * ntiles * kBlockM);
-  b += align256(sizeof(int32_t) * ntiles);
+  b += align256(sizeof(int32_t) * rows);
+  b += align256(sizeof(int32_t) * rows);
+  b += align256(sizeof(GroupInfo) * ngroups);
+  b += align256(sizeof(int2) * rows);
+  b += align256(sizeof(int32_t) * ngroups);
   return b;
 }
 
-inline AttnWorkspace carve_workspace(void* base, long long ntiles) {
+inline AttnWorkspace carve_workspace(void* base, long long ngroups, int group_rows) {
+  const long long rows = ngroups * group_rows;
   char* p = static_cast<char*>(base);
   AttnWorkspace w;
-  w.row_lo = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * ntiles * kBlockM);
-  w.row_hi = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * ntiles * kBlockM);
-  w.tile_info = reinterpret_cast<TileInfo*>(p); p += align256(sizeof(TileInfo) * ntiles);
-  w.intervals = reinterpret_cast<int2*>(p); p += align256(sizeof(int2) * ntiles * kBlockM);
+  w.row_lo = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * rows);
+  w.row_hi = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * rows);
+  w.group_info = reinterpret_cast<GroupInfo*>(p); p += align256(sizeof(GroupInfo) * ngroups);
+  w.intervals = reinterpret_cast<int2*>(p); p += align256(sizeof(int2) * rows);
   w.order = reinterpret_cast<int32_t*>(p);
   return w;
 }
 
-// Document table checks: offsets start at 0, never decrease, padded offsets
-// end at T, and L_j <= P_j.
-__global__ void attn_validate_docs_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cup,
-                                          int num_docs, long long T, int32_t* err) {
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j <= num_docs; j += gridDim.x * blockDim.x) {
+// One block of ROWS threads per row group; thread t owns local row
+// group * ROWS + t. The blocks also check the document table (offsets start
+// at 0 and never decrease, padded offsets end at T, L_j <= P_j) in a
+// grid-stride loop over documents.
+template <int ROWS>
+__global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
+    const int32_t* __restrict__ idx, long long t_local, const int32_t* __restrict__ cu,
+    const int32_t* __restrict__ cup, int num_docs, long long T, AttnWorkspace ws, int32_t* err) {
+  constexpr int kWarps = ROWS / 32;
+  __shared__ unsigned long long keys[ROWS];
+  __shared__ int warp_sum[kWarps];
+  __shared__ int red_blocks[kWarps];
+  __shared__ int red_lo[kWarps];
+  __shared__ int red_hi[kWarps];
+  const int t = threadIdx.x;
+  const int lane = t & 31, wid = t >> 5;
+  const long long group = blockIdx.x;
+  const long long row = group * ROWS + t;
+
+  for (long long j = blockIdx.x * (long long)ROWS + t; j <= num_docs; j += (long long)gridDim.x * ROWS) {
     if (j == 0 && (cu[0] != 0 || cup[0] != 0)) record_error(err, CPTHD_ERR_BAD_OFFSETS, 0);
     if (j == num_docs && cup[j] != T) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
     if (j < num_docs) {
@@ -77,21 +98,6 @@ __global__ void attn_validate_docs_kernel(const int32_t* __restrict__ cu, const 
       else if (L > P) record_error(err, CPTHD_ERR_PAD_LENGTH, j);
     }
   }
-}
-
-// One block of kBlockM threads per tile; thread t owns local row tile*kBlockM + t.
-__global__ void __launch_bounds__(kBlockM) attn_tile_meta_kernel(
-    const int32_t* __restrict__ idx, long long t_local, const int32_t* __restrict__ cu,
-    const int32_t* __restrict__ cup, int num_docs, long long T, AttnWorkspace ws, int32_t* err) {
-  __shared__ unsigned long long keys[kBlockM];
-  __shared__ int warp_sum[kBlockM / 32];
-  __shared__ int red_blocks[kBlockM / 32];
-  __shared__ int red_lo[kBlockM / 32];
-  __shared__ int red_hi[kBlockM / 32];
-  const int t = threadIdx.x;
-  const int lane = t & 31, wid = t >> 5;
-  const long long tile = blockIdx.x;
-  const long long row = tile * kBlockM + t;
 
   int lo = 1, hi = 0;  // empty interval
   bool valid = false;
@@ -112,11 +118,10 @@ __global__ void __launch_bounds__(kBlockM) attn_tile_meta_kernel(
   }
   ws.row_lo[row] = lo;
   ws.row_hi[row] = hi;
-  keys[t] = valid ? ((static_cast<unsigned long long>(doc) << 32) | static_cast<unsigned>(hi))
-                  : ~0ull;
+  keys[t] = valid ? ((static_cast<unsigned long long>(doc) << 32) | static_cast<unsigned>(hi)) : ~0ull;
   __syncthreads();
   // bitonic sort of the (document, end) keys, ascending
-  for (int k = 2; k <= kBlockM; k <<= 1) {
+  for (int k = 2; k <= ROWS; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
       const int ixj = t ^ j;
       if (ixj > t) {
@@ -128,7 +133,7 @@ __global__ void __launch_bounds__(kBlockM) attn_tile_meta_kernel(
     }
   }
   const unsigned long long key = keys[t];
-  const unsigned long long nxt = (t + 1 < kBlockM) ? keys[t + 1] : ~0ull;
+  const unsigned long long nxt = (t + 1 < ROWS) ? keys[t + 1] : ~0ull;
   const bool last = (key != ~0ull) && ((nxt >> 32) != (key >> 32));
   int my_lo = 0, my_hi = -1, my_blocks = 0;
   if (last) {
@@ -137,7 +142,7 @@ __global__ void __launch_bounds__(kBlockM) attn_tile_meta_kernel(
     my_hi = static_cast<int>(key & 0xffffffffu);
     my_blocks = (my_hi - my_lo + kBlockN) / kBlockN;
   }
-  // compact the interval ends in document order
+  // compact the intervals in document order; reduce cost and per-warp bounds
   const unsigned ballot = __ballot_sync(0xffffffffu, last);
   if (lane == 0) warp_sum[wid] = __popc(ballot);
   int blocks = my_blocks;
@@ -154,35 +159,39 @@ __global__ void __launch_bounds__(kBlockM) attn_tile_meta_kernel(
   for (int w = 0; w < wid; ++w) base += warp_sum[w];
   if (last) {
     const int slot = base + __popc(ballot & ((1u << lane) - 1u));
-    ws.intervals[tile * kBlockM + slot] = make_int2(my_lo, my_hi);
+    ws.intervals[group * ROWS + slot] = make_int2(my_lo, my_hi);
   }
   if (t == 0) {
-    TileInfo ti;
-    ti.n_intervals = 0; ti.n_blocks = 0; ti.max_lo = INT_MIN; ti.min_hi = INT_MAX;
-    for (int w = 0; w < kBlockM / 32; ++w) {
-      ti.n_intervals += warp_sum[w];
-      ti.n_blocks += red_blocks[w];
-      ti.max_lo = max(ti.max_lo, red_lo[w]);
-      ti.min_hi = min(ti.min_hi, red_hi[w]);
+    GroupInfo gi;
+    gi.n_intervals = 0;
+    gi.n_blocks = 0;
+    for (int x = 0; x < 2; ++x) { gi.max_lo[x] = INT_MIN; gi.min_hi[x] = INT_MAX; }
+    for (int w = 0; w < kWarps; ++w) {
+      gi.n_intervals += warp_sum[w];
+      gi.n_blocks += red_blocks[w];
+      const int x = (w * 32) / kBlockM;  // tile of this warp's rows
+      gi.max_lo[x] = max(gi.max_lo[x], red_lo[w]);
+      gi.min_hi[x] = min(gi.min_hi[x], red_hi[w]);
     }
-    ws.tile_info[tile] = ti;
+    if (ROWS == kBlockM) { gi.max_lo[1] = gi.max_lo[0]; gi.min_hi[1] = gi.min_hi[0]; }
+    ws.group_info[group] = gi;
   }
 }
 
-// One block of 1024 threads: order[] = tiles by decreasing block count
-// (ties by tile index). Larger tile counts keep the natural order.
-__global__ void __launch_bounds__(1024) attn_tile_order_kernel(int ntiles, AttnWorkspace ws) {
-  __shared__ unsigned keys[kMaxSortTiles];
+// One block of 1024 threads: order[] = groups by decreasing block count
+// (ties by group index). Larger group counts keep the natural order.
+__global__ void __launch_bounds__(1024) attn_group_order_kernel(int ngroups, AttnWorkspace ws) {
+  __shared__ unsigned keys[kMaxSortGroups];
   const int t = threadIdx.x;
-  if (ntiles > kMaxSortTiles) {
-    for (int i = t; i < ntiles; i += blockDim.x) ws.order[i] = i;
+  if (ngroups > kMaxSortGroups) {
+    for (int i = t; i < ngroups; i += blockDim.x) ws.order[i] = i;
     return;
   }
   int n2 = 1;
-  while (n2 < ntiles) n2 <<= 1;
+  while (n2 < ngroups) n2 <<= 1;
   for (int i = t; i < n2; i += blockDim.x) {
-    if (i < ntiles) {
-      const unsigned cost = static_cast<unsigned>(min(max(ws.tile_info[i].n_blocks, 0), (1 << 18) - 1));
+    if (i < ngroups) {
+      const unsigned cost = static_cast<unsigned>(min(max(ws.group_info[i].n_blocks, 0), (1 << 18) - 1));
       keys[i] = ((cost ^ 0x3ffffu) << 13) | static_cast<unsigned>(i);
     } else {
       keys[i] = 0xffffffffu;
@@ -202,7 +211,7 @@ __global__ void __launch_bounds__(1024) attn_tile_order_kernel(int ntiles, AttnW
       __syncthreads();
     }
   }
-  for (int i = t; i < ntiles; i += blockDim.x) ws.order[i] = static_cast<int>(keys[i] & 0x1fffu);
+  for (int i = t; i < ngroups; i += blockDim.x) ws.order[i] = static_cast<int>(keys[i] & 0x1fffu);
 }
 
 }  // namespace cpthd

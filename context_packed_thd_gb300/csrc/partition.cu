@@ -13,23 +13,28 @@
 
 namespace cpthd {
 
-__global__ void validate_offsets_kernel(const int32_t* __restrict__ cup, int num_docs, long long T,
-                                        int cp, int dcs, int32_t* err) {
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j <= num_docs; j += gridDim.x * blockDim.x) {
-    int32_t a = cup[j];
+// Offset-table checks shared by both index kernels: cup starts at 0, never
+// decreases and ends at T; under DualChunkSwap every padded length is a
+// multiple of 2*cp_size.
+__device__ __forceinline__ void check_offsets(const int32_t* __restrict__ cup, int num_docs, long long T, int cp,
+                                              int dcs, int32_t* err) {
+  for (long long j = blockIdx.x * (long long)blockDim.x + threadIdx.x; j <= num_docs;
+       j += (long long)gridDim.x * blockDim.x) {
+    const int32_t a = cup[j];
     if (j == 0 && a != 0) record_error(err, CPTHD_ERR_BAD_OFFSETS, 0);
     if (j == num_docs && a != T) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
     if (j < num_docs) {
-      int32_t b = cup[j + 1];
+      const int32_t b = cup[j + 1];
       if (b < a) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
       else if (dcs && ((b - a) % (2 * cp)) != 0) record_error(err, CPTHD_ERR_NOT_DIVISIBLE, j);
     }
   }
 }
 
-__global__ void dual_chunk_swap_index_kernel(const int32_t* __restrict__ cup, int num_docs, int cp,
+__global__ void dual_chunk_swap_index_kernel(const int32_t* __restrict__ cup, int num_docs, long long T, int cp,
                                              int rank, long long t_local, long long total,
-                                             int32_t* __restrict__ idx) {
+                                             int32_t* __restrict__ idx, int32_t* err) {
+  check_offsets(cup, num_docs, T, cp, 1, err);
   for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
        o += (long long)gridDim.x * blockDim.x) {
     int r = rank;
@@ -50,8 +55,10 @@ __global__ void dual_chunk_swap_index_kernel(const int32_t* __restrict__ cup, in
   }
 }
 
-__global__ void no_load_balance_index_kernel(int rank, long long t_local, long long total,
-                                             int32_t* __restrict__ idx) {
+__global__ void no_load_balance_index_kernel(const int32_t* __restrict__ cup, int num_docs, long long T, int cp,
+                                             int rank, long long t_local, long long total,
+                                             int32_t* __restrict__ idx, int32_t* err) {
+  check_offsets(cup, num_docs, T, cp, 0, err);
   for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
        o += (long long)gridDim.x * blockDim.x) {
     long long p = (rank < 0) ? o : rank * t_local + o;
@@ -83,16 +90,14 @@ extern "C" int cp_partition_index(int strategy, const int32_t* cu_seqlens_padded
   if (total > 0 && num_docs == 0) return CPTHD_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int dcs = (strategy == CPTHD_DUAL_CHUNK_SWAP);
-  cpthd::validate_offsets_kernel<<<cpthd::grid_for(num_docs + 1, 256, 64), 256, 0, s>>>(
-      cu_seqlens_padded_dev, num_docs, T, cp_size, dcs, err_dev);
-  CPTHD_TRY_CUDA(cudaGetLastError());
-  if (total == 0) return CPTHD_OK;
-  const int grid = cpthd::grid_for(total, 256, 152 * 16);
+  const long long work = total > num_docs + 1 ? total : num_docs + 1;
+  const int grid = cpthd::grid_for(work, 256, 152 * 16);
   if (dcs) {
-    cpthd::dual_chunk_swap_index_kernel<<<grid, 256, 0, s>>>(cu_seqlens_padded_dev, num_docs, cp_size,
-                                                             rank, t_local, total, idx_out_dev);
+    cpthd::dual_chunk_swap_index_kernel<<<grid, 256, 0, s>>>(cu_seqlens_padded_dev, num_docs, T, cp_size, rank,
+                                                             t_local, total, idx_out_dev, err_dev);
   } else {
-    cpthd::no_load_balance_index_kernel<<<grid, 256, 0, s>>>(rank, t_local, total, idx_out_dev);
+    cpthd::no_load_balance_index_kernel<<<grid, 256, 0, s>>>(cu_seqlens_padded_dev, num_docs, T, cp_size, rank,
+                                                             t_local, total, idx_out_dev, err_dev);
   }
   CPTHD_TRY_CUDA(cudaGetLastError());
   return CPTHD_OK;

@@ -81,6 +81,8 @@ def test_host_validation_launches_nothing(cp):
 
 def test_workspace_size(cp):
     a = cp.thd_causal_attn_workspace_size(128, 8, 8, 128)
-    b = cp.thd_causal_attn_workspace_size(129, 8, 8, 128)
-    assert 0 < a < b
+    b = cp.thd_causal_attn_workspace_size(257, 8, 8, 128)      # 256-row groups (one head, two row tiles)
+    c = cp.thd_causal_attn_workspace_size(128, 32, 8, 128)     # 128-row groups (two heads, one row tile)
+    e = cp.thd_causal_attn_workspace_size(129, 32, 8, 128)
+    assert 0 < a < b and 0 < c < e
     assert cp.thd_causal_attn_workspace_size(0, 8, 8, 128) >= 0
