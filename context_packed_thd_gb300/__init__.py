@@ -17,7 +17,8 @@ import torch
 __all__ = [
     "DUAL_CHUNK_SWAP", "NO_LOAD_BALANCE", "CpthdError", "LIB_PATH", "lib",
     "cpthd_status_string", "cp_local_tokens", "cp_partition_index", "cp_reorder", "cp_reorder_multi",
-    "thd_causal_attn_workspace_size", "thd_causal_attn_fwd", "get_batch_on_this_cp_rank", "strategy_code",
+    "thd_causal_attn_workspace_size", "thd_causal_attn_fwd", "thd_causal_attn_fwd_static_scratch",
+    "get_batch_on_this_cp_rank", "strategy_code",
 ]
 
 DUAL_CHUNK_SWAP = 0
@@ -32,9 +33,11 @@ def _load_library():
     from . import build as _build
     try:
         _build.build()
-    except Exception as e:  # no nvcc, compile error ...
+    except _build.NvccMissing as e:  # a prebuilt library may still be there
         if not os.path.exists(LIB_PATH):
             raise ImportError(f"libcpthd.so is missing and could not be built: {e}") from e
+    except RuntimeError as e:       # a compile or link error never falls back to a stale library
+        raise ImportError(f"building libcpthd.so failed: {e}") from e
     return ctypes.CDLL(LIB_PATH)
 
 
@@ -62,6 +65,9 @@ lib.thd_causal_attn_workspace_size.restype = _i32
 lib.thd_causal_attn_fwd.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _f32, _vp,
                                     _vp, _vp, _sz, _vp, _vp]
 lib.thd_causal_attn_fwd.restype = _i32
+lib.thd_causal_attn_fwd_static_scratch.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32,
+                                                   _f32, _vp, _vp, _vp, _vp]
+lib.thd_causal_attn_fwd_static_scratch.restype = _i32
 
 
 class CpthdError(RuntimeError):
@@ -191,6 +197,33 @@ def thd_causal_attn_fwd(q_slice_idx: torch.Tensor, q: torch.Tensor, k: torch.Ten
                                    float(softmax_scale) if softmax_scale else 0.0, _ptr(out), _ptr(lse),
                                    _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)),
            "thd_causal_attn_fwd")
+    return out, lse
+
+
+def thd_causal_attn_fwd_static_scratch(q_slice_idx: torch.Tensor, q: torch.Tensor, k: torch.Tensor,
+                                       v: torch.Tensor, cu_seqlens: torch.Tensor,
+                                       cu_seqlens_padded: Optional[torch.Tensor] = None,
+                                       softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                                       lse: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None,
+                                       stream=None):
+    """thd_causal_attn_fwd for callers that cannot allocate device memory: the
+    library's built-in scratch array replaces the workspace. Pass ``out`` and
+    ``lse`` to keep the call itself free of allocations (when they are None
+    this convenience wrapper creates them with torch)."""
+    _need_cuda(q_slice_idx, q, k, v, cu_seqlens, cu_seqlens_padded, out, lse, err)
+    t_local, Hq, d = q.shape
+    T, Hkv, _ = k.shape
+    for t in (q, k, v):
+        assert t.dtype == torch.bfloat16 and t.is_contiguous()
+    assert q_slice_idx.dtype == torch.int32 and q_slice_idx.numel() == t_local
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, t_local), dtype=torch.float32, device=q.device)
+    _check(lib.thd_causal_attn_fwd_static_scratch(
+        _ptr(q_slice_idx), t_local, _ptr(q), _ptr(k), _ptr(v), T, _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
+        cu_seqlens.numel() - 1, Hq, Hkv, d, float(softmax_scale) if softmax_scale else 0.0, _ptr(out), _ptr(lse),
+        _ptr(err), _stream(stream)), "thd_causal_attn_fwd_static_scratch")
     return out, lse
 
 

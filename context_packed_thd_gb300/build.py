@@ -28,11 +28,15 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-
                      "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 
 
+class NvccMissing(RuntimeError):
+    pass
+
+
 def _nvcc() -> str:
     for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
         if cand and os.path.exists(cand):
             return cand
-    raise RuntimeError("nvcc not found: the CUDA 13 toolkit is required to build libcpthd")
+    raise NvccMissing("nvcc not found: the CUDA 13 toolkit is required to build libcpthd")
 
 
 def _sources():

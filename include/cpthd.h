@@ -75,7 +75,8 @@ enum {
   CPTHD_ERR_BAD_OFFSETS = -6,   /* (device) offsets not non-decreasing, not starting at 0, or not ending at T */
   CPTHD_ERR_INDEX_RANGE = -7,   /* (device) an index outside [0, rows) */
   CPTHD_ERR_PAD_LENGTH = -8,    /* (device) actual length L_j larger than padded length P_j */
-  CPTHD_ERR_TIMEOUT = -9        /* (device) a pipeline wait gave up; the kernel returned early */
+  CPTHD_ERR_TIMEOUT = -9,       /* (device) a pipeline wait gave up; the kernel returned early */
+  CPTHD_ERR_SCRATCH_LIMIT = -10 /* slice needs more scratch than thd_causal_attn_fwd_static_scratch holds */
 };
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -154,6 +155,29 @@ CPTHD_API int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loca
                         int num_docs, int Hq, int Hkv, int d, float softmax_scale, void* out_dev,
                         float* lse_dev, void* workspace_dev, size_t workspace_bytes,
                         int32_t* err_dev, cpthd_stream_t stream);
+
+/* Same computation as thd_causal_attn_fwd for callers that cannot allocate
+ * device memory (a host framework that owns all allocations, a plugin that
+ * must not call cudaMalloc mid-step, a path that may never enter an
+ * allocator). The pages have no counterpart: this is a deployment variant.
+ * Instead of a caller workspace it uses a fixed 4 MiB device array built into
+ * the library, which every GPU that loads the library holds until the
+ * process exits; the call allocates nothing. That is enough for slices of at
+ * least 250,000 query rows; a larger slice is rejected with
+ * CPTHD_ERR_SCRATCH_LIMIT before anything is launched.
+ * The first call on a device looks up the array's device address for that
+ * device (with it current); make that first call before any stream capture.
+ * All calls share the one array: calls that overlap on the GPU (different
+ * streams without ordering between them) race and corrupt each other's
+ * results. Nothing in the array needs clearing between calls.
+ * Arguments, layouts and device checks as thd_causal_attn_fwd, without the
+ * workspace pair. */
+CPTHD_API int thd_causal_attn_fwd_static_scratch(const int32_t* q_slice_idx_dev, int64_t t_local,
+                                                 const void* q_dev, const void* k_dev, const void* v_dev,
+                                                 int64_t T, const int32_t* cu_seqlens_dev,
+                                                 const int32_t* cu_seqlens_padded_dev, int num_docs, int Hq,
+                                                 int Hkv, int d, float softmax_scale, void* out_dev,
+                                                 float* lse_dev, int32_t* err_dev, cpthd_stream_t stream);
 
 #ifdef __cplusplus
 }
