@@ -15,18 +15,21 @@
 //  * warp 0      TMA producer: both Q tiles once, then K and V 128-key blocks
 //                into a two-stage shared-memory ring (128-byte swizzle, the
 //                layout the UMMA shared-memory descriptors read).
-//  * warp 1      owns the 512-column TMEM allocation (S_A, S_B, O_A, O_B);
-//                one lane issues the tcgen05 MMAs in the order
-//                  S_A(0), S_B(0), then per block j:
-//                  O_A += P_A(j) V_j, S_A(j+1), O_B += P_B(j) V_j, S_B(j+1)
-//                so that each softmax warpgroup works while the tensor core
-//                runs the other tile's two MMAs. P_x(j) is written by the
-//                softmax into the first 64 columns of S_x (bf16 pairs) and is
-//                read from TMEM by the MMA. Because MMAs complete in issue
-//                order, the commit that reports S_x(j+1) also reports that
-//                O_x += P_x(j) V_j is done, so the softmax may then rescale O_x
-//                and overwrite P_x without further waits.
-//  * warps 2-3   idle.
+//  * warps 1, 2  one lane each issues the tcgen05 MMAs of one tile x:
+//                S_x(0), then per block j: O_x += P_x(j) V_j, S_x(j+1). Two
+//                issuing threads are needed: one thread issuing 128x128x16
+//                MMAs back to back reaches about 85% of the tensor rate on
+//                GB300, two reach all of it. The issue is fully unrolled
+//                with descriptors precomputed; an issue loop with address
+//                arithmetic per MMA halves the rate. Warp 1 also owns the
+//                512-column TMEM allocation (S_A, S_B, O_A, O_B). P_x(j) is
+//                written by the softmax into the first 64 columns of S_x
+//                (bf16 pairs) and is read from TMEM by the MMA. Because one
+//                thread's MMAs complete in issue order, the commit that
+//                reports S_x(j+1) also reports that O_x += P_x(j) V_j is
+//                done, so the softmax may then rescale O_x and overwrite P_x
+//                without further waits.
+//  * warp 3      idle.
 //  * warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: each thread
 //                owns one query row (its TMEM lane). It reads S with one
 //                tcgen05.ld, masks by the row's key interval [document
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sV = smem + L::kVOff;
 
   __shared__ uint64_t q_full, k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
-  __shared__ uint64_t s_full[2], p_full[2], o_final, drain;
+  __shared__ uint64_t s_full[2], p_full[2], o_final[2], drain[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -157,15 +160,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&k_empty[s], 2);  // released by both MMA issuers
+      mbar_init(&v_empty[s], 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
       mbar_init(&p_full[x], 4);
+      mbar_init(&o_final[x], 1);
+      mbar_init(&drain[x], 1);
     }
-    mbar_init(&o_final, 1);
-    mbar_init(&drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -220,69 +223,66 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
     }
-   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+   } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread per tile (warp 1: tile A, warp 2: tile B); two issuing
+    // threads keep the tensor core busy with 128-wide MMAs where one cannot.
+    const int x = warp - 1;
     if (lane == 0 && n_blocks > 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kBlockM, D, 0, 1);
-      const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
-      // Descriptors differ only in their start-address field (bits 0-13,
-      // address >> 4), so each one is a base descriptor plus an offset >> 4;
-      // shared-memory addresses stay below 256 KB, so the field never carries.
-      const uint64_t dq = smem_desc_sw128(q0, 16, 1024);
-      const uint64_t dk = smem_desc_sw128(k0, 16, 1024);
-      const uint64_t dv = smem_desc_sw128(v0, L::kChunk, 1024);
-      auto issue_s = [&](int x, int j) {  // S_x = Q_x K_j^T
-        const uint32_t qoff = (x * L::kQ) >> 4, koff = ((j & 1) * L::kKV) >> 4;
-#pragma unroll 1
+      // A descriptor's low word holds the start address (>> 4) and the
+      // leading-byte offset; its high word (stride offset, version, swizzle)
+      // is the same for every block of one operand. Addresses stay below
+      // 256 KB, so adding an offset to the low word never carries.
+      const uint64_t dq = smem_desc_sw128(smem_u32(sQ + x * L::kQ), 16, 1024);
+      const uint64_t dk = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dv = smem_desc_sw128(smem_u32(sV), L::kChunk, 1024);
+      const uint32_t q_lo = static_cast<uint32_t>(dq), q_hi = static_cast<uint32_t>(dq >> 32);
+      const uint32_t k_lo = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
+      const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
+      const uint32_t t_s = tmem + x * kBlockN;
+      const uint32_t t_o = tmem + 256 + x * D;
+      auto issue_s = [&](int j) {  // S_x = Q_x K_j^T
+        const uint32_t kb = k_lo + (((j & 1) * L::kKV) >> 4);
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
-          umma_ss(tmem + x * kBlockN, dq + qoff + off, dk + koff + off, kIdescS, kk > 0);
+          umma_ss_w(t_s, q_lo + off, q_hi, kb + off, k_hi, kIdescS, kk > 0);
         }
       };
-      auto issue_pv = [&](int x, int j) {  // O_x += P_x V_j, P_x read from TMEM
-        const uint32_t voff = ((j & 1) * L::kKV) >> 4;
-#pragma unroll 1
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          umma_ts(tmem + 256 + x * D, tmem + x * kBlockN + kk * 8, dv + voff + ((kk * 16 * 128) >> 4), kIdescO,
-                  (j > 0 || kk > 0));
-        }
+      auto issue_pv = [&](int j) {  // O_x += P_x V_j, P_x read from TMEM
+        const uint32_t vb = v_lo + (((j & 1) * L::kKV) >> 4);
+        const uint32_t acc0 = (j > 0) ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          umma_ts_w(t_o, t_s + kk * 8, vb + ((kk * 16 * 128) >> 4), v_hi, kIdescO, kk > 0 ? 1u : acc0);
       };
       bool ok = mbar_wait(&q_full, 0, &abort_flag) && mbar_wait(&k_full[0], 0, &abort_flag);
       if (ok) {
         tc_fence_after_sync();
-        issue_s(0, 0);
-        umma_commit(&s_full[0]);
-        issue_s(1, 0);
-        umma_commit(&s_full[1]);
+        issue_s(0);
+        umma_commit(&s_full[x]);
         umma_commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < n_blocks; ++j) {
         const int st = j & 1;
-        const bool more = (j + 1 < n_blocks);
         if (!mbar_wait(&v_full[st], (j >> 1) & 1, &abort_flag)) break;
-        if (!mbar_wait(&p_full[0], j & 1, &abort_flag)) break;
+        if (!mbar_wait(&p_full[x], j & 1, &abort_flag)) break;
         tc_fence_after_sync();
-        issue_pv(0, j);
-        if (more) {
+        issue_pv(j);
+        umma_commit(&v_empty[st]);
+        if (j + 1 < n_blocks) {
           if (!mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, &abort_flag)) break;
           tc_fence_after_sync();
-          issue_s(0, j + 1);
-          umma_commit(&s_full[0]);
-        }
-        if (!mbar_wait(&p_full[1], j & 1, &abort_flag)) break;
-        tc_fence_after_sync();
-        issue_pv(1, j);
-        umma_commit(&v_empty[st]);
-        if (more) {
-          issue_s(1, j + 1);
-          umma_commit(&s_full[1]);
+          issue_s(j + 1);
+          umma_commit(&s_full[x]);
           umma_commit(&k_empty[(j + 1) & 1]);
         }
       }
-      umma_commit(&o_final);
-      umma_commit(&drain);
-      mbar_wait_drain(&drain, 0);
+      umma_commit(&o_final[x]);
+      umma_commit(&drain[x]);
+      mbar_wait_drain(&drain[x], 0);
     }
    }
   } else {
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (lane == 0) mbar_arrive(&p_full[x]);
     }
     // ---------------------------------------------------------- epilogue
-    if (ok && n_blocks > 0) ok = warp_wait(&o_final, 0, &abort_flag);
+    if (ok && n_blocks > 0) ok = warp_wait(&o_final[x], 0, &abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after_sync();
     if (ok) {
