@@ -11,8 +11,13 @@ metadata + attention kernel).
 The headline metric is attention TFLOPS over unmasked pairs only
 (4 * d * pairs * Hq per step, pairs counted from the rank's index list)
 divided by the device time of the step, measured with CUDA events on the
-launching stream. L2 (129 MB) is flushed between timed steps by writing a
-256 MB buffer outside the timed region.
+launching stream. The step's library calls are captured once into a CUDA
+graph and replayed, so host launch overhead does not enter the device time.
+L2 (129 MB) is flushed between timed steps by writing a 256 MB buffer
+outside the timed region. Each (strategy, rank) part is also replayed alone
+to report per-rank attention times and the attention roofline. The
+end-to-end figure adds, every step, the host-to-device copy of all inputs
+from pinned memory and the device-to-host copy of every output and LSE.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the float64 CPU oracle, timed on host cores
@@ -172,19 +177,51 @@ class Strategy:
     # tensors 1, attention (row-group metadata, group order, attention) 3
     LAUNCHES_PER_RANK = 5
 
-    def run_rank(self, cp, r, ev=None):
+    def run_prep(self, cp, r):
         d = self.dev
-        if ev is not None:
-            ev[0].record()
         cp.cp_partition_index(self.name, d["cup"], self.T, self.cpsize, r, out=self.idx[r], err=self.err)
         cp.cp_reorder_multi([d["q"], d["ids"], d["labels"], d["pos"]], self.idx[r],
                             outs=[self.q_loc[r]] + self.ids_loc[r], err=self.err)
-        if ev is not None:
-            ev[1].record()
+
+    def run_attn(self, cp, r):
+        d = self.dev
         cp.thd_causal_attn_fwd(self.idx[r], self.q_loc[r], d["k"], d["v"], d["cu"], d["cup"], out=self.out[r],
                                lse=self.lse[r], workspace=self.ws, err=self.err)
-        if ev is not None:
-            ev[2].record()
+
+    def run_rank(self, cp, r):
+        self.run_prep(cp, r)
+        self.run_attn(cp, r)
+
+
+def activation_reorder(cp, cfg, st, ranks, flush, dev, hbm_peak):
+    """Reorder of the workload's [T, width] bf16 activations into every rank's
+    token order (graph replays, L2 flushed before each)."""
+    act = W.make_activations(cfg.seed, st.T, cfg.act_width, device=str(dev))
+    out = torch.empty((st.t_local, cfg.act_width), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    times = []
+    for r in ranks:
+        cp.cp_reorder(act, st.idx[r], out=out, err=st.err)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cp.cp_reorder(act, st.idx[r], out=out, err=st.err)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ms = []
+        for _ in range(5):
+            flush.zero_()
+            ev0.record(stream)
+            g.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(ev0.elapsed_time(ev1))
+        times.append(statistics.median(ms))
+    row = cfg.act_width * 2
+    per_rank_bytes = st.t_local * (2 * row + 4)
+    gbs = per_rank_bytes * len(ranks) / (sum(times) * 1e-3) / 1e9
+    del act, out
+    return {"GB/s": round(gbs, 1), "peak_GB/s": hbm_peak, "frac": round(gbs / hbm_peak, 4),
+            "bytes_per_rank": per_rank_bytes, "ms_per_rank_max": round(max(times), 5),
+            "shape": f"[{st.T}, {cfg.act_width}] bf16 -> [{st.t_local}, {cfg.act_width}] per rank, {st.name}"}
 
 
 def run_cuda(args):
@@ -207,12 +244,10 @@ def run_cuda(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(evs=None):
-        k = 0
+    def step():
         for st in strategies:
             for r in ranks:
-                st.run_rank(cp, r, None if evs is None else evs[k])
-                k += 1
+                st.run_rank(cp, r)
 
     n_ranks = len(ranks) * len(strategies)
     for _ in range(args.warmup):
@@ -224,10 +259,30 @@ def run_cuda(args):
         if e[0] != 0:
             raise RuntimeError(f"device check failed during warm-up: {cp.cpthd_status_string(e[0])} ({e})")
 
+    # ---- CUDA graphs: the whole step, and every (strategy, rank) part alone ---
+    # The library's calls are plain kernel launches on the current stream, so
+    # a step is captured once and replayed; this removes the host-side launch
+    # gaps that would otherwise dominate the small workloads.
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step()
+    g_prep, g_attn = [], []
+    for st in strategies:
+        for r in ranks:
+            gp, ga = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gp):
+                st.run_prep(cp, r)
+            with torch.cuda.graph(ga):
+                st.run_attn(cp, r)
+            g_prep.append(gp)
+            g_attn.append(ga)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        g_step.replay()
+    torch.cuda.synchronize()
+
     # ---- device-timed region -------------------------------------------------
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    rank_ev = [[tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(n_ranks)]
-               for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
@@ -237,7 +292,7 @@ def run_cuda(args):
     for i in range(args.steps):
         flush.zero_()
         step_ev[i][0].record(stream)
-        step(rank_ev[i])
+        g_step.replay()
         step_ev[i][1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -246,8 +301,6 @@ def run_cuda(args):
 
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     total_ms = sum(step_ms)
-    attn_ms = [[rank_ev[i][k][1].elapsed_time(rank_ev[i][k][2]) for k in range(n_ranks)] for i in range(args.steps)]
-    prep_ms = [[rank_ev[i][k][0].elapsed_time(rank_ev[i][k][1]) for k in range(n_ranks)] for i in range(args.steps)]
     flops_step = sum(st.flops[r] for st in strategies for r in ranks)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -255,8 +308,28 @@ def run_cuda(args):
         total_ms = float(t.item())
     value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
 
-    # per-rank attention times (median over steps) and the dominant-kernel roofline
-    med_attn = [statistics.median(attn_ms[i][k] for i in range(args.steps)) for k in range(n_ranks)]
+    # ---- each part of the step alone (graph replays, L2 flushed before each) --
+    reps = max(3, min(args.steps, 10))
+    attn_ms = [[0.0] * reps for _ in range(n_ranks)]
+    prep_ms = [[0.0] * reps for _ in range(n_ranks)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for k in range(n_ranks):
+        for i in range(reps):
+            flush.zero_()
+            ev[0].record(stream)
+            g_prep[k].replay()
+            ev[1].record(stream)
+            flush.zero_()
+            ev[2].record(stream)
+            g_attn[k].replay()
+            ev[3].record(stream)
+            torch.cuda.synchronize()
+            prep_ms[k][i] = ev[0].elapsed_time(ev[1])
+            attn_ms[k][i] = ev[2].elapsed_time(ev[3])
+
+    # per-rank attention times (median over replays) and the dominant-kernel roofline
+    med_attn = [statistics.median(x) for x in attn_ms]
+    med_prep = [statistics.median(x) for x in prep_ms]
     per_strategy = {}
     k = 0
     for st in strategies:
@@ -264,17 +337,18 @@ def run_cuda(args):
         fl = [st.flops[r] for r in ranks]
         pr = [st.pairs[r] for r in ranks]
         per_strategy[st.name] = {
-            "attn_ms_per_rank_max": max(ms), "attn_ms_per_rank_min": min(ms),
-            "attn_tflops": sum(fl) / (sum(ms) * 1e-3) / 1e12,
+            "attn_ms_per_rank_max": round(max(ms), 5), "attn_ms_per_rank_min": round(min(ms), 5),
+            "attn_tflops": round(sum(fl) / (sum(ms) * 1e-3) / 1e12, 3),
             "pairs_per_rank_max": max(pr), "pairs_per_rank_min": min(pr),
         }
         k += len(ranks)
-    attn_total_ms = sum(sum(x) for x in attn_ms)
-    achieved = flops_step * args.steps / (attn_total_ms * 1e-3) / 1e12
+    achieved = flops_step / (sum(med_attn) * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     reorder_bytes = sum(st.reorder_bytes * len(ranks) for st in strategies)
-    prep_total_ms = sum(sum(x) for x in prep_ms)
+    prep_total_ms = sum(med_prep)
+    act = activation_reorder(cp, cfg, strategies[0], ranks, flush, dev, hbm_peak) if cfg.act_width else None
 
     # ---- end to end: pinned host inputs -> step -> host results --------------
     e2e_steps = max(1, min(args.steps, 10))
@@ -287,7 +361,7 @@ def run_cuda(args):
         for st in strategies:
             for key, h in st.host.items():
                 st.dev[key].copy_(h, non_blocking=True)
-        step()
+        g_step.replay()
         for st in strategies:
             for r in ranks:
                 st.out_host[r].copy_(st.out[r], non_blocking=True)
@@ -320,11 +394,13 @@ def run_cuda(args):
                        "subset": None if (args.strategy is None and args.rank is None)
                        else {"strategy": args.strategy, "rank": args.rank},
                        "l2": "flushed between timed steps (256 MB write, untimed)",
+                       "launch": "one CUDA graph per step (the library calls, captured once)",
                        "parallelism": f"replicas{world}"},
             "per_strategy": per_strategy,
-            "reorder": {"GB/s": round(reorder_bytes * args.steps / (prep_total_ms * 1e-3) / 1e9, 2),
+            "reorder": {"GB/s": round(reorder_bytes / (prep_total_ms * 1e-3) / 1e9, 2),
                         "bytes_per_step": reorder_bytes,
                         "note": "partition index + one reorder launch of Q and the int64 ids, timed together per rank"},
+            "reorder_activations": act,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
                          "kernel": "thd_causal_attn_fwd (timed per call: row-group metadata, group order, attention kernel)",
@@ -332,6 +408,7 @@ def run_cuda(args):
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": Strategy.LAUNCHES_PER_RANK * n_ranks * args.steps,
+            "gpu_launches_note": "library kernels inside the timed step replays; the L2 flush between steps is a torch fill",
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

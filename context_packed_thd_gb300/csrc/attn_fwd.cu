@@ -14,7 +14,9 @@
 // the 168 * 384 the launch allocates):
 //  * warp 0      TMA producer: both Q tiles once, then K and V 128-key blocks
 //                into a two-stage shared-memory ring (128-byte swizzle, the
-//                layout the UMMA shared-memory descriptors read).
+//                layout the UMMA shared-memory descriptors read). Both MMA
+//                issuers release a stage through commits (K after S, V after
+//                PV).
 //  * warps 1, 2  one lane each issues the tcgen05 MMAs of one tile x:
 //                S_x(0), then per block j: O_x += P_x(j) V_j, S_x(j+1). Two
 //                issuing threads are needed: one thread issuing 128x128x16
@@ -267,16 +269,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       for (int j = 0; ok && j < n_blocks; ++j) {
         const int st = j & 1;
+        const bool more = (j + 1 < n_blocks);
+        // V_j and K_{j+1} normally landed long ago: check them before the
+        // softmax's P, so that PV and the next S issue back to back
         if (!mbar_wait(&v_full[st], (j >> 1) & 1, &abort_flag)) break;
+        if (more && !mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, &abort_flag)) break;
         if (!mbar_wait(&p_full[x], j & 1, &abort_flag)) break;
         tc_fence_after_sync();
         issue_pv(j);
         umma_commit(&v_empty[st]);
-        if (j + 1 < n_blocks) {
-          if (!mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, &abort_flag)) break;
-          tc_fence_after_sync();
+        if (more) {
           issue_s(j + 1);
-          umma_commit(&s_full[x]);
+          umma_commit(&s_full[x]);  // also reports O_x += P_x(j) V_j done
           umma_commit(&k_empty[(j + 1) & 1]);
         }
       }
@@ -326,16 +330,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (key < lo || key > row_end) sr[c] = __float_as_uint(-INFINITY);
         }
       }
-      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+      // row max of the raw scores: four chains of three-input max
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 4; c < kBlockN; c += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+      for (int c = 0; c < kBlockN; c += 8) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          mx[u] = max3f(mx[u], __uint_as_float(sr[c + 2 * u]), __uint_as_float(sr[c + 2 * u + 1]));
       }
-      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+      const float m_new = fmaxf(m, max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2);
       const bool grow_o = (m != -INFINITY) && (m_new > m + kRescaleThreshold);
       float alpha = 1.f;
       if (m == -INFINITY) {
@@ -346,21 +349,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m = m_new;
       }
       const float mref = (m == -INFINITY) ? 0.f : m;
-      float rs0 = 0.f, rs1 = 0.f;
+      // p = 2^(scale*log2(e)*s - m): one packed FMA per pair, ex2 per element,
+      // row sum in two packed accumulators
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float e0 = ex2(fmaf(__uint_as_float(sr[64 * h2 + 2 * c]), sl2, -mref));
-          const float e1 = ex2(fmaf(__uint_as_float(sr[64 * h2 + 2 * c + 1]), sl2, -mref));
-          rs0 += e0;
-          rs1 += e1;
+          float a0, a1;
+          fma2(a0, a1, __uint_as_float(sr[64 * h2 + 2 * c]), __uint_as_float(sr[64 * h2 + 2 * c + 1]), sl2, -mref);
+          const float e0 = ex2(a0);
+          const float e1 = ex2(a1);
+          add2(rs[2 * (c & 1)], rs[2 * (c & 1) + 1], e0, e1);
           pk[c] = pack_bf16x2(e0, e1);
         }
         tmem_st32(t_s + 32 * h2, pk);
       }
-      l += rs0 + rs1;
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       if (__any_sync(0xffffffffu, grow_o)) {
         // O_x holds P_x(j-1) V_{j-1} (complete before S_x(j) was reported) and
         // nothing newer: rescale it before O_x += P_x(j) V_j is issued
