@@ -60,6 +60,28 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def measured_traffic(workload: str, subset: bool):
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, or None when the workload differs or the kernel sources changed
+    since the capture."""
+    path = os.path.join(ROOT, "profiles", "attn_fwd_tc_t8192_traffic.md")
+    if subset or workload != W.CONFIGS[1].name or not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    try:
+        traffic = int(txt.split("traffic_bytes_per_launch:")[1].split()[0])
+        want = txt.split("source_sha256:")[1].split()[0]
+        files = txt.split("source_files:")[1].splitlines()[0].split()
+    except (IndexError, ValueError):
+        return None
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "context_packed_thd_gb300", f), "rb") as fh:
+            h.update(fh.read())
+    return traffic if h.hexdigest() == want else None
+
+
 def rank_pairs(idx: np.ndarray, lay: W.Layout) -> int:
     """Unmasked (query, key) pairs of one rank's slice, per head: a row at
     position pos of a document sees pos + 1 keys; pad rows see none."""
@@ -402,7 +424,8 @@ def run_cuda(args):
                         "note": "partition index + one reorder launch of Q and the int64 ids, timed together per rank"},
             "reorder_activations": act,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "frac": round(achieved / peak, 4),
+                         "traffic": measured_traffic(cfg.name, args.strategy is not None or args.rank is not None),
                          "kernel": "thd_causal_attn_fwd (timed per call: row-group metadata, group order, attention kernel)",
                          "peak_source": f"{peak_src} bf16_tflops (burst)"},
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
