@@ -62,6 +62,7 @@ constexpr int kRegsSoftmax = 224;  // warpgroups 1 and 2
 static_assert(kRegsControl * 128 + kRegsSoftmax * 256 <= 168 * kAttnThreads, "register split exceeds the launch");
 constexpr int kStages = 2;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 256x
+constexpr float kMaskShift = 1.2676506e30f;  // 2^100: subtracted from masked scores
 
 template <int D>
 struct AttnSmem {
@@ -321,13 +322,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint32_t sr[kBlockN];
       tmem_ld128(t_s, sr);
       tmem_ld_wait128(sr);
-      const int row_end = min(hi, kend);
       const bool full = (kstart >= tmax_lo) && (kstart + kBlockN - 1 <= min(tmin_hi, kend));
       if (!full) {
+        // allowed columns of this row: [c_lo, c_hi] (empty when c_lo > c_hi)
+        const int c_lo = min(max(lo - kstart, 0), kBlockN);
+        const int c_hi = max(min(min(hi, kend) - kstart, kBlockN - 1), -1);
+        const bool cut_lo = __any_sync(0xffffffffu, c_lo > 0);
+        const bool cut_hi = __any_sync(0xffffffffu, c_hi < kBlockN - 1);
+        // The mask runs on the FMA pipe: u = saturate(c - c_hi) is 1 exactly
+        // for columns past the row's last key (c is an integer), and
+        // s - u * 2^100 pushes them far below any real score; likewise for
+        // columns before its first key. A row left with no key in this block
+        // is caught after the max (below), so no two huge values are ever
+        // subtracted from each other.
+        const float f_hi = static_cast<float>(c_hi), f_lo = static_cast<float>(c_lo);
+        if (cut_hi) {
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c) {
-          const int key = kstart + c;
-          if (key < lo || key > row_end) sr[c] = __float_as_uint(-INFINITY);
+          for (int c = 0; c < kBlockN; ++c)
+            sr[c] = __float_as_uint(fmaf(__saturatef(static_cast<float>(c) - f_hi), -kMaskShift, __uint_as_float(sr[c])));
+        }
+        if (cut_lo) {
+#pragma unroll
+          for (int c = 0; c < kBlockN; ++c)
+            sr[c] = __float_as_uint(fmaf(__saturatef(f_lo - static_cast<float>(c)), -kMaskShift, __uint_as_float(sr[c])));
         }
       }
       // row max of the raw scores: four chains of three-input max
@@ -338,7 +355,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int u = 0; u < 4; ++u)
           mx[u] = max3f(mx[u], __uint_as_float(sr[c + 2 * u]), __uint_as_float(sr[c + 2 * u + 1]));
       }
-      const float m_new = fmaxf(m, max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2);
+      float mx_row = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      if (mx_row < -0.5f * kMaskShift) mx_row = -INFINITY;  // no key of this row in this block
+      const float m_new = fmaxf(m, mx_row * sl2);
       const bool grow_o = (m != -INFINITY) && (m_new > m + kRescaleThreshold);
       float alpha = 1.f;
       if (m == -INFINITY) {
