@@ -215,6 +215,76 @@ class Strategy:
         self.run_attn(cp, r)
 
 
+def _graph_ms(fn, flush, reps=5):
+    """Median device time of ``fn`` captured as a CUDA graph (L2 flushed before each replay)."""
+    fn()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        ev0.record(stream)
+        g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(ev0.elapsed_time(ev1))
+    return statistics.median(ms)
+
+
+def kv_restore(cp, cfg, st, flush, dev, hbm_peak):
+    """Restore of all-gathered K and V (rank-major) to token order: the
+    gathered buffers are simulated on one GPU, the restore is one reorder
+    launch of both tensors through cp_restore_index."""
+    d = st.dev
+    idx_all = cp.cp_partition_index(st.name, d["cup"], st.T, cfg.cp, -1)
+    kg, vg = cp.cp_reorder(d["k"], idx_all), cp.cp_reorder(d["v"], idx_all)
+    restore = cp.cp_restore_index(st.name, d["cup"], st.T, cfg.cp)
+    ko, vo = torch.empty_like(kg), torch.empty_like(vg)
+    ms = _graph_ms(lambda: cp.cp_reorder_multi([kg, vg], restore, outs=[ko, vo], err=st.err), flush)
+    ok = torch.equal(ko.view(torch.int16), d["k"].view(torch.int16)) and torch.equal(vo.view(torch.int16),
+                                                                                     d["v"].view(torch.int16))
+    row = cfg.hkv * cfg.d * 2
+    nbytes = st.T * (2 * 2 * row + 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"strategy": st.name, "GB/s": round(gbs, 1), "peak_GB/s": hbm_peak, "frac": round(gbs / hbm_peak, 4),
+            "ms": round(ms, 5), "bytes": nbytes, "bit_exact": bool(ok)}
+
+
+def dcs_two_launch(cp, cfg, st, ranks, flush):
+    """Matched-input comparison: a DualChunkSwap rank's attention as one launch
+    over its whole slice against two launches, one per owned chunk (the two
+    attention steps the pages describe), on the same inputs."""
+    d = st.dev
+    lay = st.lay
+    lcu = lay.cu_seqlens_padded.astype(np.int64) // cfg.cp
+    halves = [[], []]
+    for j in range(lay.num_docs):
+        c = (lcu[j + 1] - lcu[j]) // 2
+        halves[0].append(np.arange(lcu[j], lcu[j] + c))
+        halves[1].append(np.arange(lcu[j] + c, lcu[j + 1]))
+    rows = [np.concatenate(h).astype(np.int64) for h in halves]
+    fused, split = [], []
+    for r in ranks:
+        idx_h = [st.idx[r][torch.from_numpy(x).to(st.idx[r].device)].contiguous() for x in rows]
+        q_h = [st.q_loc[r][torch.from_numpy(x).to(st.q_loc[r].device)].contiguous() for x in rows]
+        out_h = [torch.empty_like(q) for q in q_h]
+        lse_h = [torch.empty((cfg.hq, q.shape[0]), dtype=torch.float32, device=q.device) for q in q_h]
+        ws_h = [torch.empty(cp.thd_causal_attn_workspace_size(q.shape[0], cfg.hq, cfg.hkv, cfg.d), dtype=torch.uint8,
+                            device=q.device) for q in q_h]
+
+        def two():
+            for h in range(2):
+                cp.thd_causal_attn_fwd(idx_h[h], q_h[h], d["k"], d["v"], d["cu"], d["cup"], out=out_h[h],
+                                       lse=lse_h[h], workspace=ws_h[h], err=st.err)
+        fused.append(_graph_ms(lambda: st.run_attn(cp, r), flush, reps=3))
+        split.append(_graph_ms(two, flush, reps=3))
+    return {"attn_ms_one_launch": round(sum(fused), 5), "attn_ms_two_launches": round(sum(split), 5),
+            "two_over_one": round(sum(split) / sum(fused), 3), "ranks": len(ranks)}
+
+
 def activation_reorder(cp, cfg, st, ranks, flush, dev, hbm_peak):
     """Reorder of the workload's [T, width] bf16 activations into every rank's
     token order (graph replays, L2 flushed before each)."""
@@ -259,6 +329,8 @@ def run_cuda(args):
     dev = torch.device("cuda", local_rank)
     cfg = W.CONFIG_BY_NAME[args.workload]
     names = [s for s in cfg.strategies if args.strategy in (None, s)]
+    if args.strategy == W.PACKED_MIRRORED:
+        names = [W.PACKED_MIRRORED]
     if not names:
         raise SystemExit(f"workload {cfg.name} does not run strategy {args.strategy}")
     strategies = [Strategy(cp, cfg, s, dev) for s in names]
@@ -371,6 +443,9 @@ def run_cuda(args):
     reorder_bytes = sum(st.reorder_bytes * len(ranks) for st in strategies)
     prep_total_ms = sum(med_prep)
     act = activation_reorder(cp, cfg, strategies[0], ranks, flush, dev, hbm_peak) if cfg.act_width else None
+    dcs_st = [st for st in strategies if st.name == W.DUAL_CHUNK_SWAP]
+    restore = kv_restore(cp, cfg, dcs_st[0], flush, dev, hbm_peak) if dcs_st and not args.no_extras else None
+    two = dcs_two_launch(cp, cfg, dcs_st[0], ranks, flush) if dcs_st and not args.no_extras else None
 
     # ---- end to end: pinned host inputs -> step -> host results --------------
     e2e_steps = max(1, min(args.steps, 10))
@@ -423,6 +498,8 @@ def run_cuda(args):
                         "bytes_per_step": reorder_bytes,
                         "note": "partition index + one reorder launch of Q and the int64 ids, timed together per rank"},
             "reorder_activations": act,
+            "kv_restore": restore,
+            "dcs_one_vs_two_launches": two,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4),
                          "traffic": measured_traffic(cfg.name, args.strategy is not None or args.rank is not None),
@@ -518,7 +595,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.CONFIG_BY_NAME))
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--strategy", choices=list(W.STRATEGIES), default=None,
+    ap.add_argument("--no-extras", action="store_true", help="skip the K/V restore and one-vs-two-launch measurements")
+    ap.add_argument("--strategy", choices=list(W.ALL_STRATEGIES), default=None,
                     help="time one strategy only (profiling); the headline runs every strategy")
     ap.add_argument("--rank", type=int, default=None,
                     help="time one context-parallel rank only (profiling); the headline runs every rank")

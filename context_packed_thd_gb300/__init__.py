@@ -15,14 +15,16 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "DUAL_CHUNK_SWAP", "NO_LOAD_BALANCE", "CpthdError", "LIB_PATH", "lib",
-    "cpthd_status_string", "cp_local_tokens", "cp_partition_index", "cp_reorder", "cp_reorder_multi",
+    "DUAL_CHUNK_SWAP", "NO_LOAD_BALANCE", "PACKED_MIRRORED", "CpthdError", "LIB_PATH", "lib",
+    "cpthd_status_string", "cp_local_tokens", "cp_partition_index", "cp_restore_index", "cp_reorder",
+    "cp_reorder_multi",
     "thd_causal_attn_workspace_size", "thd_causal_attn_fwd", "thd_causal_attn_fwd_static_scratch",
     "get_batch_on_this_cp_rank", "strategy_code",
 ]
 
 DUAL_CHUNK_SWAP = 0
 NO_LOAD_BALANCE = 1
+PACKED_MIRRORED = 2
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcpthd.so")
 
@@ -55,6 +57,8 @@ lib.cp_local_tokens.argtypes = [_i32, _i64, _i32, ctypes.POINTER(_i64)]
 lib.cp_local_tokens.restype = _i32
 lib.cp_partition_index.argtypes = [_i32, _vp, _i32, _i64, _i32, _i32, _vp, _vp, _vp]
 lib.cp_partition_index.restype = _i32
+lib.cp_restore_index.argtypes = [_i32, _vp, _i32, _i64, _i32, _vp, _vp, _vp]
+lib.cp_restore_index.restype = _i32
 lib.cp_reorder.argtypes = [_vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp]
 lib.cp_reorder.restype = _i32
 lib.cp_reorder_multi.argtypes = [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_i64), _i64, _vp,
@@ -92,6 +96,8 @@ def strategy_code(strategy) -> int:
             return DUAL_CHUNK_SWAP
         if s in ("nlb", "no_load_balance"):
             return NO_LOAD_BALANCE
+        if s in ("mirrored", "packed_mirrored"):
+            return PACKED_MIRRORED
         raise ValueError(f"unknown strategy {strategy!r}")
     return int(strategy)
 
@@ -131,6 +137,20 @@ def cp_partition_index(strategy, cu_seqlens_padded: torch.Tensor, T: int, cp_siz
     _check(lib.cp_partition_index(strategy_code(strategy), _ptr(cu_seqlens_padded), cu_seqlens_padded.numel() - 1,
                                   int(T), int(cp_size), int(rank), _ptr(out), _ptr(err), _stream(stream)),
            "cp_partition_index")
+    return out
+
+
+def cp_restore_index(strategy, cu_seqlens_padded: torch.Tensor, T: int, cp_size: int,
+                     out: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """int32 [T]: row of the rank-major all-gathered buffer holding each physical slot."""
+    _need_cuda(cu_seqlens_padded, out, err)
+    assert cu_seqlens_padded.dtype == torch.int32 and cu_seqlens_padded.is_contiguous()
+    if out is None:
+        out = torch.empty(int(T), dtype=torch.int32, device=cu_seqlens_padded.device)
+    assert out.numel() >= T and out.dtype == torch.int32
+    _check(lib.cp_restore_index(strategy_code(strategy), _ptr(cu_seqlens_padded), cu_seqlens_padded.numel() - 1,
+                                int(T), int(cp_size), _ptr(out), _ptr(err), _stream(stream)), "cp_restore_index")
     return out
 
 

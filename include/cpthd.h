@@ -61,8 +61,10 @@ extern "C" {
 typedef struct CUstream_st* cpthd_stream_t; /* == cudaStream_t */
 
 typedef enum {
-  CPTHD_DUAL_CHUNK_SWAP = 0, /* default strategy */
-  CPTHD_NO_LOAD_BALANCE = 1  /* experimental strategy */
+  CPTHD_DUAL_CHUNK_SWAP = 0,  /* default strategy */
+  CPTHD_NO_LOAD_BALANCE = 1,  /* experimental strategy */
+  CPTHD_PACKED_MIRRORED = 2   /* the PR's interim "packed super-sequence": the whole buffer as one
+                                 sequence cut into 2*cp_size mirrored chunks */
 } cpthd_strategy_t;
 
 enum {
@@ -82,10 +84,11 @@ enum {
 /* Human-readable name of a status code (static storage, never NULL). */
 CPTHD_API const char* cpthd_status_string(int status);
 
-/* Tokens every rank holds: T / cp_size under either strategy (TE PR, "Scope
+/* Tokens every rank holds: T / cp_size under every strategy (TE PR, "Scope
  * and constraints": equal local Q/K/V physical lengths).
  * Host only, launches nothing. Errors: INVALID_ARG (cp_size < 1, T < 0,
- * null output, unknown strategy), NOT_DIVISIBLE (T % cp_size != 0). */
+ * null output, unknown strategy), NOT_DIVISIBLE (T % cp_size != 0, or
+ * T % (2*cp_size) != 0 for PACKED_MIRRORED). */
 CPTHD_API int cp_local_tokens(int strategy, int64_t T, int cp_size, int64_t* t_local_host);
 
 /* Partition index: the physical token indices a CP rank owns (TE PR,
@@ -95,8 +98,13 @@ CPTHD_API int cp_local_tokens(int strategy, int64_t T, int cp_size, int64_t* t_l
  *     cup[j] + (2*cp_size-1-r)*c_j + t (t < c_j). The rank-local offsets are
  *     therefore cu_seqlens_padded / cp_size. Needs every P_j % (2*cp_size) == 0.
  *   NO_LOAD_BALANCE: slots rank*T/cp_size + t. Needs T % cp_size == 0.
- * cu_seqlens_padded_dev: int32 [num_docs+1], device, read only (NLB reads it
- *   only to validate cup[num_docs] == T).
+ *   PACKED_MIRRORED (TE PR commit notes: the complete physical buffer
+ *     represented as one partitioning sequence, mirrored chunks, document
+ *     boundaries kept by the attention's sequence metadata): DUAL_CHUNK_SWAP
+ *     applied to the single sequence [0, T). Needs T % (2*cp_size) == 0, not
+ *     per-document divisibility.
+ * cu_seqlens_padded_dev: int32 [num_docs+1], device, read only (NLB and
+ *   PACKED_MIRRORED read it only to validate it).
  * rank: 0..cp_size-1 writes T/cp_size indices; -1 writes all ranks,
  *   rank-major, cp_size*(T/cp_size) = T indices.
  * idx_out_dev: int32, device, caller-allocated, size as above.
@@ -104,6 +112,17 @@ CPTHD_API int cp_local_tokens(int strategy, int64_t T, int cp_size, int64_t* t_l
 CPTHD_API int cp_partition_index(int strategy, const int32_t* cu_seqlens_padded_dev, int num_docs, int64_t T,
                        int cp_size, int rank, int32_t* idx_out_dev, int32_t* err_dev,
                        cpthd_stream_t stream);
+
+/* K/V restore index: after an all-gather of every rank's slice, rank-major
+ * (gathered[r*T/cp_size + t] = x[index of rank r][t]), restore_idx[p] is the
+ * row of the gathered buffer that holds physical slot p, so that
+ * cp_reorder(gathered, restore_idx) brings K/V back to token order (TE PR,
+ * Greptile summary: "stable K/V restoration"; commit notes: rank-major
+ * ownership needs no KV reorder). NO_LOAD_BALANCE gives the identity.
+ * restore_idx_out_dev: int32 [T], device, caller-allocated.
+ * Device checks (err_dev): as cp_partition_index. */
+CPTHD_API int cp_restore_index(int strategy, const int32_t* cu_seqlens_padded_dev, int num_docs, int64_t T,
+                               int cp_size, int32_t* restore_idx_out_dev, int32_t* err_dev, cpthd_stream_t stream);
 
 /* Reorder: dst[i, :] = src[idx[i], :] for i < n_rows, byte for byte, for
  * any row width (TE PR "How to use": input_ids, labels, position_ids and

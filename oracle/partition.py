@@ -25,6 +25,7 @@ from typing import List, Sequence
 
 DUAL_CHUNK_SWAP = "dcs"
 NO_LOAD_BALANCE = "nlb"
+PACKED_MIRRORED = "mirrored"
 
 
 class PartitionError(ValueError):
@@ -71,13 +72,39 @@ def no_load_balance_indices(T: int, cp_size: int, rank: int) -> List[int]:
     return out
 
 
+def packed_mirrored_indices(T: int, cp_size: int, rank: int) -> List[int]:
+    """The PR's interim packed super-sequence partition (commit notes: the
+    complete physical token buffer represented as one partitioning sequence,
+    mirrored chunks): DualChunkSwap of the single sequence [0, T)."""
+    if T % (2 * cp_size) != 0:
+        raise PartitionError("T must be divisible by 2*cp_size")
+    return dual_chunk_swap_indices([0, T], cp_size, rank)
+
+
 def partition_index(strategy: str, cu_seqlens_padded: Sequence[int], cp_size: int, rank: int) -> List[int]:
     T = int(cu_seqlens_padded[-1])
     if strategy == DUAL_CHUNK_SWAP:
         return dual_chunk_swap_indices(cu_seqlens_padded, cp_size, rank)
     if strategy == NO_LOAD_BALANCE:
         return no_load_balance_indices(T, cp_size, rank)
+    if strategy == PACKED_MIRRORED:
+        return packed_mirrored_indices(T, cp_size, rank)
     raise PartitionError(f"unknown strategy {strategy!r}")
+
+
+def restore_index(strategy: str, cu_seqlens_padded: Sequence[int], cp_size: int) -> List[int]:
+    """K/V restoration after an all-gather (TE PR, Greptile summary: "stable
+    K/V restoration"): the gathered buffer is the rank-major concatenation of
+    the ranks' index lists; restore[p] is the position of physical slot p in
+    that concatenation, so gathered[restore] is back in token order."""
+    T = int(cu_seqlens_padded[-1])
+    concat: List[int] = []
+    for r in range(cp_size):
+        concat += partition_index(strategy, cu_seqlens_padded, cp_size, r)
+    restore = [-1] * T
+    for pos, p in enumerate(concat):
+        restore[p] = pos
+    return restore
 
 
 def local_cu_seqlens_padded(cu_seqlens_padded: Sequence[int], cp_size: int) -> List[int]:

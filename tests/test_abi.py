@@ -29,7 +29,7 @@ def cp():
 
 def test_every_declared_symbol_is_exported(cp):
     names = _declared()
-    assert {"cp_partition_index", "cp_reorder", "cp_reorder_multi", "thd_causal_attn_fwd",
+    assert {"cp_partition_index", "cp_restore_index", "cp_reorder", "cp_reorder_multi", "thd_causal_attn_fwd",
             "thd_causal_attn_workspace_size", "cp_local_tokens", "cpthd_status_string"} <= set(names)
     raw = ctypes.CDLL(cp.LIB_PATH)
     for n in names:
@@ -44,6 +44,10 @@ def test_binding_names_match_abi(cp):
 def test_local_tokens(cp):
     assert cp.cp_local_tokens("dcs", 132, 2) == 66
     assert cp.cp_local_tokens("nlb", 131072, 16) == 8192
+    assert cp.cp_local_tokens("mirrored", 128, 2) == 64
+    with pytest.raises(cp.CpthdError) as e:
+        cp.cp_local_tokens("mirrored", 132, 4)      # divisible by 4, not by 8
+    assert e.value.status == -2
     with pytest.raises(cp.CpthdError) as e:
         cp.cp_local_tokens("nlb", 130, 4)
     assert e.value.status == -2

@@ -62,7 +62,7 @@ def _sample_rows(lay, ref_idx, cpsize, rng, n_random=40):
 
 
 @pytest.mark.parametrize("name", ["tiny", "t8192_mha16"])
-@pytest.mark.parametrize("strategy", ["dcs", "nlb"])
+@pytest.mark.parametrize("strategy", ["dcs", "nlb", "mirrored"])
 def test_small_configs_all_rows(name, strategy):
     dev = cuda_or_skip(); cp = load_lib()
     cfg = W.CONFIG_BY_NAME[name]
@@ -82,6 +82,7 @@ def test_small_configs_all_rows(name, strategy):
 
 @pytest.mark.parametrize("name,strategy", [
     ("t32768_lognormal_gqa32x8", "dcs"), ("t32768_lognormal_gqa32x8", "nlb"),
+    ("t32768_lognormal_gqa32x8", "mirrored"),
     ("padded48_gqa32x8", "dcs"),
     ("long131072_h8", "dcs"), ("long131072_h8", "nlb"),
 ])

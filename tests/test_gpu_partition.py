@@ -63,3 +63,55 @@ def test_partition_device_checks():
     err = new_err(dev)
     cp.cp_partition_index("dcs", cup, 16, 2, 0, err=err)
     assert err.cpu().tolist()[0] == -6
+
+
+@pytest.mark.parametrize("cfg", W.CONFIGS, ids=lambda c: c.name)
+def test_packed_mirrored_every_config(cfg):
+    dev = cuda_or_skip(); cp = load_lib()
+    lay = W.layout_for(cfg, "mirrored")
+    if lay.T % (2 * cfg.cp):
+        pytest.skip("T not divisible by 2*cp_size")
+    cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
+    err = new_err(dev)
+    for r in range(cfg.cp):
+        got = cp.cp_partition_index("mirrored", cup, lay.T, cfg.cp, r, err=err).cpu().numpy()
+        ref = np.asarray(P.partition_index("mirrored", lay.cu_seqlens_padded.tolist(), cfg.cp, r), dtype=np.int32)
+        assert np.array_equal(got, ref)
+    assert err.cpu().tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("cfg", W.CONFIGS, ids=lambda c: c.name)
+def test_restore_index_every_config(cfg):
+    dev = cuda_or_skip(); cp = load_lib()
+    for s in W.ALL_STRATEGIES:
+        if s not in cfg.strategies and s != "mirrored":
+            continue
+        lay = W.layout_for(cfg, s)
+        if s == "mirrored" and lay.T % (2 * cfg.cp):
+            continue
+        cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
+        err = new_err(dev)
+        got = cp.cp_restore_index(s, cup, lay.T, cfg.cp, err=err).cpu().numpy()
+        ref = np.asarray(P.restore_index(s, lay.cu_seqlens_padded.tolist(), cfg.cp), dtype=np.int32)
+        assert np.array_equal(got, ref), s
+        assert err.cpu().tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("name,strategy", [("long131072_h8", "dcs"), ("padded48_gqa32x8", "dcs"),
+                                           ("t32768_lognormal_gqa32x8", "mirrored"),
+                                           ("t32768_lognormal_gqa32x8", "nlb")])
+def test_kv_restore_round_trip_full_size(name, strategy):
+    """Simulated all-gather of every rank's K slice (rank-major), then the
+    restore gather: K comes back bit for bit."""
+    dev = cuda_or_skip(); cp = load_lib()
+    cfg = W.CONFIG_BY_NAME[name]
+    lay = W.layout_for(cfg, strategy)
+    cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
+    k = W.make_activations(cfg.seed, lay.T, cfg.hkv * cfg.d, device="cuda:0")
+    err = new_err(dev)
+    idx_all = cp.cp_partition_index(strategy, cup, lay.T, cfg.cp, -1, err=err)
+    gathered = cp.cp_reorder(k, idx_all, err=err)
+    restore = cp.cp_restore_index(strategy, cup, lay.T, cfg.cp, err=err)
+    back = cp.cp_reorder(gathered, restore, err=err)
+    assert torch.equal(back.view(torch.int16), k.view(torch.int16))
+    assert err.cpu().tolist() == [0, 0]

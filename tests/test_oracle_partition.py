@@ -145,3 +145,44 @@ def test_every_config_partitions():
                 assert len(lst) == n
                 seen[np.asarray(lst)] += 1
             assert (seen == 1).all()
+
+
+def _restore_cases():
+    return _golden()["restore"]["cases"]
+
+
+@pytest.mark.parametrize("case", _restore_cases(), ids=lambda c: c["note"][:40])
+def test_restore_hand_worked(case):
+    assert P.restore_index(case["strategy"], case["cu_seqlens_padded"], case["cp_size"]) == case["restore"]
+
+
+@pytest.mark.parametrize("strategy", ["dcs", "nlb", "mirrored"])
+@pytest.mark.parametrize("cp", [1, 2, 3, 4])
+def test_restore_round_trip(strategy, cp):
+    """Gathering every rank's slice rank-major and then reading it through the
+    restore index gives back the token order; for NO_LOAD_BALANCE the restore
+    index is the identity (no K/V reorder)."""
+    rng = np.random.default_rng(31 * cp)
+    for _ in range(4):
+        pad = 2 * cp if strategy == "dcs" else 1
+        lay = W.random_layout(rng, int(rng.integers(1, 6)), 50, pad, allow_empty=True)
+        cup = lay.cu_seqlens_padded.tolist()
+        mult = 2 * cp if strategy == "mirrored" else cp
+        if cup[-1] % mult:
+            continue
+        x = rng.integers(0, 1 << 30, size=cup[-1])
+        gathered = np.concatenate([x[P.partition_index(strategy, cup, cp, r)] for r in range(cp)])
+        restore = P.restore_index(strategy, cup, cp)
+        assert np.array_equal(gathered[restore], x)
+        if strategy == "nlb":
+            assert restore == list(range(cup[-1]))
+
+
+@pytest.mark.parametrize("cp", [1, 2, 4, 8])
+def test_mirrored_is_head_tail_of_whole_buffer(cp):
+    T = 2 * cp * 7
+    pieces = np.array_split(np.arange(T), 2 * cp)
+    cup = [0, 3, 10, T]          # document boundaries do not matter
+    for r in range(cp):
+        expect = np.concatenate([pieces[r], pieces[2 * cp - 1 - r]]).tolist()
+        assert P.partition_index("mirrored", cup, cp, r) == expect

@@ -21,7 +21,8 @@ Layouts
 * ``padded``: every document padded up to a multiple of ``pad_multiple``
   (`cu_seqlens_padded`); pad slots hold zeros (bf16) or -1 (int64 ids).
   DualChunkSwap runs on the padded layout with ``pad_multiple = 2*cp_size``;
-  NO_LOAD_BALANCE runs on the logical layout (``pad_between_seqs=False``).
+  NO_LOAD_BALANCE and the packed mirrored partition run on the logical layout
+  (``pad_between_seqs=False``).
 """
 from __future__ import annotations
 
@@ -34,7 +35,9 @@ import torch
 
 DUAL_CHUNK_SWAP = "dcs"
 NO_LOAD_BALANCE = "nlb"
+PACKED_MIRRORED = "mirrored"
 STRATEGIES = (DUAL_CHUNK_SWAP, NO_LOAD_BALANCE)
+ALL_STRATEGIES = (DUAL_CHUNK_SWAP, NO_LOAD_BALANCE, PACKED_MIRRORED)
 
 
 @dataclasses.dataclass(frozen=True)
