@@ -60,6 +60,29 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def dist_env():
+    """(world_size, rank, local_rank) from the torchrun environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of ``x`` over all ranks (a time: the slowest replica
+    counts). Identity without an initialised process group."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(units_per_replica: float, world: int, seconds: float) -> float:
+    """Whole-job throughput of ``world`` replicas that each did the same work
+    in at most ``seconds`` (weak scaling)."""
+    return world * units_per_replica / seconds
+
+
 def measured_traffic(workload: str, subset: bool):
     """Per-launch DRAM bytes of the attention kernel from the committed ncu
     summary, or None when the workload differs or the kernel sources changed
@@ -319,9 +342,7 @@ def activation_reorder(cp, cfg, st, ranks, flush, dev, hbm_peak):
 def run_cuda(args):
     import context_packed_thd_gb300 as cp
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local_rank = dist_env()
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
@@ -396,11 +417,8 @@ def run_cuda(args):
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     total_ms = sum(step_ms)
     flops_step = sum(st.flops[r] for st in strategies for r in ranks)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(total_ms, dev)
+    value = replica_value(flops_step * args.steps, world, total_ms * 1e-3) / 1e12
 
     # ---- each part of the step alone (graph replays, L2 flushed before each) --
     reps = max(3, min(args.steps, 10))
@@ -465,11 +483,8 @@ def run_cuda(args):
                 st.lse_host[r].copy_(st.lse[r], non_blocking=True)
         torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = world * flops_step / e2e_s / 1e12
+    e2e_s = max_over_ranks(e2e_s, dev)
+    e2e_value = replica_value(flops_step, world, e2e_s) / 1e12
 
     for st in strategies:
         e = st.err.cpu().tolist()
@@ -556,8 +571,7 @@ def cpu_baseline(cfg, seconds):
 
 
 def run_reference(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    world, rank, _ = dist_env()
     if rank != 0:
         return
     cfg = W.CONFIG_BY_NAME[args.workload]
