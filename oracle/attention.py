@@ -166,3 +166,67 @@ def unmasked_pairs(idx, cu_seqlens, cu_seqlens_padded) -> int:
     sum over real rows of (pos + 1)."""
     j, pos, valid = locate_rows(idx, cu_seqlens, cu_seqlens_padded)
     return int((pos[valid] + 1).sum())
+
+
+def attention_bwd(q_local, k, v, cu_seqlens, cu_seqlens_padded, idx, dout, scale: Optional[float] = None,
+                  block_rows: int = 1024):
+    """Oracle backward of ``attention_fwd`` for one rank's query slice.
+
+    The forward is recomputed here in float64 (out and lse from the
+    definition), then, for every allowed pair (i, u) of a row i with keys u:
+      P    = exp(s - lse_i)
+      D_i  = <dout_i, out_i>
+      dV_u += P dout_i
+      dS   = P (<dout_i, v_u> - D_i)
+      dQ_i += scale dS k_u,   dK_u += scale dS q_i
+    (the gradients of sum(dout * out) with respect to q, k, v). K/V heads
+    collect the gradients of every query head of their group. dK and dV cover
+    the whole buffer [T, Hkv, d] and hold this rank's contribution only (the
+    part a reduce-scatter over CP ranks would sum; TE PR: backward reuses the
+    forward's layout).
+    Returns (dq [T_loc, Hq, d], dk [T, Hkv, d], dv [T, Hkv, d]) float64.
+    """
+    Q = _f64(q_local)
+    K = _f64(k)
+    V = _f64(v)
+    dO = _f64(dout)
+    idx = np.asarray(idx, dtype=np.int64)
+    T_loc, Hq, d = Q.shape
+    Hkv = K.shape[1]
+    g = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = np.zeros_like(Q)
+    dk = np.zeros_like(K)
+    dv = np.zeros_like(V)
+    if T_loc == 0:
+        return dq, dk, dv
+    cup = np.asarray(cu_seqlens_padded, dtype=np.int64)
+    j, pos, valid = locate_rows(idx, cu_seqlens, cu_seqlens_padded)
+    for doc in np.unique(j[valid]):
+        members = np.nonzero(valid & (j == doc))[0]
+        start = int(cup[doc])
+        for b0 in range(0, members.shape[0], block_rows):
+            mb = members[b0:b0 + block_rows]
+            p = pos[mb]
+            nk = int(p.max()) + 1
+            allowed = np.arange(nk)[None, :] <= p[:, None]
+            for h in range(Hq):
+                kvh = h // g
+                qh = Q[mb, h, :]
+                kh = K[start:start + nk, kvh, :]
+                vh = V[start:start + nk, kvh, :]
+                doh = dO[mb, h, :]
+                s = scale * (qh @ kh.T)
+                s = np.where(allowed, s, -np.inf)
+                mx = s.max(axis=1, keepdims=True)
+                e = np.exp(s - mx)
+                P = e / e.sum(axis=1, keepdims=True)                 # exp(s - lse)
+                out = P @ vh
+                D = (doh * out).sum(axis=1, keepdims=True)
+                dP = doh @ vh.T
+                dS = P * (dP - D)                                   # zero where not allowed (P = 0)
+                dq[mb, h, :] += scale * (dS @ kh)
+                dk[start:start + nk, kvh, :] += scale * (dS.T @ qh)
+                dv[start:start + nk, kvh, :] += P.T @ doh
+    return dq, dk, dv
