@@ -19,6 +19,7 @@ __all__ = [
     "cpthd_status_string", "cp_local_tokens", "cp_partition_index", "cp_restore_index", "cp_reorder",
     "cp_reorder_multi",
     "thd_causal_attn_workspace_size", "thd_causal_attn_fwd", "thd_causal_attn_fwd_static_scratch",
+    "thd_causal_attn_bwd_workspace_size", "thd_causal_attn_bwd",
     "get_batch_on_this_cp_rank", "strategy_code",
 ]
 
@@ -69,6 +70,11 @@ lib.thd_causal_attn_workspace_size.restype = _i32
 lib.thd_causal_attn_fwd.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _f32, _vp,
                                     _vp, _vp, _sz, _vp, _vp]
 lib.thd_causal_attn_fwd.restype = _i32
+lib.thd_causal_attn_bwd_workspace_size.argtypes = [_i64, _i32, _i32, _i32, ctypes.POINTER(_sz)]
+lib.thd_causal_attn_bwd_workspace_size.restype = _i32
+lib.thd_causal_attn_bwd.argtypes = [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32,
+                                    _f32, _vp, _vp, _vp, _vp, _sz, _vp, _vp]
+lib.thd_causal_attn_bwd.restype = _i32
 lib.thd_causal_attn_fwd_static_scratch.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32,
                                                    _f32, _vp, _vp, _vp, _vp]
 lib.thd_causal_attn_fwd_static_scratch.restype = _i32
@@ -245,6 +251,45 @@ def thd_causal_attn_fwd_static_scratch(q_slice_idx: torch.Tensor, q: torch.Tenso
         cu_seqlens.numel() - 1, Hq, Hkv, d, float(softmax_scale) if softmax_scale else 0.0, _ptr(out), _ptr(lse),
         _ptr(err), _stream(stream)), "thd_causal_attn_fwd_static_scratch")
     return out, lse
+
+
+def thd_causal_attn_bwd_workspace_size(t_local: int, Hq: int, Hkv: int, d: int) -> int:
+    out = _sz(0)
+    _check(lib.thd_causal_attn_bwd_workspace_size(int(t_local), int(Hq), int(Hkv), int(d), ctypes.byref(out)),
+           "thd_causal_attn_bwd_workspace_size")
+    return int(out.value)
+
+
+def thd_causal_attn_bwd(q_slice_idx: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                        out: torch.Tensor, dout: torch.Tensor, lse: torch.Tensor, cu_seqlens: torch.Tensor,
+                        cu_seqlens_padded: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
+                        dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+                        dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        err: Optional[torch.Tensor] = None, stream=None):
+    """Gradients of sum(dout * out) for a rank's slice. Returns fp32
+    (dq [t_local, Hq, d], dk [T, Hkv, d], dv [T, Hkv, d]); dk/dv hold this
+    rank's contribution."""
+    _need_cuda(q_slice_idx, q, k, v, out, dout, lse, cu_seqlens, cu_seqlens_padded, dq, dk, dv, workspace, err)
+    t_local, Hq, d = q.shape
+    T, Hkv, _ = k.shape
+    for t in (q, k, v, out, dout):
+        assert t.dtype == torch.bfloat16 and t.is_contiguous()
+    assert lse.dtype == torch.float32 and lse.is_contiguous()
+    if dq is None:
+        dq = torch.empty((t_local, Hq, d), dtype=torch.float32, device=q.device)
+    if dk is None:
+        dk = torch.empty((T, Hkv, d), dtype=torch.float32, device=q.device)
+    if dv is None:
+        dv = torch.empty((T, Hkv, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(thd_causal_attn_bwd_workspace_size(t_local, Hq, Hkv, d), dtype=torch.uint8,
+                                device=q.device)
+    _check(lib.thd_causal_attn_bwd(_ptr(q_slice_idx), t_local, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
+                                   _ptr(lse), T, _ptr(cu_seqlens), _ptr(cu_seqlens_padded), cu_seqlens.numel() - 1,
+                                   Hq, Hkv, d, float(softmax_scale) if softmax_scale else 0.0, _ptr(dq), _ptr(dk),
+                                   _ptr(dv), _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)),
+           "thd_causal_attn_bwd")
+    return dq, dk, dv
 
 
 def get_batch_on_this_cp_rank(cu_seqlens_padded: torch.Tensor, *tensors: torch.Tensor, cp_size: int, rank: int,

@@ -1,0 +1,651 @@
+// Causal packed-THD attention backward (dQ, dK, dV) on tcgen05 (sm_103a).
+//
+// The backward of the forward in attn_fwd.cu, for one context-parallel rank:
+// the rank's query slice against the full K/V buffer, with the layout and the
+// LSE the forward produced (TransformerEngine PR #3221: the strategy is
+// captured for backward so forward and backward use the same token layout).
+// With P = exp(scale q.k - lse) over the allowed pairs and D = rowsum(dO * O):
+//   dV_k += P dO_q,   dS = P (dO_q . v_k - D_q),
+//   dQ_q += scale dS k_k,   dK_k += scale dS q_q.
+// dK and dV cover the whole [T, Hkv, d] buffer and hold this rank's
+// contribution (what a reduce-scatter across CP ranks would sum); K/V heads
+// collect every query head of their GQA group.
+//
+// No atomics: two passes, each owning its outputs.
+//  * dQ pass, one CTA per (128-row query tile, query head), walking the
+//    tile's key blocks exactly as the forward does: S = Q K^T and
+//    dP = dO V^T into TMEM, the elementwise warps turn them into dS (bf16,
+//    written back over S), then dQ += dS K with dS read from TMEM.
+//  * dK/dV pass, one CTA per (128-key tile, KV head), over every query tile
+//    whose key intervals reach the key tile and every query head of the
+//    group: S^T = K Q^T and dP^T = V dO^T into TMEM, the elementwise warps
+//    write P^T and dS^T (bf16) back over them, then dV += P^T dO and
+//    dK += dS^T Q, both accumulated in TMEM and written once.
+// Warp roles as in the forward: warp 0 TMA producer, warp 1 MMA issuer
+// (owns TMEM), warps 2-5 elementwise (thread = TMEM lane). Every wait is
+// bounded; a timeout drains, frees TMEM and records CPTHD_ERR_TIMEOUT.
+#include "attn_common.cuh"
+
+namespace cpthd {
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdMaxTiles = 2048;  // query tiles of one slice the dK/dV pass can list
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kChunk = kBlockM * 64 * 2;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = kChunks * kChunk;  // one 128-row bf16 tile of Q, dO, K or V
+  static constexpr int kCol = 4 * kBlockM * 4;    // row_lo, row_hi, lse2, D of 128 query rows
+  // dQ pass: Q, dO, K[2], V[2]
+  static constexpr int kDqBytes = 6 * kTile;
+  // dK/dV pass: K, V, Q[2], dO[2], column info[2], tile list
+  static constexpr int kDkvBytes = 6 * kTile + 2 * kCol + kBwdMaxTiles * 4;
+  static constexpr int launch(int b) { return (b + 1024 > 120 * 1024) ? b + 1024 : 120 * 1024; }
+};
+
+struct BwdParams {
+  const int32_t* row_lo;
+  const int32_t* row_hi;
+  const GroupInfo* tile_info;
+  const int2* intervals;
+  const float* lse2;  // [Hq, rows_pad]: lse * log2(e)
+  const float* dvec;  // [Hq, rows_pad]: rowsum(dO * O)
+  float* dq;
+  float* dk;
+  float* dv;
+  long long t_local;
+  long long T;
+  int Hq;
+  int Hkv;
+  int ntiles;
+  int rows_pad;
+  int max_blocks;
+  float scale;
+  float scale_log2;
+  int32_t* err;
+};
+
+// D = rowsum(dO * O) and lse * log2(e), laid out [Hq, rows_pad]; one warp per (row, head).
+template <int D>
+static __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
+                                                                  const __nv_bfloat16* __restrict__ dout,
+                                                                  const float* __restrict__ lse, long long t_local,
+                                                                  int Hq, int rows_pad, float* lse2, float* dvec) {
+  const long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= (long long)rows_pad * Hq) return;
+  const long long row = w / Hq;
+  const int h = static_cast<int>(w - row * Hq);
+  float acc = 0.f, l2 = 0.f;
+  if (row < t_local) {
+    const __nv_bfloat16* o = out + (row * Hq + h) * D;
+    const __nv_bfloat16* g = dout + (row * Hq + h) * D;
+#pragma unroll
+    for (int e = lane; e < D; e += 32) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
+    l2 = lse[(long long)h * t_local + row] * 1.4426950408889634f;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    dvec[(long long)h * rows_pad + row] = acc;
+    lse2[(long long)h * rows_pad + row] = l2;
+  }
+}
+
+__device__ __forceinline__ void umma_desc_words(uint64_t d, uint32_t& lo, uint32_t& hi) {
+  lo = static_cast<uint32_t>(d);
+  hi = static_cast<uint32_t>(d >> 32);
+}
+
+// ------------------------------------------------------------------ dQ pass
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const BwdParams p) {
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + L::kTile;
+  uint8_t* sK = smem + 2 * L::kTile;  // two stages
+  uint8_t* sV = smem + 4 * L::kTile;  // two stages
+
+  __shared__ uint64_t qdo_full, k_full[2], v_full[2], kv_empty[2], sdp_full, ds_full, dq_final, drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x / p.Hq;
+  const int h = blockIdx.x % p.Hq;
+  const int kvh = h / (p.Hq / p.Hkv);
+  const GroupInfo ti = p.tile_info[tile];
+  const int n_blocks = min(max(ti.n_blocks, 0), p.max_blocks);
+  const int2* tile_iv = p.intervals + static_cast<long long>(tile) * kBlockM;
+  const int n_iv = min(max(ti.n_intervals, 0), kBlockM);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&qdo_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(&sdp_full, 1);
+    mbar_init(&ds_full, 4);
+    mbar_init(&dq_final, 1);
+    mbar_init(&drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;  // S [0,128), dP [128,256), dQ [256, 256+D)
+
+  if (warp == 0) {
+    if (lane == 0 && n_blocks > 0) {
+      mbar_arrive_expect_tx(&qdo_full, 2 * L::kTile);
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_3d(sQ + c * L::kChunk, &tm_q, &qdo_full, c * 64, h, tile * kBlockM);
+        tma_load_3d(sDO + c * L::kChunk, &tm_do, &qdo_full, c * 64, h, tile * kBlockM);
+      }
+      BlockCursor cur;
+      cur.init(tile_iv, n_iv);
+      int issued = 0;
+      for (int i = 0; i < n_blocks; ++i) {
+        const int st = i & 1;
+        if (i >= 2 && !mbar_wait(&kv_empty[st], ((i >> 1) + 1) & 1, &abort_flag)) break;
+        mbar_arrive_expect_tx(&k_full[st], L::kTile);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sK + st * L::kTile + c * L::kChunk, &tm_k, &k_full[st], c * 64, kvh, cur.start);
+        mbar_arrive_expect_tx(&v_full[st], L::kTile);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sV + st * L::kTile + c * L::kChunk, &tm_v, &v_full[st], c * 64, kvh, cur.start);
+        issued = i + 1;
+        cur.next();
+      }
+      if (abort_flag) {
+        mbar_wait_drain(&qdo_full, 0);
+        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
+          mbar_wait_drain(&k_full[i & 1], (i >> 1) & 1);
+          mbar_wait_drain(&v_full[i & 1], (i >> 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n_blocks > 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
+      constexpr uint32_t kIdQ = idesc_bf16_f32(kBlockM, D, 0, 1);
+      uint32_t q_lo, q_hi, do_lo, do_hi, k_lo, k_hi, kmn_lo, kmn_hi, v_lo, v_hi;
+      umma_desc_words(smem_desc_sw128(smem_u32(sQ), 16, 1024), q_lo, q_hi);
+      umma_desc_words(smem_desc_sw128(smem_u32(sDO), 16, 1024), do_lo, do_hi);
+      umma_desc_words(smem_desc_sw128(smem_u32(sK), 16, 1024), k_lo, k_hi);
+      umma_desc_words(smem_desc_sw128(smem_u32(sK), L::kChunk, 1024), kmn_lo, kmn_hi);
+      umma_desc_words(smem_desc_sw128(smem_u32(sV), 16, 1024), v_lo, v_hi);
+      bool ok = mbar_wait(&qdo_full, 0, &abort_flag);
+      for (int j = 0; ok && j < n_blocks; ++j) {
+        const int st = j & 1;
+        const uint32_t so = (st * L::kTile) >> 4;
+        if (!mbar_wait(&k_full[st], (j >> 1) & 1, &abort_flag)) break;
+        if (!mbar_wait(&v_full[st], (j >> 1) & 1, &abort_flag)) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T
+          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+          umma_ss_w(tmem, q_lo + off, q_hi, k_lo + so + off, k_hi, kIdS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T
+          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+          umma_ss_w(tmem + 128, do_lo + off, do_hi, v_lo + so + off, v_hi, kIdS, kk > 0);
+        }
+        umma_commit(&sdp_full);
+        if (!mbar_wait(&ds_full, j & 1, &abort_flag)) break;
+        tc_fence_after_sync();
+        const uint32_t acc0 = (j > 0) ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ += dS K, dS from TMEM, K as the MN-major operand
+          umma_ts_w(tmem + 256, tmem + kk * 8, kmn_lo + so + ((kk * 16 * 128) >> 4), kmn_hi, kIdQ,
+                    kk > 0 ? 1u : acc0);
+        umma_commit(&kv_empty[st]);
+      }
+      umma_commit(&dq_final);
+      umma_commit(&drain);
+      mbar_wait_drain(&drain, 0);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const long long grow = static_cast<long long>(tile) * kBlockM + r;
+    const int lo = p.row_lo[grow], hi = p.row_hi[grow];
+    const float lse2 = p.lse2[(long long)h * p.rows_pad + grow];
+    const float drow = p.dvec[(long long)h * p.rows_pad + grow];
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128, t_q = tmem + lane_off + 256;
+    const float sl2 = p.scale_log2;
+    BlockCursor cur;
+    cur.init(tile_iv, n_iv);
+    bool ok = true;
+    for (int j = 0; j < n_blocks; ++j) {
+      const int kstart = cur.start, kend = cur.end;
+      cur.next();
+      if (!warp_wait(&sdp_full, j & 1, &abort_flag)) { ok = false; break; }
+      tc_fence_after_sync();
+      const int c_lo = min(max(lo - kstart, 0), kBlockN);
+      const int c_hi = max(min(min(hi, kend) - kstart, kBlockN - 1), -1);
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(t_s + 32 * c4, sv);
+        tmem_ld32(t_dp + 32 * c4, dp);
+        tmem_ld_wait(sv);
+        tmem_ld_wait(dp);
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          float ds2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = 32 * c4 + 2 * q + u;
+            const float e = ex2(fmaf(__uint_as_float(sv[2 * q + u]), sl2, -lse2));
+            const float pv = (col >= c_lo && col <= c_hi) ? e : 0.f;
+            ds2[u] = pv * (__uint_as_float(dp[2 * q + u]) - drow);
+          }
+          pk[q] = pack_bf16x2(ds2[0], ds2[1]);
+        }
+        tmem_st16(t_s + 16 * c4, pk);  // dS over S columns already read
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ds_full);
+    }
+    if (ok && n_blocks > 0) ok = warp_wait(&dq_final, 0, &abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after_sync();
+    if (ok) {
+      float* dst = p.dq + (grow * p.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        if (n_blocks > 0) {
+          tmem_ld32(t_q + 32 * c, rr);
+          tmem_ld_wait(rr);
+        }
+        if (grow < p.t_local) {
+          float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 v;
+            v.x = n_blocks > 0 ? __uint_as_float(rr[4 * q]) * p.scale : 0.f;
+            v.y = n_blocks > 0 ? __uint_as_float(rr[4 * q + 1]) * p.scale : 0.f;
+            v.z = n_blocks > 0 ? __uint_as_float(rr[4 * q + 2]) * p.scale : 0.f;
+            v.w = n_blocks > 0 ? __uint_as_float(rr[4 * q + 3]) * p.scale : 0.f;
+            d4[q] = v;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (abort_flag && threadIdx.x == 0) record_error(p.err, CPTHD_ERR_TIMEOUT, blockIdx.x);
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// --------------------------------------------------------------- dK/dV pass
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const BwdParams p) {
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + L::kTile;
+  uint8_t* sQ = smem + 2 * L::kTile;   // two stages
+  uint8_t* sDO = smem + 4 * L::kTile;  // two stages
+  uint8_t* sCol = smem + 6 * L::kTile; // two stages of {row_lo, row_hi, lse2, D} x 128
+  int* sList = reinterpret_cast<int*>(sCol + 2 * L::kCol);
+
+  __shared__ uint64_t kv_full, qdo_full[2], qdo_empty[2], sdp_full, pds_full, kv_final, drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag, list_n;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kt = blockIdx.x / p.Hkv;
+  const int g = blockIdx.x % p.Hkv;
+  const int group = p.Hq / p.Hkv;
+  const int K0 = kt * kBlockN;
+
+  // query tiles whose key intervals reach [K0, K0 + 127]
+  if (threadIdx.x == 0) list_n = 0;
+  __syncthreads();
+  for (int t = threadIdx.x; t < p.ntiles; t += blockDim.x) {
+    const GroupInfo ti = p.tile_info[t];
+    const int n_iv = min(max(ti.n_intervals, 0), kBlockM);
+    const int2* iv = p.intervals + static_cast<long long>(t) * kBlockM;
+    bool rel = false;
+    for (int k = 0; k < n_iv && !rel; ++k) {
+      const int2 a = iv[k];
+      rel = (a.x <= K0 + kBlockN - 1) && (a.y >= K0);
+    }
+    if (rel) {
+      const int slot = atomicAdd(&list_n, 1);
+      if (slot < kBwdMaxTiles) sList[slot] = t;
+    }
+  }
+  __syncthreads();
+  const int n_items = min(list_n, kBwdMaxTiles) * group;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&qdo_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
+    mbar_init(&sdp_full, 1);
+    mbar_init(&pds_full, 4);
+    mbar_init(&kv_final, 1);
+    mbar_init(&drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;  // S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D)
+
+  if (warp == 0) {
+    if (lane == 0 && n_items > 0) {
+      mbar_arrive_expect_tx(&kv_full, 2 * L::kTile);
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_3d(sK + c * L::kChunk, &tm_k, &kv_full, c * 64, g, K0);
+        tma_load_3d(sV + c * L::kChunk, &tm_v, &kv_full, c * 64, g, K0);
+      }
+      int issued = 0;
+      for (int i = 0; i < n_items; ++i) {
+        const int st = i & 1;
+        const int t = sList[i / group];
+        const int h = g * group + i % group;
+        if (i >= 2 && !mbar_wait(&qdo_empty[st], ((i >> 1) + 1) & 1, &abort_flag)) break;
+        mbar_arrive_expect_tx(&qdo_full[st], 2 * L::kTile + L::kCol);
+        for (int c = 0; c < L::kChunks; ++c) {
+          tma_load_3d(sQ + st * L::kTile + c * L::kChunk, &tm_q, &qdo_full[st], c * 64, h, t * kBlockM);
+          tma_load_3d(sDO + st * L::kTile + c * L::kChunk, &tm_do, &qdo_full[st], c * 64, h, t * kBlockM);
+        }
+        uint8_t* col = sCol + st * L::kCol;
+        const long long r0 = static_cast<long long>(t) * kBlockM;
+        const long long hr = static_cast<long long>(h) * p.rows_pad + r0;
+        bulk_load(col, p.row_lo + r0, kBlockM * 4, &qdo_full[st]);
+        bulk_load(col + kBlockM * 4, p.row_hi + r0, kBlockM * 4, &qdo_full[st]);
+        bulk_load(col + 2 * kBlockM * 4, p.lse2 + hr, kBlockM * 4, &qdo_full[st]);
+        bulk_load(col + 3 * kBlockM * 4, p.dvec + hr, kBlockM * 4, &qdo_full[st]);
+        issued = i + 1;
+      }
+      if (abort_flag) {
+        mbar_wait_drain(&kv_full, 0);
+        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) mbar_wait_drain(&qdo_full[i & 1], (i >> 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n_items > 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
+      constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, D, 0, 1);
+      uint32_t k_lo, k_hi, v_lo, v_hi, q_lo, q_hi, do_lo, do_hi, qmn_lo, qmn_hi, domn_lo, domn_hi;
+      umma_desc_words(smem_desc_sw128(smem_u32(sK), 16, 1024), k_lo, k_hi);
+      umma_desc_words(smem_desc_sw128(smem_u32(sV), 16, 1024), v_lo, v_hi);
+      umma_desc_words(smem_desc_sw128(smem_u32(sQ), 16, 1024), q_lo, q_hi);
+      umma_desc_words(smem_desc_sw128(smem_u32(sDO), 16, 1024), do_lo, do_hi);
+      umma_desc_words(smem_desc_sw128(smem_u32(sQ), L::kChunk, 1024), qmn_lo, qmn_hi);
+      umma_desc_words(smem_desc_sw128(smem_u32(sDO), L::kChunk, 1024), domn_lo, domn_hi);
+      bool ok = mbar_wait(&kv_full, 0, &abort_flag);
+      for (int i = 0; ok && i < n_items; ++i) {
+        const int st = i & 1;
+        const uint32_t so = (st * L::kTile) >> 4;
+        if (!mbar_wait(&qdo_full[st], (i >> 1) & 1, &abort_flag)) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
+          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+          umma_ss_w(tmem, k_lo + off, k_hi, q_lo + so + off, q_hi, kIdS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
+          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+          umma_ss_w(tmem + 128, v_lo + off, v_hi, do_lo + so + off, do_hi, kIdS, kk > 0);
+        }
+        umma_commit(&sdp_full);
+        if (!mbar_wait(&pds_full, i & 1, &abort_flag)) break;
+        tc_fence_after_sync();
+        const uint32_t acc0 = (i > 0) ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < kBlockM / 16; ++kk) {  // dV += P^T dO
+          umma_ts_w(tmem + 256, tmem + kk * 8, domn_lo + so + ((kk * 16 * 128) >> 4), domn_hi, kIdO,
+                    kk > 0 ? 1u : acc0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kBlockM / 16; ++kk) {  // dK += dS^T Q
+          umma_ts_w(tmem + 256 + D, tmem + 128 + kk * 8, qmn_lo + so + ((kk * 16 * 128) >> 4), qmn_hi, kIdO,
+                    kk > 0 ? 1u : acc0);
+        }
+        umma_commit(&qdo_empty[st]);
+      }
+      umma_commit(&kv_final);
+      umma_commit(&drain);
+      mbar_wait_drain(&drain, 0);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int key = K0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
+    const uint32_t t_v = tmem + lane_off + 256, t_k = tmem + lane_off + 256 + D;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int i = 0; i < n_items; ++i) {
+      const int st = i & 1;
+      // the column data arrived with Q/dO through the TMA barrier
+      if (!warp_wait(&qdo_full[st], (i >> 1) & 1, &abort_flag)) { ok = false; break; }
+      if (!warp_wait(&sdp_full, i & 1, &abort_flag)) { ok = false; break; }
+      tc_fence_after_sync();
+      const int* c_lo = reinterpret_cast<const int*>(sCol + st * L::kCol);
+      const int* c_hi = c_lo + kBlockM;
+      const float* c_l2 = reinterpret_cast<const float*>(c_lo + 2 * kBlockM);
+      const float* c_d = c_l2 + kBlockM;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(t_s + 32 * c4, sv);
+        tmem_ld32(t_dp + 32 * c4, dp);
+        tmem_ld_wait(sv);
+        tmem_ld_wait(dp);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const int col = 32 * c4 + 4 * q4;
+          const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
+          const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
+          const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
+          const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
+          const int los[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
+          const int his[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+          const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
+          const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], dsv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float e = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
+            pv[u] = (key >= los[u] && key <= his[u]) ? e : 0.f;
+            dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
+          }
+          pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
+          pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
+          pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+          pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+        }
+        tmem_st16(t_s + 16 * c4, pp);
+        tmem_st16(t_dp + 16 * c4, pd);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pds_full);
+    }
+    if (ok && n_items > 0) ok = warp_wait(&kv_final, 0, &abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after_sync();
+    if (ok && n_items > 0) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rv[32], rk[32];
+        tmem_ld32(t_v + 32 * c, rv);
+        tmem_ld32(t_k + 32 * c, rk);
+        tmem_ld_wait(rv);
+        tmem_ld_wait(rk);
+        if (key < p.T) {
+          float4* dv4 = reinterpret_cast<float4*>(p.dv + (static_cast<long long>(key) * p.Hkv + g) * D + 32 * c);
+          float4* dk4 = reinterpret_cast<float4*>(p.dk + (static_cast<long long>(key) * p.Hkv + g) * D + 32 * c);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            dv4[q] = make_float4(__uint_as_float(rv[4 * q]), __uint_as_float(rv[4 * q + 1]),
+                                 __uint_as_float(rv[4 * q + 2]), __uint_as_float(rv[4 * q + 3]));
+            dk4[q] = make_float4(__uint_as_float(rk[4 * q]) * p.scale, __uint_as_float(rk[4 * q + 1]) * p.scale,
+                                 __uint_as_float(rk[4 * q + 2]) * p.scale, __uint_as_float(rk[4 * q + 3]) * p.scale);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (abort_flag && threadIdx.x == 0) record_error(p.err, CPTHD_ERR_TIMEOUT, blockIdx.x);
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+static size_t bwd_workspace_bytes(long long ntiles, int Hq) {
+  const long long rows_pad = ntiles * kBlockM;
+  return attn_workspace_bytes(ntiles, kBlockM) + 2 * align256(sizeof(float) * rows_pad * Hq);
+}
+
+template <int D>
+static int launch_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                      const float* lse, long long t_local, long long T, int Hq, int Hkv, float scale,
+                      const AttnWorkspace& ws, float* lse2, float* dvec, long long ntiles, float* dq, float* dk,
+                      float* dv, int32_t* err, cudaStream_t s) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (enc == nullptr) return CPTHD_ERR_CUDA;
+  CUtensorMap mq, mdo, mk, mv;
+  if (!make_rows_heads_map(enc, &mq, q, t_local, Hq, D) || !make_rows_heads_map(enc, &mdo, dout, t_local, Hq, D) ||
+      !make_rows_heads_map(enc, &mk, k, T, Hkv, D) || !make_rows_heads_map(enc, &mv, v, T, Hkv, D))
+    return CPTHD_ERR_UNSUPPORTED;
+  const int rows_pad = static_cast<int>(ntiles * kBlockM);
+  const long long warps = static_cast<long long>(rows_pad) * Hq;
+  attn_bwd_pre_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, t_local, Hq, rows_pad,
+      lse2, dvec);
+  BwdParams p;
+  p.row_lo = ws.row_lo;
+  p.row_hi = ws.row_hi;
+  p.tile_info = ws.group_info;
+  p.intervals = ws.intervals;
+  p.lse2 = lse2;
+  p.dvec = dvec;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.t_local = t_local;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.ntiles = static_cast<int>(ntiles);
+  p.rows_pad = rows_pad;
+  p.max_blocks = static_cast<int>((T + kBlockN - 1) / kBlockN + kBlockM);
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = err;
+  const int smem_dq = BwdSmem<D>::launch(BwdSmem<D>::kDqBytes);
+  const int smem_kv = BwdSmem<D>::launch(BwdSmem<D>::kDkvBytes);
+  CPTHD_TRY_CUDA(cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_dq));
+  CPTHD_TRY_CUDA(cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv));
+  attn_bwd_dq_kernel<D><<<static_cast<unsigned>(ntiles * Hq), kBwdThreads, smem_dq, s>>>(mq, mdo, mk, mv, p);
+  const long long kts = (T + kBlockN - 1) / kBlockN;
+  attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(kts * Hkv), kBwdThreads, smem_kv, s>>>(mq, mdo, mk, mv, p);
+  CPTHD_TRY_CUDA(cudaGetLastError());
+  return CPTHD_OK;
+}
+
+}  // namespace cpthd
+
+extern "C" int thd_causal_attn_bwd_workspace_size(int64_t t_local, int Hq, int Hkv, int d, size_t* bytes_host) {
+  if (bytes_host == nullptr || t_local < 0 || Hq < 1 || Hkv < 1) return CPTHD_ERR_INVALID_ARG;
+  (void)Hkv;
+  (void)d;
+  const long long ntiles = (t_local + cpthd::kBlockM - 1) / cpthd::kBlockM;
+  *bytes_host = cpthd::bwd_workspace_bytes(ntiles, Hq);
+  return CPTHD_OK;
+}
+
+extern "C" int thd_causal_attn_bwd(const int32_t* q_slice_idx_dev, int64_t t_local, const void* q_dev,
+                                   const void* k_dev, const void* v_dev, const void* out_dev, const void* dout_dev,
+                                   const float* lse_dev, int64_t T, const int32_t* cu_seqlens_dev,
+                                   const int32_t* cu_seqlens_padded_dev, int num_docs, int Hq, int Hkv, int d,
+                                   float softmax_scale, float* dq_dev, float* dk_dev, float* dv_dev,
+                                   void* workspace_dev, size_t workspace_bytes, int32_t* err_dev,
+                                   cpthd_stream_t stream) {
+  using namespace cpthd;
+  if (t_local < 0 || T < 0 || T > INT32_MAX || t_local > INT32_MAX || num_docs < 0 || Hq < 1 || Hkv < 1)
+    return CPTHD_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return CPTHD_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0 || Hq > 65535) return CPTHD_ERR_UNSUPPORTED;
+  const long long ntiles = (t_local + kBlockM - 1) / kBlockM;
+  if (ntiles > kBwdMaxTiles) return CPTHD_ERR_UNSUPPORTED;
+  if (dk_dev == nullptr || dv_dev == nullptr || (T > 0 && k_dev == nullptr)) return CPTHD_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // this rank's dK/dV contribution: keys its queries do not reach stay zero
+  CPTHD_TRY_CUDA(cudaMemsetAsync(dk_dev, 0, sizeof(float) * static_cast<size_t>(T) * Hkv * d, s));
+  CPTHD_TRY_CUDA(cudaMemsetAsync(dv_dev, 0, sizeof(float) * static_cast<size_t>(T) * Hkv * d, s));
+  if (t_local == 0) return CPTHD_OK;
+  if (q_slice_idx_dev == nullptr || q_dev == nullptr || v_dev == nullptr || out_dev == nullptr ||
+      dout_dev == nullptr || lse_dev == nullptr || cu_seqlens_dev == nullptr || dq_dev == nullptr || num_docs < 1 ||
+      T < 1)
+    return CPTHD_ERR_INVALID_ARG;
+  const uintptr_t align = reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(k_dev) |
+                          reinterpret_cast<uintptr_t>(v_dev) | reinterpret_cast<uintptr_t>(dout_dev) |
+                          reinterpret_cast<uintptr_t>(dq_dev) | reinterpret_cast<uintptr_t>(dk_dev) |
+                          reinterpret_cast<uintptr_t>(dv_dev);
+  if (align & 15) return CPTHD_ERR_UNSUPPORTED;
+  if (workspace_dev == nullptr || workspace_bytes < bwd_workspace_bytes(ntiles, Hq) ||
+      (reinterpret_cast<uintptr_t>(workspace_dev) & 255))
+    return CPTHD_ERR_WORKSPACE;
+  const int32_t* cup = cu_seqlens_padded_dev ? cu_seqlens_padded_dev : cu_seqlens_dev;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
+  AttnWorkspace ws = carve_workspace(workspace_dev, ntiles, kBlockM);
+  char* extra = static_cast<char*>(workspace_dev) + attn_workspace_bytes(ntiles, kBlockM);
+  float* lse2 = reinterpret_cast<float*>(extra);
+  float* dvec = reinterpret_cast<float*>(extra + align256(sizeof(float) * ntiles * kBlockM * Hq));
+  attn_group_meta_kernel<kBlockM><<<static_cast<unsigned>(ntiles), kBlockM, 0, s>>>(
+      q_slice_idx_dev, t_local, cu_seqlens_dev, cup, num_docs, T, ws, err_dev);
+  CPTHD_TRY_CUDA(cudaGetLastError());
+  if (d == 128)
+    return launch_bwd<128>(q_dev, k_dev, v_dev, out_dev, dout_dev, lse_dev, t_local, T, Hq, Hkv, scale, ws, lse2,
+                           dvec, ntiles, dq_dev, dk_dev, dv_dev, err_dev, s);
+  return launch_bwd<64>(q_dev, k_dev, v_dev, out_dev, dout_dev, lse_dev, t_local, T, Hq, Hkv, scale, ws, lse2, dvec,
+                        ntiles, dq_dev, dk_dev, dv_dev, err_dev, s);
+}

@@ -74,7 +74,7 @@ inline AttnWorkspace carve_workspace(void* base, long long ngroups, int group_ro
 // at 0 and never decrease, padded offsets end at T, L_j <= P_j) in a
 // grid-stride loop over documents.
 template <int ROWS>
-__global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
+static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
     const int32_t* __restrict__ idx, long long t_local, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ cup, int num_docs, long long T, AttnWorkspace ws, int32_t* err) {
   constexpr int kWarps = ROWS / 32;
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
 
 // One block of 1024 threads: order[] = groups by decreasing block count
 // (ties by group index). Larger group counts keep the natural order.
-__global__ void __launch_bounds__(1024) attn_group_order_kernel(int ngroups, AttnWorkspace ws) {
+static __global__ void __launch_bounds__(1024) attn_group_order_kernel(int ngroups, AttnWorkspace ws) {
   __shared__ unsigned keys[kMaxSortGroups];
   const int t = threadIdx.x;
   if (ngroups > kMaxSortGroups) {

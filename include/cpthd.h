@@ -175,6 +175,34 @@ CPTHD_API int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loca
                         float* lse_dev, void* workspace_dev, size_t workspace_bytes,
                         int32_t* err_dev, cpthd_stream_t stream);
 
+/* Device workspace thd_causal_attn_bwd needs (per-row key bounds, per-tile key
+ * intervals, lse * log2(e) and rowsum(dO * O) per row and query head). Host only. */
+CPTHD_API int thd_causal_attn_bwd_workspace_size(int64_t t_local, int Hq, int Hkv, int d, size_t* bytes_host);
+
+/* Causal packed-THD attention backward for one rank's query slice: the
+ * gradients of sum(dout * out) for the forward above, with the same slice
+ * layout (TE PR: the strategy is captured for backward, so forward and
+ * backward use the same token layout) and the forward's LSE.
+ *   q_slice_idx_dev, q_dev, k_dev, v_dev, cu_seqlens*, num_docs, Hq, Hkv, d,
+ *     softmax_scale: exactly as passed to thd_causal_attn_fwd.
+ *   out_dev: bf16 [t_local, Hq, d], lse_dev: fp32 [Hq, t_local] -- the
+ *     forward's outputs; dout_dev: bf16 [t_local, Hq, d].
+ *   dq_dev: fp32 [t_local, Hq, d].
+ *   dk_dev, dv_dev: fp32 [T, Hkv, d] for the whole K/V buffer, holding this
+ *     rank's contribution (the part a reduce-scatter over CP ranks would sum);
+ *     the call zeroes them first, so keys no query of the slice reaches get 0.
+ *   workspace_dev: thd_causal_attn_bwd_workspace_size() bytes, 256-byte aligned.
+ * Supported: d in {64, 128}; Hq % Hkv == 0; t_local <= 262,144 (2048 query
+ * tiles). Host errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. Device
+ * checks (err_dev): BAD_OFFSETS, PAD_LENGTH, INDEX_RANGE, TIMEOUT. */
+CPTHD_API int thd_causal_attn_bwd(const int32_t* q_slice_idx_dev, int64_t t_local, const void* q_dev,
+                                  const void* k_dev, const void* v_dev, const void* out_dev, const void* dout_dev,
+                                  const float* lse_dev, int64_t T, const int32_t* cu_seqlens_dev,
+                                  const int32_t* cu_seqlens_padded_dev, int num_docs, int Hq, int Hkv, int d,
+                                  float softmax_scale, float* dq_dev, float* dk_dev, float* dv_dev,
+                                  void* workspace_dev, size_t workspace_bytes, int32_t* err_dev,
+                                  cpthd_stream_t stream);
+
 /* Same computation as thd_causal_attn_fwd for callers that cannot allocate
  * device memory (a host framework that owns all allocations, a plugin that
  * must not call cudaMalloc mid-step, a path that may never enter an
