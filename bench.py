@@ -308,6 +308,41 @@ def dcs_two_launch(cp, cfg, st, ranks, flush):
             "two_over_one": round(sum(split) / sum(fused), 3), "ranks": len(ranks)}
 
 
+def backward(cp, cfg, strategies, ranks, flush, peak):
+    """The attention backward of every (strategy, rank) slice of the step,
+    timed alone (graph replays, L2 flushed before each). Algorithmic work is
+    the usual 2.5x the forward: 10 * d * pairs * Hq (the S recompute, dP, dS V,
+    dQ, dK, dV products counted once)."""
+    res = {}
+    tot_f, tot_ms = 0.0, 0.0
+    for st in strategies:
+        d = st.dev
+        dev = d["q"].device
+        tl = st.t_local
+        dout = W.randn_bf16(cfg.seed, 6, (tl, cfg.hq, cfg.d)).to(dev)
+        dq = torch.empty((tl, cfg.hq, cfg.d), dtype=torch.float32, device=dev)
+        dk = torch.empty((st.T, cfg.hkv, cfg.d), dtype=torch.float32, device=dev)
+        dv = torch.empty_like(dk)
+        ws = torch.empty(cp.thd_causal_attn_bwd_workspace_size(tl, cfg.hq, cfg.hkv, cfg.d), dtype=torch.uint8,
+                         device=dev)
+        ms, fl = [], []
+        for r in ranks:
+            st.run_rank(cp, r)
+            ms.append(_graph_ms(lambda: cp.thd_causal_attn_bwd(
+                st.idx[r], st.q_loc[r], d["k"], d["v"], st.out[r], dout, st.lse[r], d["cu"], d["cup"], dq=dq, dk=dk,
+                dv=dv, workspace=ws, err=st.err), flush, reps=3))
+            fl.append(2.5 * st.flops[r])
+        res[st.name] = {"ms_per_rank_max": round(max(ms), 5), "ms_per_rank_min": round(min(ms), 5),
+                        "tflops": round(sum(fl) / (sum(ms) * 1e-3) / 1e12, 3)}
+        tot_f += sum(fl)
+        tot_ms += sum(ms)
+        del dq, dk, dv, ws
+    tf = tot_f / (tot_ms * 1e-3) / 1e12
+    res["all"] = {"tflops": round(tf, 3), "frac_of_peak": round(tf / peak, 4),
+                  "flops": "10 * d * unmasked pairs * Hq per slice"}
+    return res
+
+
 def activation_reorder(cp, cfg, st, ranks, flush, dev, hbm_peak):
     """Reorder of the workload's [T, width] bf16 activations into every rank's
     token order (graph replays, L2 flushed before each)."""
@@ -464,6 +499,7 @@ def run_cuda(args):
     dcs_st = [st for st in strategies if st.name == W.DUAL_CHUNK_SWAP]
     restore = kv_restore(cp, cfg, dcs_st[0], flush, dev, hbm_peak) if dcs_st and not args.no_extras else None
     two = dcs_two_launch(cp, cfg, dcs_st[0], ranks, flush) if dcs_st and not args.no_extras else None
+    bwd = backward(cp, cfg, strategies, ranks, flush, peak) if not args.no_extras else None
 
     # ---- end to end: pinned host inputs -> step -> host results --------------
     e2e_steps = max(1, min(args.steps, 10))
@@ -515,6 +551,7 @@ def run_cuda(args):
             "reorder_activations": act,
             "kv_restore": restore,
             "dcs_one_vs_two_launches": two,
+            "backward": bwd,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4),
                          "traffic": measured_traffic(cfg.name, args.strategy is not None or args.rank is not None),
@@ -609,7 +646,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.CONFIG_BY_NAME))
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extras", action="store_true", help="skip the K/V restore and one-vs-two-launch measurements")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the K/V restore, one-vs-two-launch and backward measurements")
     ap.add_argument("--strategy", choices=list(W.ALL_STRATEGIES), default=None,
                     help="time one strategy only (profiling); the headline runs every strategy")
     ap.add_argument("--rank", type=int, default=None,
