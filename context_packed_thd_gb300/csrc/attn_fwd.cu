@@ -10,27 +10,30 @@
 // same K/V blocks: one row tile under two query heads that share a KV head
 // (GQA group sizes divisible by 2), or two consecutive row tiles under one
 // head. Twelve warps in three warpgroups; warpgroup 0 gives registers to the
-// softmax warpgroups (setmaxnreg: 56 vs 224 per thread; 56*128 + 224*256 equals
-// the 168 * 384 the launch allocates):
+// softmax warpgroups (setmaxnreg: 96 vs 192 per thread; 96*128 + 192*256 stays
+// within the 168 * 384 the launch allocates):
 //  * warp 0      TMA producer: both Q tiles once, then K and V 128-key blocks
 //                into a two-stage shared-memory ring (128-byte swizzle, the
-//                layout the UMMA shared-memory descriptors read). Both MMA
-//                issuers release a stage through commits (K after S, V after
+//                layout the UMMA shared-memory descriptors read). The MMA
+//                issuer releases a stage through commits (K after S, V after
 //                PV).
-//  * warps 1, 2  one lane each issues the tcgen05 MMAs of one tile x:
-//                S_x(0), then per block j: O_x += P_x(j) V_j, S_x(j+1). Two
-//                issuing threads are needed: one thread issuing 128x128x16
-//                MMAs back to back reaches about 85% of the tensor rate on
-//                GB300, two reach all of it. The issue is fully unrolled
-//                with descriptors precomputed; an issue loop with address
-//                arithmetic per MMA halves the rate. Warp 1 also owns the
-//                512-column TMEM allocation (S_A, S_B, O_A, O_B). P_x(j) is
-//                written by the softmax into the first 64 columns of S_x
-//                (bf16 pairs) and is read from TMEM by the MMA. Because one
-//                thread's MMAs complete in issue order, the commit that
-//                reports S_x(j+1) also reports that O_x += P_x(j) V_j is
-//                done, so the softmax may then rescale O_x and overwrite P_x
-//                without further waits.
+//  * warp 1      one lane issues all tcgen05 MMAs: S_A(0), S_B(0), then per
+//                block j and tile x = A, B: O_x += P_x(j) V_j, S_x(j+1).
+//                Issuing tile A's batch before tile B's from one thread keeps
+//                the two tiles half a period apart, so that each tile's
+//                softmax runs while the tensor pipe works on the other tile.
+//                The issue is fully unrolled with descriptors precomputed
+//                (an issue loop with address arithmetic per MMA halves the
+//                rate). Warp 1 also owns the 512-column TMEM allocation (S_A,
+//                S_B, O_A, O_B). P_x(j) is written by the softmax into the
+//                first 64 columns of S_x (bf16 pairs) and is read from TMEM
+//                by the MMA. Because one thread's MMAs complete in issue
+//                order, the commit that reports S_x(j+1) also reports that
+//                O_x += P_x(j) V_j is done, so the softmax may then rescale
+//                O_x and overwrite P_x without further waits.
+//  * warp 2      data relay: per block j, waits until V_j and K_{j+1} have
+//                landed and arrives on both tiles' P-ready barriers, so that
+//                the issuer waits once per tile and block.
 //  * warp 3      idle.
 //  * warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: each thread
 //                owns one query row (its TMEM lane). It reads S with one
@@ -55,8 +58,8 @@ namespace cpthd {
 using namespace sm100;
 
 constexpr int kAttnThreads = 384;
-constexpr int kRegsControl = 56;   // warpgroup 0: producer, MMA issuer
-constexpr int kRegsSoftmax = 224;  // warpgroups 1 and 2
+constexpr int kRegsControl = 96;   // warpgroup 0: producer, MMA issuer, data relay
+constexpr int kRegsSoftmax = 192;  // warpgroups 1 and 2
 static_assert(kRegsControl * 128 + kRegsSoftmax * 256 <= 168 * kAttnThreads, "register split exceeds the launch");
 constexpr int kStages = 2;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 256x
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sV = smem + L::kVOff;
 
   __shared__ uint64_t q_full, k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
-  __shared__ uint64_t s_full[2], p_full[2], o_final[2], drain[2];
+  __shared__ uint64_t s_full[2], p_full[2], o_final[2], drain[1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -130,15 +133,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 2);  // released by both MMA issuers
-      mbar_init(&v_empty[s], 2);
+      mbar_init(&k_empty[s], 1);  // released by the MMA issuer's commits
+      mbar_init(&v_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 4);
+      mbar_init(&p_full[x], 5);  // four softmax warps and the data relay
       mbar_init(&o_final[x], 1);
-      mbar_init(&drain[x], 1);
     }
+    mbar_init(&drain[0], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -193,11 +196,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
     }
-   } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ MMA issuers
-    // One thread per tile (warp 1: tile A, warp 2: tile B); two issuing
-    // threads keep the tensor core busy with 128-wide MMAs where one cannot.
-    const int x = warp - 1;
+   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // One thread issues both tiles' MMAs, tile A's batch before tile B's.
+    // Issued from one thread they run in that order, so tile B's scores
+    // arrive a batch after tile A's and the two tiles settle into a
+    // staggered schedule: one tile's softmax runs under the other tile's
+    // MMAs. (Two issuing threads started together interleave their MMAs on
+    // the tensor pipe, both tiles finish together, and their softmaxes then
+    // leave the tensor pipe idle: a lockstep that a single issuer avoids.)
     if (lane == 0 && n_blocks > 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kBlockM, D, 0, 1);
@@ -205,23 +212,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // leading-byte offset; its high word (stride offset, version, swizzle)
       // is the same for every block of one operand. Addresses stay below
       // 256 KB, so adding an offset to the low word never carries.
-      const uint64_t dq = smem_desc_sw128(smem_u32(sQ + x * L::kQ), 16, 1024);
+      const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dk = smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dv = smem_desc_sw128(smem_u32(sV), L::kChunk, 1024);
       const uint32_t q_lo = static_cast<uint32_t>(dq), q_hi = static_cast<uint32_t>(dq >> 32);
       const uint32_t k_lo = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
       const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
-      const uint32_t t_s = tmem + x * kBlockN;
-      const uint32_t t_o = tmem + 256 + x * D;
-      auto issue_s = [&](int j) {  // S_x = Q_x K_j^T
+      auto issue_s = [&](int j, int x) {  // S_x = Q_x K_j^T
+        const uint32_t t_s = tmem + x * kBlockN;
+        const uint32_t qb = q_lo + ((x * L::kQ) >> 4);
         const uint32_t kb = k_lo + (((j & 1) * L::kKV) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
-          umma_ss_w(t_s, q_lo + off, q_hi, kb + off, k_hi, kIdescS, kk > 0);
+          umma_ss_w(t_s, qb + off, q_hi, kb + off, k_hi, kIdescS, kk > 0);
         }
       };
-      auto issue_pv = [&](int j) {  // O_x += P_x V_j, P_x read from TMEM
+      auto issue_pv = [&](int j, int x) {  // O_x += P_x V_j, P_x read from TMEM
+        const uint32_t t_s = tmem + x * kBlockN;
+        const uint32_t t_o = tmem + 256 + x * D;
         const uint32_t vb = v_lo + (((j & 1) * L::kKV) >> 4);
         const uint32_t acc0 = (j > 0) ? 1u : 0u;
 #pragma unroll
@@ -231,30 +240,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool ok = mbar_wait(&q_full, 0, &abort_flag) && mbar_wait(&k_full[0], 0, &abort_flag);
       if (ok) {
         tc_fence_after_sync();
-        issue_s(0);
-        umma_commit(&s_full[x]);
+        issue_s(0, 0);
+        umma_commit(&s_full[0]);
+        issue_s(0, 1);
+        umma_commit(&s_full[1]);
         umma_commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < n_blocks; ++j) {
         const int st = j & 1;
         const bool more = (j + 1 < n_blocks);
-        // V_j and K_{j+1} normally landed long ago: check them before the
-        // softmax's P, so that PV and the next S issue back to back
-        if (!mbar_wait(&v_full[st], (j >> 1) & 1, &abort_flag)) break;
-        if (more && !mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, &abort_flag)) break;
-        if (!mbar_wait(&p_full[x], j & 1, &abort_flag)) break;
-        tc_fence_after_sync();
-        issue_pv(j);
-        umma_commit(&v_empty[st]);
-        if (more) {
-          issue_s(j + 1);
-          umma_commit(&s_full[x]);  // also reports O_x += P_x(j) V_j done
-          umma_commit(&k_empty[(j + 1) & 1]);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          // P_x(j) is ready, and (through the relay's arrival) V_j and K_{j+1}
+          // have landed
+          if (!mbar_wait(&p_full[x], j & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after_sync();
+          issue_pv(j, x);
+          if (x == 1) umma_commit(&v_empty[st]);
+          if (more) {
+            issue_s(j + 1, x);
+            umma_commit(&s_full[x]);  // also reports O_x += P_x(j) V_j done
+          }
         }
+        if (ok && more) umma_commit(&k_empty[(j + 1) & 1]);
       }
-      umma_commit(&o_final[x]);
-      umma_commit(&drain[x]);
-      mbar_wait_drain(&drain[x], 0);
+      umma_commit(&o_final[0]);
+      umma_commit(&o_final[1]);
+      umma_commit(&drain[0]);
+      mbar_wait_drain(&drain[0], 0);
+    }
+   } else if (warp == 2) {
+    // ------------------------------------------------------------ data relay
+    // Waits, per block j, until V_j and K_{j+1} have landed and then arrives
+    // on both tiles' p_full, so that the MMA issuer (the busiest thread of
+    // the CTA) needs a single wait per tile and block. Before arriving for
+    // block j it waits for both p_full phases of block j - 1 to complete, so
+    // that an early arrival never counts toward the previous phase.
+    if (lane == 0) {
+      for (int j = 0; j < n_blocks; ++j) {
+        if (j > 0 && !(mbar_wait(&p_full[0], (j - 1) & 1, &abort_flag) &&
+                       mbar_wait(&p_full[1], (j - 1) & 1, &abort_flag)))
+          break;
+        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, &abort_flag)) break;
+        if (j + 1 < n_blocks && !mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, &abort_flag)) break;
+        mbar_arrive(&p_full[0]);
+        mbar_arrive(&p_full[1]);
+      }
     }
    }
   } else {
@@ -290,28 +321,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tmem_ld128(t_s, sr);
       tmem_ld_wait128(sr);
       const bool full = (kstart >= tmax_lo) && (kstart + kBlockN - 1 <= min(tmin_hi, kend));
+      // 16-column groups of this block that no row of the warp may use
+      uint32_t dead_groups = 0;
       if (!full) {
         // allowed columns of this row: [c_lo, c_hi] (empty when c_lo > c_hi)
         const int c_lo = min(max(lo - kstart, 0), kBlockN);
-        const int c_hi = max(min(min(hi, kend) - kstart, kBlockN - 1), -1);
-        const bool cut_lo = __any_sync(0xffffffffu, c_lo > 0);
-        const bool cut_hi = __any_sync(0xffffffffu, c_hi < kBlockN - 1);
-        // The mask runs on the FMA pipe: u = saturate(c - c_hi) is 1 exactly
-        // for columns past the row's last key (c is an integer), and
-        // s - u * 2^100 pushes them far below any real score; likewise for
-        // columns before its first key. A row left with no key in this block
-        // is caught after the max (below), so no two huge values are ever
-        // subtracted from each other.
-        const float f_hi = static_cast<float>(c_hi), f_lo = static_cast<float>(c_lo);
-        if (cut_hi) {
-#pragma unroll
-          for (int c = 0; c < kBlockN; ++c)
-            sr[c] = __float_as_uint(fmaf(__saturatef(static_cast<float>(c) - f_hi), -kMaskShift, __uint_as_float(sr[c])));
-        }
-        if (cut_lo) {
+        int c_hi = max(min(min(hi, kend) - kstart, kBlockN - 1), -1);
+        // Blocks start at document starts, so a row either starts at or
+        // before the block (c_lo = 0) or has no key in it (c_lo > c_hi). The
+        // low-side mask is kept for any other case so that no row can ever
+        // use a key before its own start.
+        if (__any_sync(0xffffffffu, c_lo > 0 && c_lo <= c_hi)) {
+          const float f_lo = static_cast<float>(c_lo);
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
             sr[c] = __float_as_uint(fmaf(__saturatef(f_lo - static_cast<float>(c)), -kMaskShift, __uint_as_float(sr[c])));
+        }
+        if (c_lo > c_hi) c_hi = -1;
+        const int w_min = __reduce_min_sync(0xffffffffu, c_hi);
+        const int w_max = __reduce_max_sync(0xffffffffu, c_hi);
+        // The mask runs on the FMA pipe: u = saturate(c - c_hi) is 1 exactly
+        // for columns past the row's last key (c is an integer), and
+        // s - u * 2^100 pushes them far below any real score. A row left
+        // with no key in this block is caught after the max (below), so no
+        // two huge values are ever subtracted from each other. Groups every
+        // row may use are left alone; groups no row may use become -inf and
+        // skip the exponentials.
+        const float f_hi = static_cast<float>(c_hi);
+#pragma unroll
+        for (int g = 0; g < kBlockN / 16; ++g) {
+          if (16 * g + 15 <= w_min) continue;
+          if (16 * g > w_max) {
+            dead_groups |= 1u << g;
+#pragma unroll
+            for (int c = 16 * g; c < 16 * g + 16; ++c) sr[c] = 0xff800000u;
+          } else {
+#pragma unroll
+            for (int c = 16 * g; c < 16 * g + 16; c += 2) {
+              float s0, s1;
+              fma2(s0, s1, __saturatef(static_cast<float>(c) - f_hi), __saturatef(static_cast<float>(c + 1) - f_hi),
+                   -kMaskShift, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+              sr[c] = __float_as_uint(s0);
+              sr[c + 1] = __float_as_uint(s1);
+            }
+          }
         }
       }
       // row max of the raw scores: four chains of three-input max
@@ -336,21 +389,48 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       const float mref = (m == -INFINITY) ? 0.f : m;
       // p = 2^(scale*log2(e)*s - m): one packed FMA per pair, ex2 per element,
-      // row sum in two packed accumulators
+      // row sum in two packed accumulators; groups no row may use give p = 0
       float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      if (dead_groups == 0) {
+        // straight-line form, so that the exponentials of a half overlap
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t pk[32];
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float a0, a1;
-          fma2(a0, a1, __uint_as_float(sr[64 * h2 + 2 * c]), __uint_as_float(sr[64 * h2 + 2 * c + 1]), sl2, -mref);
-          const float e0 = ex2(a0);
-          const float e1 = ex2(a1);
-          add2(rs[2 * (c & 1)], rs[2 * (c & 1) + 1], e0, e1);
-          pk[c] = pack_bf16x2(e0, e1);
+          for (int c = 0; c < 32; ++c) {
+            float a0, a1;
+            fma2(a0, a1, __uint_as_float(sr[64 * h2 + 2 * c]), __uint_as_float(sr[64 * h2 + 2 * c + 1]), sl2, -mref);
+            const float e0 = ex2(a0);
+            const float e1 = ex2(a1);
+            add2(rs[2 * (c & 1)], rs[2 * (c & 1) + 1], e0, e1);
+            pk[c] = pack_bf16x2(e0, e1);
+          }
+          tmem_st32(t_s + 32 * h2, pk);
         }
-        tmem_st32(t_s + 32 * h2, pk);
+      } else {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            if ((dead_groups >> (4 * h2 + gg)) & 1u) {
+#pragma unroll
+              for (int c = 8 * gg; c < 8 * gg + 8; ++c) pk[c] = 0u;
+            } else {
+#pragma unroll
+              for (int c = 8 * gg; c < 8 * gg + 8; ++c) {
+                float a0, a1;
+                fma2(a0, a1, __uint_as_float(sr[64 * h2 + 2 * c]), __uint_as_float(sr[64 * h2 + 2 * c + 1]), sl2,
+                     -mref);
+                const float e0 = ex2(a0);
+                const float e1 = ex2(a1);
+                add2(rs[2 * (c & 1)], rs[2 * (c & 1) + 1], e0, e1);
+                pk[c] = pack_bf16x2(e0, e1);
+              }
+            }
+          }
+          tmem_st32(t_s + 32 * h2, pk);
+        }
       }
       l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       if (__any_sync(0xffffffffu, grow_o)) {
