@@ -217,10 +217,14 @@ class Strategy:
         # reorder bytes per rank: read + write of every gathered row, plus the index list
         rb = hq * d * 2 + 3 * 8
         self.reorder_bytes = tl * (2 * rb + 4)
-
-    # launches per rank: partition index 1, one reorder of Q and the three id
-    # tensors 1, attention (row-group metadata, group order, attention) 3
-    LAUNCHES_PER_RANK = 5
+        # launches per rank: partition index 1, one reorder of Q and the three
+        # id tensors 1, attention: row-group metadata 1, group order 1 (only
+        # when the attention grid needs more than one wave of CTAs, one per
+        # SM), attention 1
+        rows = 128 if (hq // cfg.hkv) % 2 == 0 else 256
+        items = -(-tl // rows) * (hq // 2 if rows == 128 else hq)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.launches_per_rank = 4 + (1 if items > sms else 0)
 
     def run_prep(self, cp, r):
         d = self.dev
@@ -255,6 +259,38 @@ def _graph_ms(fn, flush, reps=5):
         torch.cuda.synchronize()
         ms.append(ev0.elapsed_time(ev1))
     return statistics.median(ms)
+
+
+def other_workloads(cp, current, dev, flush, peak):
+    """Attention throughput of every other multi-rank workload: all ranks of
+    all its strategies in one CUDA graph (L2 flushed before each replay), so
+    that the line also carries the long-context and many-document figures."""
+    out = {}
+    for cfg in W.CONFIGS[1:]:
+        if cfg.name == current:
+            continue
+        sts = [Strategy(cp, cfg, s, dev) for s in cfg.strategies]
+        for st in sts:
+            for r in range(cfg.cp):
+                st.run_prep(cp, r)
+
+        def attn_all():
+            for st in sts:
+                for r in range(cfg.cp):
+                    st.run_attn(cp, r)
+
+        ms = _graph_ms(attn_all, flush, reps=3)
+        for st in sts:
+            e = st.err.cpu().tolist()
+            if e[0] != 0:
+                raise RuntimeError(f"device check failed on {cfg.name}: {cp.cpthd_status_string(e[0])} ({e})")
+        flops = sum(sum(st.flops) for st in sts)
+        tf = flops / (ms * 1e-3) / 1e12
+        out[cfg.name] = {"attn_tflops": round(tf, 3), "frac_of_peak": round(tf / peak, 4), "ms": round(ms, 4),
+                         "rank_slices": cfg.cp * len(sts), "strategies": list(cfg.strategies)}
+        del sts
+        torch.cuda.empty_cache()
+    return out
 
 
 def kv_restore(cp, cfg, st, flush, dev, hbm_peak):
@@ -500,6 +536,7 @@ def run_cuda(args):
     restore = kv_restore(cp, cfg, dcs_st[0], flush, dev, hbm_peak) if dcs_st and not args.no_extras else None
     two = dcs_two_launch(cp, cfg, dcs_st[0], ranks, flush) if dcs_st and not args.no_extras else None
     bwd = backward(cp, cfg, strategies, ranks, flush, peak) if not args.no_extras else None
+    others = other_workloads(cp, cfg.name, dev, flush, peak) if not args.no_extras else None
 
     # ---- end to end: pinned host inputs -> step -> host results --------------
     e2e_steps = max(1, min(args.steps, 10))
@@ -552,6 +589,7 @@ def run_cuda(args):
             "kv_restore": restore,
             "dcs_one_vs_two_launches": two,
             "backward": bwd,
+            "attention_other_workloads": others,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4),
                          "traffic": measured_traffic(cfg.name, args.strategy is not None or args.rank is not None),
@@ -559,7 +597,7 @@ def run_cuda(args):
                          "peak_source": f"{peak_src} bf16_tflops (burst)"},
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": Strategy.LAUNCHES_PER_RANK * n_ranks * args.steps,
+            "gpu_launches": sum(st.launches_per_rank for st in strategies) * len(ranks) * args.steps,
             "gpu_launches_note": "library kernels inside the timed step replays; the L2 flush between steps is a torch fill",
             "clocks": clocks,
             "cpu_baseline": cpu,

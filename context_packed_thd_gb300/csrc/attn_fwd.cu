@@ -113,11 +113,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int units = p.head_pairs ? (p.Hq >> 1) : p.Hq;
   const int item = blockIdx.x;
-  const int group = __ldg(p.order + item / units);
+  // without an order (a grid of one wave) the groups run in index order
+  const int group = p.order ? __ldg(p.order + item / units) : item / units;
   const int unit = item % units;
   const int head0 = p.head_pairs ? 2 * unit : unit;
   const int kvh = head0 / (p.Hq / p.Hkv);
@@ -493,7 +496,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 template <int D>
 static int launch_attn(const void* q, const void* k, const void* v, long long t_local, long long T, int Hq, int Hkv,
-                       float scale_log2, const AttnWorkspace& ws, long long ngroups, int group_rows, void* out,
+                       float scale_log2, const AttnWorkspace& ws, long long ngroups, int group_rows, bool ordered,
+                       void* out,
                        float* lse, int32_t* err, cudaStream_t s) {
   EncodeTiledFn enc = get_encode_tiled();
   if (enc == nullptr) return CPTHD_ERR_CUDA;
@@ -506,7 +510,7 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
   p.row_hi = ws.row_hi;
   p.group_info = ws.group_info;
   p.intervals = ws.intervals;
-  p.order = ws.order;
+  p.order = ordered ? ws.order : nullptr;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.t_local = t_local;
@@ -521,8 +525,8 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
   CPTHD_TRY_CUDA(cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   const long long items = ngroups * (p.head_pairs ? Hq / 2 : Hq);
   if (items > INT32_MAX) return CPTHD_ERR_UNSUPPORTED;
-  attn_fwd_tc_kernel<D><<<static_cast<unsigned>(items), kAttnThreads, smem, s>>>(mq, mk, mv, p);
-  CPTHD_TRY_CUDA(cudaGetLastError());
+  CPTHD_TRY_CUDA(launch_pdl(attn_fwd_tc_kernel<D>, dim3(static_cast<unsigned>(items)), dim3(kAttnThreads), smem, s,
+                            mq, mk, mv, p));
   return CPTHD_OK;
 }
 
@@ -568,17 +572,25 @@ extern "C" int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loc
 
   AttnWorkspace ws = carve_workspace(workspace_dev, ngroups, rows);
   if (rows == kBlockM) {
-    attn_group_meta_kernel<kBlockM><<<static_cast<unsigned>(ngroups), kBlockM, 0, s>>>(
-        q_slice_idx_dev, t_local, cu_seqlens_dev, cup, num_docs, T, ws, err_dev);
+    CPTHD_TRY_CUDA(launch_pdl(attn_group_meta_kernel<kBlockM>, dim3(static_cast<unsigned>(ngroups)), dim3(kBlockM), 0,
+                              s, q_slice_idx_dev, static_cast<long long>(t_local), cu_seqlens_dev, cup, num_docs,
+                              static_cast<long long>(T), ws, err_dev));
   } else {
-    attn_group_meta_kernel<2 * kBlockM><<<static_cast<unsigned>(ngroups), 2 * kBlockM, 0, s>>>(
-        q_slice_idx_dev, t_local, cu_seqlens_dev, cup, num_docs, T, ws, err_dev);
+    CPTHD_TRY_CUDA(launch_pdl(attn_group_meta_kernel<2 * kBlockM>, dim3(static_cast<unsigned>(ngroups)),
+                              dim3(2 * kBlockM), 0, s, q_slice_idx_dev, static_cast<long long>(t_local),
+                              cu_seqlens_dev, cup, num_docs, static_cast<long long>(T), ws, err_dev));
   }
-  attn_group_order_kernel<<<1, 1024, 0, s>>>(static_cast<int>(ngroups), ws);
-  CPTHD_TRY_CUDA(cudaGetLastError());
+  // The longest groups go first when the grid needs more than one wave (one
+  // CTA per SM); within a single wave the order makes no difference and the
+  // ordering launch is skipped.
+  const long long items = ngroups * ((rows == kBlockM) ? Hq / 2 : Hq);
+  const bool ordered = items > sm_count();
+  if (ordered)
+    CPTHD_TRY_CUDA(launch_pdl(attn_group_order_kernel, dim3(1), dim3(1024), 0, s, static_cast<int>(ngroups), ws));
   if (d == 128)
-    return launch_attn<128>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ngroups, rows, out_dev,
+    return launch_attn<128>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ngroups, rows, ordered, out_dev,
                             lse_dev, err_dev, s);
-  return launch_attn<64>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ngroups, rows, out_dev, lse_dev,
+  return launch_attn<64>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ngroups, rows, ordered, out_dev,
+                         lse_dev,
                          err_dev, s);
 }

@@ -83,6 +83,8 @@ static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
   __shared__ int red_blocks[kWarps];
   __shared__ int red_lo[kWarps];
   __shared__ int red_hi[kWarps];
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int t = threadIdx.x;
   const int lane = t & 31, wid = t >> 5;
   const long long group = blockIdx.x;
@@ -182,6 +184,8 @@ static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
 // (ties by group index). Larger group counts keep the natural order.
 static __global__ void __launch_bounds__(1024) attn_group_order_kernel(int ngroups, AttnWorkspace ws) {
   __shared__ unsigned keys[kMaxSortGroups];
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int t = threadIdx.x;
   if (ngroups > kMaxSortGroups) {
     for (int i = t; i < ngroups; i += blockDim.x) ws.order[i] = i;

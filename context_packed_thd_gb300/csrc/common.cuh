@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <utility>
+
 #include "cpthd.h"
 
 #define CPTHD_TRY_CUDA(expr)                      \
@@ -34,6 +37,47 @@ __device__ __forceinline__ int upper_bound_doc(const int32_t* __restrict__ a, in
     if (static_cast<long long>(__ldg(a + mid)) <= x) lo = mid; else hi = mid;
   }
   return lo;
+}
+
+// Programmatic dependent launch. The forward path's kernels are launched
+// with programmatic stream serialization, so that a kernel's launch and
+// first instructions overlap the tail of the kernel before it on the
+// stream. Every such kernel calls grid_dependency_wait() first, before it
+// reads or writes global memory: it returns once the preceding kernel has
+// completed and its writes are visible (immediately when the launch had no
+// programmatic dependency), so ordering on the stream is as strict as with
+// a plain launch. grid_dependents_launch() then lets the next kernel start
+// launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KernelArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KernelArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Number of SMs of the current device (looked up once per device).
+inline int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
 }
 
 inline int grid_for(long long work, int per_block, int max_blocks) {

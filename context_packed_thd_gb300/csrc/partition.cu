@@ -38,6 +38,8 @@ __device__ __forceinline__ void check_offsets(const int32_t* __restrict__ cup, i
 __global__ void dual_chunk_swap_index_kernel(const int32_t* __restrict__ cup, int num_docs, long long T, int cp,
                                              int rank, long long t_local, long long total,
                                              int32_t* __restrict__ idx, int32_t* err) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   check_offsets(cup, num_docs, T, cp, 1, err);
   for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
        o += (long long)gridDim.x * blockDim.x) {
@@ -62,6 +64,8 @@ __global__ void dual_chunk_swap_index_kernel(const int32_t* __restrict__ cup, in
 __global__ void no_load_balance_index_kernel(const int32_t* __restrict__ cup, int num_docs, long long T, int cp,
                                              int rank, long long t_local, long long total,
                                              int32_t* __restrict__ idx, int32_t* err) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   check_offsets(cup, num_docs, T, cp, 0, err);
   for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
        o += (long long)gridDim.x * blockDim.x) {
@@ -73,6 +77,8 @@ __global__ void no_load_balance_index_kernel(const int32_t* __restrict__ cup, in
 __global__ void packed_mirrored_index_kernel(const int32_t* __restrict__ cup, int num_docs, long long T, int cp,
                                              int rank, long long t_local, long long total,
                                              int32_t* __restrict__ idx, int32_t* err) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   check_offsets(cup, num_docs, T, cp, 0, err);
   const long long chunk = T / (2LL * cp);
   for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
@@ -88,6 +94,8 @@ __global__ void packed_mirrored_index_kernel(const int32_t* __restrict__ cup, in
 // restore[p] = row of the rank-major gathered buffer holding physical slot p.
 __global__ void restore_index_kernel(int strategy, const int32_t* __restrict__ cup, int num_docs, long long T,
                                      int cp, int32_t* __restrict__ restore, int32_t* err) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   check_offsets(cup, num_docs, T, cp, strategy == CPTHD_DUAL_CHUNK_SWAP, err);
   const long long t_local = T / cp;
   for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < T;
@@ -143,17 +151,12 @@ extern "C" int cp_partition_index(int strategy, const int32_t* cu_seqlens_padded
   const bool dcs = (strategy == CPTHD_DUAL_CHUNK_SWAP);
   const long long work = total > num_docs + 1 ? total : num_docs + 1;
   const int grid = cpthd::grid_for(work, 256, 152 * 16);
-  if (dcs) {
-    cpthd::dual_chunk_swap_index_kernel<<<grid, 256, 0, s>>>(cu_seqlens_padded_dev, num_docs, T, cp_size, rank,
-                                                             t_local, total, idx_out_dev, err_dev);
-  } else if (strategy == CPTHD_NO_LOAD_BALANCE) {
-    cpthd::no_load_balance_index_kernel<<<grid, 256, 0, s>>>(cu_seqlens_padded_dev, num_docs, T, cp_size, rank,
-                                                             t_local, total, idx_out_dev, err_dev);
-  } else {
-    cpthd::packed_mirrored_index_kernel<<<grid, 256, 0, s>>>(cu_seqlens_padded_dev, num_docs, T, cp_size, rank,
-                                                             t_local, total, idx_out_dev, err_dev);
-  }
-  CPTHD_TRY_CUDA(cudaGetLastError());
+  auto kernel = dcs ? cpthd::dual_chunk_swap_index_kernel
+                    : (strategy == CPTHD_NO_LOAD_BALANCE ? cpthd::no_load_balance_index_kernel
+                                                         : cpthd::packed_mirrored_index_kernel);
+  CPTHD_TRY_CUDA(cpthd::launch_pdl(kernel, dim3(grid), dim3(256), 0, s, cu_seqlens_padded_dev, num_docs,
+                                   static_cast<long long>(T), cp_size, rank, static_cast<long long>(t_local), total,
+                                   idx_out_dev, err_dev));
   return CPTHD_OK;
 }
 
@@ -166,8 +169,8 @@ extern "C" int cp_restore_index(int strategy, const int32_t* cu_seqlens_padded_d
   if (T > 0 && (restore_idx_out_dev == nullptr || num_docs == 0)) return CPTHD_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const long long work = T > num_docs + 1 ? T : num_docs + 1;
-  cpthd::restore_index_kernel<<<cpthd::grid_for(work, 256, 152 * 16), 256, 0, s>>>(
-      strategy, cu_seqlens_padded_dev, num_docs, T, cp_size, restore_idx_out_dev, err_dev);
-  CPTHD_TRY_CUDA(cudaGetLastError());
+  CPTHD_TRY_CUDA(cpthd::launch_pdl(cpthd::restore_index_kernel, dim3(cpthd::grid_for(work, 256, 152 * 16)),
+                                   dim3(256), 0, s, strategy, cu_seqlens_padded_dev, num_docs,
+                                   static_cast<long long>(T), cp_size, restore_idx_out_dev, err_dev));
   return CPTHD_OK;
 }

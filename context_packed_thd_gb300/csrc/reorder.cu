@@ -102,6 +102,10 @@ __device__ __forceinline__ void gather_one(const ReorderTensor& t, long long src
 __global__ void __launch_bounds__(256) reorder_kernel(ReorderBatch batch, long long src_rows,
                                                       const int32_t* __restrict__ idx, long long n_rows,
                                                       int32_t* err) {
+  // every block waits, even one with nothing to copy, so that this grid never
+  // completes before the kernel it depends on
+  grid_dependency_wait();
+  grid_dependents_launch();
   const ReorderTensor& t = batch.t[blockIdx.y];
   if (t.row_bytes == 0) return;
   switch (t.vec) {
@@ -149,8 +153,8 @@ static int launch_reorder(int n, const void* const* src, void* const* dst, const
   }
   const int grid = grid_for(work, 256, 152 * 8);
   dim3 g(grid, n);
-  reorder_kernel<<<g, 256, 0, s>>>(b, src_rows, idx, n_rows, err);
-  CPTHD_TRY_CUDA(cudaGetLastError());
+  CPTHD_TRY_CUDA(launch_pdl(reorder_kernel, g, dim3(256), 0, s, b, static_cast<long long>(src_rows), idx,
+                            static_cast<long long>(n_rows), err));
   return CPTHD_OK;
 }
 
