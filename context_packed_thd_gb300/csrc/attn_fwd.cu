@@ -14,9 +14,10 @@
 // within the 168 * 384 the launch allocates):
 //  * warp 0      TMA producer: both Q tiles once, then K and V 128-key blocks
 //                into a two-stage shared-memory ring (128-byte swizzle, the
-//                layout the UMMA shared-memory descriptors read). The MMA
-//                issuer releases a stage through commits (K after S, V after
-//                PV).
+//                layout the UMMA shared-memory descriptors read). A stage is
+//                refilled once tile B's score barrier reports that the MMAs
+//                reading it are done, so the issuer commits only to the two
+//                score barriers inside its loop.
 //  * warp 1      one lane issues all tcgen05 MMAs: S_A(0), S_B(0), then per
 //                block j and tile x = A, B: O_x += P_x(j) V_j, S_x(j+1).
 //                Issuing tile A's batch before tile B's from one thread keeps
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sK = smem + L::kKOff;
   uint8_t* sV = smem + L::kVOff;
 
-  __shared__ uint64_t q_full, k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
+  __shared__ uint64_t q_full, k_full[kStages], v_full[kStages];
   __shared__ uint64_t s_full[2], p_full[2], o_final[2], drain[1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
@@ -136,8 +137,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);  // released by the MMA issuer's commits
-      mbar_init(&v_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
@@ -177,13 +176,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int issued = 0;
       for (int i = 0; i < n_blocks; ++i) {
         const int st = i & 1;
-        const uint32_t par = ((i >> 1) + 1) & 1;
-        if (i >= kStages && !mbar_wait(&k_empty[st], par, &abort_flag)) break;
+        // Stages are released through tile B's score barrier: its phase k
+        // completes when every MMA issued up to S_B(k) is done (one thread
+        // issues them all, tile B last), so phase i - 2 frees K_{i-2} and
+        // phase i - 1 frees V_{i-2}. Each phase is waited for once, in order
+        // (phase 0 before K_2, then phase i - 1 before V_i; K_i for i >= 3
+        // needs phase i - 2, already seen before V_{i-1}). A phase can only
+        // complete after loads this thread issues just before waiting for
+        // the phase ahead of it, so the barrier is never two phases ahead
+        // of a wait and the parity is unambiguous.
+        if (i == kStages && !mbar_wait(&s_full[1], 0, &abort_flag)) break;
         mbar_arrive_expect_tx(&k_full[st], L::kKV);
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(sK + st * L::kKV + c * L::kChunk, &tm_k, &k_full[st], c * 64, kvh, cur.start);
         issued = 2 * i + 1;
-        if (i >= kStages && !mbar_wait(&v_empty[st], par, &abort_flag)) break;
+        if (i >= kStages && !mbar_wait(&s_full[1], (i - 1) & 1, &abort_flag)) break;
         mbar_arrive_expect_tx(&v_full[st], L::kKV);
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(sV + st * L::kKV + c * L::kChunk, &tm_v, &v_full[st], c * 64, kvh, cur.start);
@@ -247,7 +254,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         umma_commit(&s_full[0]);
         issue_s(0, 1);
         umma_commit(&s_full[1]);
-        umma_commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < n_blocks; ++j) {
         const int st = j & 1;
@@ -259,13 +265,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!mbar_wait(&p_full[x], j & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after_sync();
           issue_pv(j, x);
-          if (x == 1) umma_commit(&v_empty[st]);
           if (more) {
             issue_s(j + 1, x);
             umma_commit(&s_full[x]);  // also reports O_x += P_x(j) V_j done
           }
         }
-        if (ok && more) umma_commit(&k_empty[(j + 1) & 1]);
       }
       umma_commit(&o_final[0]);
       umma_commit(&o_final[1]);
