@@ -78,7 +78,7 @@ static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
     const int32_t* __restrict__ idx, long long t_local, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ cup, int num_docs, long long T, AttnWorkspace ws, int32_t* err) {
   constexpr int kWarps = ROWS / 32;
-  __shared__ unsigned long long keys[ROWS];
+  __shared__ unsigned long long xbuf[2][ROWS];
   __shared__ int warp_sum[kWarps];
   __shared__ int red_blocks[kWarps];
   __shared__ int red_lo[kWarps];
@@ -89,6 +89,7 @@ static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
   const int lane = t & 31, wid = t >> 5;
   const long long group = blockIdx.x;
   const long long row = group * ROWS + t;
+  const int p = (row < t_local) ? idx[row] : 0;  // issued before anything waits
 
   for (long long j = blockIdx.x * (long long)ROWS + t; j <= num_docs; j += (long long)gridDim.x * ROWS) {
     if (j == 0 && (cu[0] != 0 || cup[0] != 0)) record_error(err, CPTHD_ERR_BAD_OFFSETS, 0);
@@ -105,7 +106,6 @@ static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
   bool valid = false;
   int doc = 0;
   if (row < t_local) {
-    const int p = idx[row];
     if (p < 0 || p >= T) {
       record_error(err, CPTHD_ERR_INDEX_RANGE, row);
     } else {
@@ -120,22 +120,31 @@ static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
   }
   ws.row_lo[row] = lo;
   ws.row_hi[row] = hi;
-  keys[t] = valid ? ((static_cast<unsigned long long>(doc) << 32) | static_cast<unsigned>(hi)) : ~0ull;
-  __syncthreads();
-  // bitonic sort of the (document, end) keys, ascending
+  // bitonic sort of the (document, end) keys, ascending, one key per
+  // thread: partners closer than 32 rows are in the same warp and exchange
+  // through shuffles; farther partners go through shared memory (double
+  // buffered, one barrier per such stage)
+  unsigned long long key = valid ? ((static_cast<unsigned long long>(doc) << 32) | static_cast<unsigned>(hi)) : ~0ull;
+  int buf = 0;
   for (int k = 2; k <= ROWS; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      const int ixj = t ^ j;
-      if (ixj > t) {
-        const unsigned long long a = keys[t], b = keys[ixj];
-        const bool up = ((t & k) == 0);
-        if ((a > b) == up) { keys[t] = b; keys[ixj] = a; }
+      unsigned long long other;
+      if (j >= 32) {
+        xbuf[buf][t] = key;
+        __syncthreads();
+        other = xbuf[buf][t ^ j];
+        buf ^= 1;
+      } else {
+        other = __shfl_xor_sync(0xffffffffu, key, j);
       }
-      __syncthreads();
+      const bool up = ((t & k) == 0);
+      const bool lower = ((t & j) == 0);
+      key = (lower == up) ? (key < other ? key : other) : (key > other ? key : other);
     }
   }
-  const unsigned long long key = keys[t];
-  const unsigned long long nxt = (t + 1 < ROWS) ? keys[t + 1] : ~0ull;
+  xbuf[buf][t] = key;
+  __syncthreads();
+  const unsigned long long nxt = (t + 1 < ROWS) ? xbuf[buf][t + 1] : ~0ull;
   const bool last = (key != ~0ull) && ((nxt >> 32) != (key >> 32));
   int my_lo = 0, my_hi = -1, my_blocks = 0;
   if (last) {

@@ -146,6 +146,28 @@ def test_edge_cases(case):
     assert err.cpu().tolist() == [0, 0]
 
 
+@pytest.mark.parametrize("n_docs", [4095, 5000])
+def test_many_short_documents(n_docs):
+    """Thousands of 1-6 token documents: a row group holds dozens of
+    documents, so the metadata's interval lists are long; every row of every
+    rank against the oracle."""
+    dev = cuda_or_skip(); cp = load_lib()
+    rng = np.random.default_rng(n_docs)
+    lengths = rng.integers(1, 7, size=n_docs).tolist()
+    inp = _custom(lengths, 4, 4, 2, 64, 17)
+    d = DevInputs(inp, dev)
+    lay = inp.layout
+    err = new_err(dev)
+    for s in ("dcs", "nlb"):
+        for r in range(2):
+            idx, out, lse = _run_rank(cp, d, s, 2, r, err)
+            ref_idx = np.asarray(P.partition_index(s, lay.cu_seqlens_padded.tolist(), 2, r))
+            ro, rl = A.attention_fwd(inp.q[torch.from_numpy(ref_idx)], inp.k, inp.v, lay.cu_seqlens,
+                                     lay.cu_seqlens_padded, ref_idx)
+            assert_attn_matches(out, lse, ro, rl, f"{n_docs} docs/{s}/rank{r}")
+    assert err.cpu().tolist() == [0, 0]
+
+
 def test_custom_scale_and_permuted_rows():
     """Any row order of the query slice works (the slice index travels with
     the rows), and an explicit softmax scale is honoured."""

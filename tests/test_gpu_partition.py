@@ -115,3 +115,26 @@ def test_kv_restore_round_trip_full_size(name, strategy):
     back = cp.cp_reorder(gathered, restore, err=err)
     assert torch.equal(back.view(torch.int16), k.view(torch.int16))
     assert err.cpu().tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("n_docs", [4095, 4096, 6000])
+def test_many_documents(n_docs):
+    """Thousands of short documents (deep binary searches over the offset
+    table), empty documents mixed in: partition and restore index bit exact."""
+    dev = cuda_or_skip(); cp = load_lib()
+    rng = np.random.default_rng(n_docs)
+    for cpsize in (2, 3):
+        lay = W.random_layout(rng, n_docs, 10, 2 * cpsize, allow_empty=True)
+        cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
+        err = new_err(dev)
+        for s in ("dcs", "nlb"):
+            if lay.T % cpsize:
+                continue
+            for r in range(cpsize):
+                got = cp.cp_partition_index(s, cup, lay.T, cpsize, r, err=err).cpu().numpy()
+                ref = np.asarray(P.partition_index(s, lay.cu_seqlens_padded.tolist(), cpsize, r), dtype=np.int32)
+                assert np.array_equal(got, ref), (s, cpsize, r)
+            got = cp.cp_restore_index(s, cup, lay.T, cpsize, err=err).cpu().numpy()
+            ref = np.asarray(P.restore_index(s, lay.cu_seqlens_padded.tolist(), cpsize), dtype=np.int32)
+            assert np.array_equal(got, ref), (s, cpsize)
+        assert err.cpu().tolist() == [0, 0]
