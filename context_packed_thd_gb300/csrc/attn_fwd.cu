@@ -330,6 +330,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const bool full = (kstart >= tmax_lo) && (kstart + kBlockN - 1 <= min(tmin_hi, kend));
       // 16-column groups of this block that no row of the warp may use
       uint32_t dead_groups = 0;
+      bool row_dead = false;  // this row has no key in this block
       if (!full) {
         // allowed columns of this row: [c_lo, c_hi] (empty when c_lo > c_hi)
         const int c_lo = min(max(lo - kstart, 0), kBlockN);
@@ -344,25 +345,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int c = 0; c < kBlockN; ++c)
             sr[c] = __float_as_uint(fmaf(__saturatef(f_lo - static_cast<float>(c)), -kMaskShift, __uint_as_float(sr[c])));
         }
-        if (c_lo > c_hi) c_hi = -1;
-        const int w_min = __reduce_min_sync(0xffffffffu, c_hi);
+        row_dead = (c_lo > c_hi);
+        if (row_dead) c_hi = -1;
+        // bounds over the warp's live rows (a warp whose rows straddle a
+        // document boundary still skips the mask where its live rows may use
+        // every column); dead rows are zeroed below whatever their scores
+        const int w_min = __reduce_min_sync(0xffffffffu, row_dead ? kBlockN - 1 : c_hi);
         const int w_max = __reduce_max_sync(0xffffffffu, c_hi);
         // The mask runs on the FMA pipe: u = saturate(c - c_hi) is 1 exactly
         // for columns past the row's last key (c is an integer), and
         // s - u * 2^100 pushes them far below any real score. A row left
         // with no key in this block is caught after the max (below), so no
-        // two huge values are ever subtracted from each other. Groups every
-        // row may use are left alone; groups no row may use become -inf and
-        // skip the exponentials.
+        // two huge values are ever subtracted from each other. Groups no row
+        // may use become -inf and skip the exponentials; groups every live
+        // row may use are left alone.
         const float f_hi = static_cast<float>(c_hi);
 #pragma unroll
         for (int g = 0; g < kBlockN / 16; ++g) {
-          if (16 * g + 15 <= w_min) continue;
           if (16 * g > w_max) {
             dead_groups |= 1u << g;
 #pragma unroll
             for (int c = 16 * g; c < 16 * g + 16; ++c) sr[c] = 0xff800000u;
-          } else {
+          } else if (16 * g + 15 > w_min) {
 #pragma unroll
             for (int c = 16 * g; c < 16 * g + 16; c += 2) {
               float s0, s1;
@@ -383,7 +387,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mx[u] = max3f(mx[u], __uint_as_float(sr[c + 2 * u]), __uint_as_float(sr[c + 2 * u + 1]));
       }
       float mx_row = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]));
-      if (mx_row < -0.5f * kMaskShift) mx_row = -INFINITY;  // no key of this row in this block
+      // no key of this row in this block
+      if (row_dead || mx_row < -0.5f * kMaskShift) mx_row = -INFINITY;
       const float m_new = fmaxf(m, mx_row * sl2);
       const bool grow_o = (m != -INFINITY) && (m_new > m + kRescaleThreshold);
       float alpha = 1.f;
@@ -394,7 +399,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         l *= alpha;
         m = m_new;
       }
-      const float mref = (m == -INFINITY) ? 0.f : m;
+      // a dead row subtracts 2^100 from every exponent, so all its p are 0
+      const float mref = row_dead ? kMaskShift : ((m == -INFINITY) ? 0.f : m);
       // p = 2^(scale*log2(e)*s - m): one packed FMA per pair, ex2 per element,
       // row sum in two packed accumulators; groups no row may use give p = 0
       float rs[4] = {0.f, 0.f, 0.f, 0.f};
