@@ -256,7 +256,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         umma_commit(&s_full[1]);
       }
       for (int j = 0; ok && j < n_blocks; ++j) {
-        const int st = j & 1;
         const bool more = (j + 1 < n_blocks);
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
@@ -335,45 +334,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // allowed columns of this row: [c_lo, c_hi] (empty when c_lo > c_hi)
         const int c_lo = min(max(lo - kstart, 0), kBlockN);
         int c_hi = max(min(min(hi, kend) - kstart, kBlockN - 1), -1);
-        // Blocks start at document starts, so a row either starts at or
-        // before the block (c_lo = 0) or has no key in it (c_lo > c_hi). The
-        // low-side mask is kept for any other case so that no row can ever
-        // use a key before its own start.
-        if (__any_sync(0xffffffffu, c_lo > 0 && c_lo <= c_hi)) {
-          const float f_lo = static_cast<float>(c_lo);
-#pragma unroll
-          for (int c = 0; c < kBlockN; ++c)
-            sr[c] = __float_as_uint(fmaf(__saturatef(f_lo - static_cast<float>(c)), -kMaskShift, __uint_as_float(sr[c])));
-        }
-        row_dead = (c_lo > c_hi);
+        // Blocks start at document starts, so with monotone offsets a row
+        // either starts at or before the block (c_lo = 0) or has no key in
+        // it (c_lo > c_hi). Anything else can only come from offsets the
+        // metadata kernel has already reported; such a row uses no key of
+        // the block, so it never reaches a key before its own start.
+        if (c_lo > 0 && c_lo <= c_hi) record_error(p.err, CPTHD_ERR_BAD_OFFSETS, grow);
+        row_dead = (c_lo > 0) || (c_hi < 0);
         if (row_dead) c_hi = -1;
         // bounds over the warp's live rows (a warp whose rows straddle a
         // document boundary still skips the mask where its live rows may use
         // every column); dead rows are zeroed below whatever their scores
         const int w_min = __reduce_min_sync(0xffffffffu, row_dead ? kBlockN - 1 : c_hi);
         const int w_max = __reduce_max_sync(0xffffffffu, c_hi);
-        // The mask runs on the FMA pipe: u = saturate(c - c_hi) is 1 exactly
-        // for columns past the row's last key (c is an integer), and
-        // s - u * 2^100 pushes them far below any real score. A row left
-        // with no key in this block is caught after the max (below), so no
-        // two huge values are ever subtracted from each other. Groups no row
-        // may use become -inf and skip the exponentials; groups every live
-        // row may use are left alone.
-        const float f_hi = static_cast<float>(c_hi);
+        dead_groups = (w_max < 0) ? 0xffu : ((0xffu << ((w_max >> 4) + 1)) & 0xffu);
+        if (w_max >= 0) {
+          // The mask runs on the FMA pipe: u = saturate(c - c_hi) is 1
+          // exactly for columns past the row's last key (c is an integer),
+          // and s - u * 2^100 pushes them far below any real score. A row
+          // left with no key in this block is caught after the max (below),
+          // so no two huge values are ever subtracted from each other.
+          // Groups every live row may use are left alone.
+          const float f_hi = static_cast<float>(c_hi);
 #pragma unroll
-        for (int g = 0; g < kBlockN / 16; ++g) {
-          if (16 * g > w_max) {
-            dead_groups |= 1u << g;
+          for (int g = 0; g < kBlockN / 16; ++g) {
+            if (16 * g + 15 > w_min) {
 #pragma unroll
-            for (int c = 16 * g; c < 16 * g + 16; ++c) sr[c] = 0xff800000u;
-          } else if (16 * g + 15 > w_min) {
-#pragma unroll
-            for (int c = 16 * g; c < 16 * g + 16; c += 2) {
-              float s0, s1;
-              fma2(s0, s1, __saturatef(static_cast<float>(c) - f_hi), __saturatef(static_cast<float>(c + 1) - f_hi),
-                   -kMaskShift, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-              sr[c] = __float_as_uint(s0);
-              sr[c + 1] = __float_as_uint(s1);
+              for (int c = 16 * g; c < 16 * g + 16; c += 2) {
+                float s0, s1;
+                fma2(s0, s1, __saturatef(static_cast<float>(c) - f_hi),
+                     __saturatef(static_cast<float>(c + 1) - f_hi), -kMaskShift, __uint_as_float(sr[c]),
+                     __uint_as_float(sr[c + 1]));
+                sr[c] = __float_as_uint(s0);
+                sr[c + 1] = __float_as_uint(s1);
+              }
             }
           }
         }
@@ -402,13 +396,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // a dead row subtracts 2^100 from every exponent, so all its p are 0
       const float mref = row_dead ? kMaskShift : ((m == -INFINITY) ? 0.f : m);
       // p = 2^(scale*log2(e)*s - m): one packed FMA per pair, ex2 per element,
-      // row sum in two packed accumulators; groups no row may use give p = 0
+      // row sum in two packed accumulators. A 64-column half no row may use
+      // stores zeros without exponentials; elsewhere masked columns give 0.
       float rs[4] = {0.f, 0.f, 0.f, 0.f};
-      if (dead_groups == 0) {
-        // straight-line form, so that the exponentials of a half overlap
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t pk[32];
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t pk[32];
+        if (((dead_groups >> (4 * h2)) & 0xfu) == 0xfu) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = 0u;
+        } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             float a0, a1;
@@ -418,32 +415,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             add2(rs[2 * (c & 1)], rs[2 * (c & 1) + 1], e0, e1);
             pk[c] = pack_bf16x2(e0, e1);
           }
-          tmem_st32(t_s + 32 * h2, pk);
         }
-      } else {
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int gg = 0; gg < 4; ++gg) {
-            if ((dead_groups >> (4 * h2 + gg)) & 1u) {
-#pragma unroll
-              for (int c = 8 * gg; c < 8 * gg + 8; ++c) pk[c] = 0u;
-            } else {
-#pragma unroll
-              for (int c = 8 * gg; c < 8 * gg + 8; ++c) {
-                float a0, a1;
-                fma2(a0, a1, __uint_as_float(sr[64 * h2 + 2 * c]), __uint_as_float(sr[64 * h2 + 2 * c + 1]), sl2,
-                     -mref);
-                const float e0 = ex2(a0);
-                const float e1 = ex2(a1);
-                add2(rs[2 * (c & 1)], rs[2 * (c & 1) + 1], e0, e1);
-                pk[c] = pack_bf16x2(e0, e1);
-              }
-            }
-          }
-          tmem_st32(t_s + 32 * h2, pk);
-        }
+        tmem_st32(t_s + 32 * h2, pk);
       }
       l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       if (__any_sync(0xffffffffu, grow_o)) {
