@@ -44,7 +44,8 @@
 //                fully), keeps the fp32 running max / sum in base 2, rescales
 //                O in TMEM only when the max grows by more than 2^8 (exact
 //                either way), and writes P back into TMEM. At the end it
-//                normalises O and writes out and LSE.
+//                normalises O into the tile's Q buffer in shared memory and
+//                one thread stores the tile with TMA; LSE per row.
 // Key blocks start at the group's interval starts (document starts), so
 // documents the group does not see are never loaded or multiplied. The grid
 // runs the groups in decreasing-cost order. Every wait is bounded; a wait
@@ -86,7 +87,6 @@ struct AttnParams {
   const GroupInfo* group_info;
   const int2* intervals;
   const int32_t* order;
-  __nv_bfloat16* out;
   float* lse;
   long long t_local;
   int Hq;
@@ -101,7 +101,8 @@ struct AttnParams {
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                       const AttnParams p) {
   using L = AttnSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -113,26 +114,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ uint64_t s_full[2], p_full[2], o_final[2], drain[1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ int epi_abort[2];
 
-  grid_dependency_wait();
-  grid_dependents_launch();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int units = p.head_pairs ? (p.Hq >> 1) : p.Hq;
-  const int item = blockIdx.x;
-  // without an order (a grid of one wave) the groups run in index order
-  const int group = p.order ? __ldg(p.order + item / units) : item / units;
-  const int unit = item % units;
-  const int head0 = p.head_pairs ? 2 * unit : unit;
-  const int kvh = head0 / (p.Hq / p.Hkv);
-  const GroupInfo gi = p.group_info[group];
-  const int n_blocks = min(max(gi.n_blocks, 0), p.max_blocks);
-  const int2* group_iv = p.intervals + static_cast<long long>(group) * p.group_rows;
-  const int n_iv = min(max(gi.n_intervals, 0), p.group_rows);
-  const long long group_row0 = static_cast<long long>(group) * p.group_rows;
-
+  // Barriers and TMEM are set up before waiting on the kernel this launch
+  // depends on: none of it touches global memory.
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    epi_abort[0] = epi_abort[1] = 0;
     mbar_init(&q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1);
@@ -155,6 +145,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
   // columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D, 256+2D)
+
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int units = p.head_pairs ? (p.Hq >> 1) : p.Hq;
+  const int item = blockIdx.x;
+  // without an order (a grid of one wave) the groups run in index order
+  const int group = p.order ? __ldg(p.order + item / units) : item / units;
+  const int unit = item % units;
+  const int head0 = p.head_pairs ? 2 * unit : unit;
+  const int kvh = head0 / (p.Hq / p.Hkv);
+  const GroupInfo gi = p.group_info[group];
+  const int n_blocks = min(max(gi.n_blocks, 0), p.max_blocks);
+  const int2* group_iv = p.intervals + static_cast<long long>(group) * p.group_rows;
+  const int n_iv = min(max(gi.n_intervals, 0), p.group_rows);
+  const long long group_row0 = static_cast<long long>(group) * p.group_rows;
 
   if (warp < 4) {
    setmaxnreg_dec<kRegsControl>();
@@ -247,6 +252,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int kk = 0; kk < kBlockN / 16; ++kk)
           umma_ts_w(t_o, t_s + kk * 8, vb + ((kk * 16 * 128) >> 4), v_hi, kIdescO, kk > 0 ? 1u : acc0);
       };
+      int finals = 0;
       bool ok = mbar_wait(&q_full, 0, &abort_flag) && mbar_wait(&k_full[0], 0, &abort_flag);
       if (ok) {
         tc_fence_after_sync();
@@ -267,11 +273,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (more) {
             issue_s(j + 1, x);
             umma_commit(&s_full[x]);  // also reports O_x += P_x(j) V_j done
+          } else {
+            umma_commit(&o_final[x]);  // tile x's epilogue need not wait for the other tile
+            finals |= 1 << x;
           }
         }
       }
-      umma_commit(&o_final[0]);
-      umma_commit(&o_final[1]);
+      // a tile whose final commit did not happen (no block, or an abort)
+      if (!(finals & 1)) umma_commit(&o_final[0]);
+      if (!(finals & 2)) umma_commit(&o_final[1]);
       umma_commit(&drain[0]);
       mbar_wait_drain(&drain[0], 0);
     }
@@ -438,12 +448,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (lane == 0) mbar_arrive(&p_full[x]);
     }
     // ---------------------------------------------------------- epilogue
+    // O / l in bf16 goes into this tile's Q buffer (free once o_final[x] is
+    // reported: the last MMA reading it is done), in the 128-byte swizzle of
+    // the output's tensor map, and one thread of the warpgroup stores the
+    // tile with TMA (rows past the slice are not written). Every warp of the
+    // warpgroup reaches the barrier; an aborted one only marks the tile.
     if (ok && n_blocks > 0) ok = warp_wait(&o_final[x], 0, &abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after_sync();
+    uint8_t* stile = sQ + x * L::kQ;
     if (ok) {
       const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.out + (grow * p.Hq + qh) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rr[32];
@@ -457,16 +472,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ob[q] = (valid && n_blocks > 0)
                       ? pack_bf16x2(__uint_as_float(rr[2 * q]) * inv, __uint_as_float(rr[2 * q + 1]) * inv)
                       : 0u;
-        if (grow < p.t_local) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(ob[4 * q4], ob[4 * q4 + 1], ob[4 * q4 + 2], ob[4 * q4 + 3]);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int u = 4 * c + q4;  // 16-byte unit of the row; 8 units per 64-column panel
+          uint8_t* dst = stile + (u >> 3) * L::kChunk + r * 128 + (((u & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(ob[4 * q4], ob[4 * q4 + 1], ob[4 * q4 + 2], ob[4 * q4 + 3]);
         }
       }
       if (grow < p.t_local)
         p.lse[static_cast<long long>(qh) * p.t_local + grow] =
             (valid && l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+      fence_proxy_async_smem();
+    } else {
+      epi_abort[x] = 1;
+    }
+    named_bar_sync(1 + x, 128);
+    const long long tile_row0 = group_row0 + (p.head_pairs ? 0 : x * kBlockM);
+    if (r == 0 && !epi_abort[x] && tile_row0 < p.t_local) {
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_store_3d(&tm_o, stile + c * L::kChunk, c * 64, qh, static_cast<int>(tile_row0));
+      bulk_commit_group();
+      bulk_wait_group_read_all();
     }
   }
 
@@ -484,9 +511,9 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
                        float* lse, int32_t* err, cudaStream_t s) {
   EncodeTiledFn enc = get_encode_tiled();
   if (enc == nullptr) return CPTHD_ERR_CUDA;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_rows_heads_map(enc, &mq, q, t_local, Hq, D) || !make_rows_heads_map(enc, &mk, k, T, Hkv, D) ||
-      !make_rows_heads_map(enc, &mv, v, T, Hkv, D))
+      !make_rows_heads_map(enc, &mv, v, T, Hkv, D) || !make_rows_heads_map(enc, &mo, out, t_local, Hq, D))
     return CPTHD_ERR_UNSUPPORTED;
   AttnParams p;
   p.row_lo = ws.row_lo;
@@ -494,7 +521,6 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
   p.group_info = ws.group_info;
   p.intervals = ws.intervals;
   p.order = ordered ? ws.order : nullptr;
-  p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.t_local = t_local;
   p.Hq = Hq;
@@ -509,7 +535,7 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
   const long long items = ngroups * (p.head_pairs ? Hq / 2 : Hq);
   if (items > INT32_MAX) return CPTHD_ERR_UNSUPPORTED;
   CPTHD_TRY_CUDA(launch_pdl(attn_fwd_tc_kernel<D>, dim3(static_cast<unsigned>(items)), dim3(kAttnThreads), smem, s,
-                            mq, mk, mv, p));
+                            mq, mk, mv, mo, p));
   return CPTHD_OK;
 }
 
