@@ -47,7 +47,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "causal-THD attn fwd TFLOPS (unmasked pairs) & % BF16 peak; reorder GB/s"
-DEFAULT_WORKLOAD = W.CONFIGS[1].name
+DEFAULT_WORKLOAD = "t8192_mha16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -89,7 +89,7 @@ def measured_traffic(workload: str, subset: bool):
     summary, or None when the workload differs or the kernel sources changed
     since the capture."""
     path = os.path.join(ROOT, "profiles", "attn_fwd_tc_t8192_traffic.md")
-    if subset or workload != W.CONFIGS[1].name or not os.path.exists(path):
+    if subset or workload != DEFAULT_WORKLOAD or not os.path.exists(path):
         return None
     txt = open(path).read()
     try:
@@ -267,8 +267,8 @@ def other_workloads(cp, current, dev, flush, peak):
     all its strategies in one CUDA graph (L2 flushed before each replay), so
     that the line also carries the long-context and many-document figures."""
     out = {}
-    for cfg in W.CONFIGS[1:]:
-        if cfg.name == current:
+    for cfg in W.CONFIGS:
+        if cfg.name in (current, "tiny"):
             continue
         sts = [Strategy(cp, cfg, s, dev) for s in cfg.strategies]
         for st in sts:
