@@ -528,7 +528,7 @@ def run_cuda(args):
     e2e_value = replica_value(flops_step, world, e2e_s) / 1e12
 
     # ---- each part of the step alone (graph replays, L2 flushed before each) --
-    reps = max(3, min(args.steps, 10))
+    reps = 20  # median of 20 replays per (strategy, rank) part
     attn_ms = [[0.0] * reps for _ in range(n_ranks)]
     prep_ms = [[0.0] * reps for _ in range(n_ranks)]
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
@@ -642,6 +642,19 @@ def _oracle_rank(cfg, strategy, r, cache):
     return dt, 4.0 * cfg.d * cfg.hq * rank_pairs(idx, lay)
 
 
+def cpu_model() -> str:
+    """Host CPU model name (best effort; Arm hosts report it through lscpu)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(cfg, seconds):
     """Time the oracle as it stands on a bounded sample: whole rank slices in
     (strategy, rank) order until about ``seconds`` of CPU work."""
@@ -659,6 +672,7 @@ def cpu_baseline(cfg, seconds):
             break
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": round(f_sum / t_sum / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{cfg.name}: rank slices {','.join(done)} (all heads, float64 numpy), {t_sum:.1f} s"}
 
 
@@ -686,7 +700,7 @@ def run_reference(args):
         "config": {"workload": cfg.name, "T": int(sum(cfg.lengths)), "Hq": cfg.hq, "Hkv": cfg.hkv, "d": cfg.d,
                    "cp_size": cfg.cp, "strategies": list(cfg.strategies)},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
