@@ -37,8 +37,8 @@ struct BwdSmem {
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = kChunks * kChunk;  // one 128-row bf16 tile of Q, dO, K or V
   static constexpr int kCol = 4 * kBlockM * 4;    // row_lo, row_hi, lse2, D of 128 query rows
-  // dQ pass: Q, dO, K[2], V[2]
-  static constexpr int kDqBytes = 6 * kTile;
+  // dQ pass: Q, dO, K[3], V[2]
+  static constexpr int kDqBytes = 7 * kTile;
   // dK/dV pass: K, V, Q[2], dO[2], column info[2], tile list
   static constexpr int kDkvBytes = 6 * kTile + 2 * kCol + kBwdMaxTiles * 4;
   static constexpr int launch(int b) { return (b + 1024 > 120 * 1024) ? b + 1024 : 120 * 1024; }
@@ -99,6 +99,12 @@ __device__ __forceinline__ void umma_desc_words(uint64_t d, uint32_t& lo, uint32
 }
 
 // ------------------------------------------------------------------ dQ pass
+// Software-pipelined over key blocks. TMEM holds two score buffers (S_0,
+// S_1), dP and the dQ accumulator, so S(j+1) is computed while the
+// elementwise warps turn block j into dS, and dP(j+1) is issued before
+// dQ(j) += dS(j) K(j), so the next block's elementwise work overlaps dQ(j).
+// K is held until dQ(j) and rides a three-stage ring; V, read by dP(j) only,
+// a two-stage ring.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -109,10 +115,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + L::kTile;
-  uint8_t* sK = smem + 2 * L::kTile;  // two stages
-  uint8_t* sV = smem + 4 * L::kTile;  // two stages
+  uint8_t* sK = smem + 2 * L::kTile;  // three stages
+  uint8_t* sV = smem + 5 * L::kTile;  // two stages
 
-  __shared__ uint64_t qdo_full, k_full[2], v_full[2], kv_empty[2], sdp_full, ds_full, dq_final, drain;
+  __shared__ uint64_t qdo_full, k_full[3], k_empty[3], v_full[2], v_empty[2], sdp_full, ds_full, dq_final, drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -128,10 +134,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&qdo_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(&sdp_full, 1);
     mbar_init(&ds_full, 4);
@@ -146,7 +155,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem = tmem_base_sh;  // S [0,128), dP [128,256), dQ [256, 256+D)
+  const uint32_t tmem = tmem_base_sh;  // S_0 [0,128), dP [128,256), dQ [256, 256+D), S_1 [384, 512)
 
   if (warp == 0) {
     if (lane == 0 && n_blocks > 0) {
@@ -157,25 +166,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       BlockCursor cur;
       cur.init(tile_iv, n_iv);
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int i = 0; i < n_blocks; ++i) {
-        const int st = i & 1;
-        if (i >= 2 && !mbar_wait(&kv_empty[st], ((i >> 1) + 1) & 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&k_full[st], L::kTile);
+        // K(i) reuses the stage of K(i-3) (released by dQ(i-3)); V(i) that
+        // of V(i-2) (released by dP(i-2)). Each release completes only
+        // after loads issued here, so no wait runs two phases behind.
+        const int ks = i % 3, vs = i & 1;
+        if (i >= 3 && !mbar_wait(&k_empty[ks], ((i / 3) + 1) & 1, &abort_flag)) break;
+        mbar_arrive_expect_tx(&k_full[ks], L::kTile);
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sK + st * L::kTile + c * L::kChunk, &tm_k, &k_full[st], c * 64, kvh, cur.start);
-        mbar_arrive_expect_tx(&v_full[st], L::kTile);
+          tma_load_3d(sK + ks * L::kTile + c * L::kChunk, &tm_k, &k_full[ks], c * 64, kvh, cur.start);
+        k_issued = i + 1;
+        if (i >= 2 && !mbar_wait(&v_empty[vs], ((i >> 1) + 1) & 1, &abort_flag)) break;
+        mbar_arrive_expect_tx(&v_full[vs], L::kTile);
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sV + st * L::kTile + c * L::kChunk, &tm_v, &v_full[st], c * 64, kvh, cur.start);
-        issued = i + 1;
+          tma_load_3d(sV + vs * L::kTile + c * L::kChunk, &tm_v, &v_full[vs], c * 64, kvh, cur.start);
+        v_issued = i + 1;
         cur.next();
       }
       if (abort_flag) {
+        // let every copy still in flight land before the CTA exits
         mbar_wait_drain(&qdo_full, 0);
-        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) {
-          mbar_wait_drain(&k_full[i & 1], (i >> 1) & 1);
-          mbar_wait_drain(&v_full[i & 1], (i >> 1) & 1);
-        }
+        for (int i = (k_issued > 3 ? k_issued - 3 : 0); i < k_issued; ++i) mbar_wait_drain(&k_full[i % 3], (i / 3) & 1);
+        for (int i = (v_issued > 2 ? v_issued - 2 : 0); i < v_issued; ++i) mbar_wait_drain(&v_full[i & 1], (i >> 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -188,32 +201,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       umma_desc_words(smem_desc_sw128(smem_u32(sK), 16, 1024), k_lo, k_hi);
       umma_desc_words(smem_desc_sw128(smem_u32(sK), L::kChunk, 1024), kmn_lo, kmn_hi);
       umma_desc_words(smem_desc_sw128(smem_u32(sV), 16, 1024), v_lo, v_hi);
-      bool ok = mbar_wait(&qdo_full, 0, &abort_flag);
-      for (int j = 0; ok && j < n_blocks; ++j) {
-        const int st = j & 1;
-        const uint32_t so = (st * L::kTile) >> 4;
-        if (!mbar_wait(&k_full[st], (j >> 1) & 1, &abort_flag)) break;
-        if (!mbar_wait(&v_full[st], (j >> 1) & 1, &abort_flag)) break;
-        tc_fence_after_sync();
+      auto t_sbuf = [&](int j) { return tmem + ((j & 1) ? 384u : 0u); };
+      auto issue_s = [&](int j) {  // S(j) = Q K(j)^T into S_(j&1)
+        const uint32_t so = ((j % 3) * L::kTile) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
-          umma_ss_w(tmem, q_lo + off, q_hi, k_lo + so + off, k_hi, kIdS, kk > 0);
+          umma_ss_w(t_sbuf(j), q_lo + off, q_hi, k_lo + so + off, k_hi, kIdS, kk > 0);
         }
+      };
+      auto issue_dp = [&](int j) {  // dP(j) = dO V(j)^T
+        const uint32_t so = ((j & 1) * L::kTile) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
           umma_ss_w(tmem + 128, do_lo + off, do_hi, v_lo + so + off, v_hi, kIdS, kk > 0);
         }
+      };
+      bool ok = mbar_wait(&qdo_full, 0, &abort_flag) && mbar_wait(&k_full[0], 0, &abort_flag) &&
+                mbar_wait(&v_full[0], 0, &abort_flag);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_s(0);
+        issue_dp(0);
         umma_commit(&sdp_full);
+        umma_commit(&v_empty[0]);
+      }
+      for (int j = 0; ok && j < n_blocks; ++j) {
+        const bool more = (j + 1 < n_blocks);
+        if (more) {  // S(j+1) while the elementwise warps work on block j
+          if (!mbar_wait(&k_full[(j + 1) % 3], ((j + 1) / 3) & 1, &abort_flag)) break;
+          tc_fence_after_sync();
+          issue_s(j + 1);
+        }
+        // dS(j) is in S_(j&1) and dP(j) has been read
         if (!mbar_wait(&ds_full, j & 1, &abort_flag)) break;
         tc_fence_after_sync();
+        if (more) {
+          if (!mbar_wait(&v_full[(j + 1) & 1], ((j + 1) >> 1) & 1, &abort_flag)) break;
+          tc_fence_after_sync();
+          issue_dp(j + 1);
+          umma_commit(&sdp_full);  // reports S(j+1) and dP(j+1)
+          umma_commit(&v_empty[(j + 1) & 1]);
+        }
         const uint32_t acc0 = (j > 0) ? 1u : 0u;
+        const uint32_t ko = ((j % 3) * L::kTile) >> 4;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)  // dQ += dS K, dS from TMEM, K as the MN-major operand
-          umma_ts_w(tmem + 256, tmem + kk * 8, kmn_lo + so + ((kk * 16 * 128) >> 4), kmn_hi, kIdQ,
+          umma_ts_w(tmem + 256, t_sbuf(j) + kk * 8, kmn_lo + ko + ((kk * 16 * 128) >> 4), kmn_hi, kIdQ,
                     kk > 0 ? 1u : acc0);
-        umma_commit(&kv_empty[st]);
+        umma_commit(&k_empty[j % 3]);
       }
       umma_commit(&dq_final);
       umma_commit(&drain);
@@ -227,7 +264,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float lse2 = p.lse2[(long long)h * p.rows_pad + grow];
     const float drow = p.dvec[(long long)h * p.rows_pad + grow];
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128, t_q = tmem + lane_off + 256;
+    const uint32_t t_dp = tmem + lane_off + 128, t_q = tmem + lane_off + 256;
     const float sl2 = p.scale_log2;
     BlockCursor cur;
     cur.init(tile_iv, n_iv);
@@ -237,6 +274,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       cur.next();
       if (!warp_wait(&sdp_full, j & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after_sync();
+      const uint32_t t_s = tmem + lane_off + ((j & 1) ? 384u : 0u);
+      // allowed columns [c_lo, c_hi]; a pad row gets an empty range
       const int c_lo = min(max(lo - kstart, 0), kBlockN);
       const int c_hi = max(min(min(hi, kend) - kstart, kBlockN - 1), -1);
 #pragma unroll
@@ -317,7 +356,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sCol = smem + 6 * L::kTile; // two stages of {row_lo, row_hi, lse2, D} x 128
   int* sList = reinterpret_cast<int*>(sCol + 2 * L::kCol);
 
-  __shared__ uint64_t kv_full, qdo_full[2], qdo_empty[2], sdp_full, pds_full, kv_final, drain;
+  __shared__ uint64_t kv_full, qdo_full[2], qdo_empty[2], sdp_full[2], pds_full[2], kv_final, drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, list_n;
 
@@ -353,9 +392,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&qdo_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
+      mbar_init(&sdp_full[s], 1);
+      mbar_init(&pds_full[s], 4);
     }
-    mbar_init(&sdp_full, 1);
-    mbar_init(&pds_full, 4);
     mbar_init(&kv_final, 1);
     mbar_init(&drain, 1);
     fence_mbar_init();
@@ -367,7 +406,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem = tmem_base_sh;  // S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D)
+  // S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D). An item
+  // (query tile, head) is processed as two halves of 64 queries: half x uses
+  // columns [64x, 64x+64) of S^T and dP^T, its P^T / dS^T (bf16) go to the
+  // first 32 of them. Once a half's dV / dK MMAs are issued, the next item's
+  // scores for that half can be computed while the elementwise warps work on
+  // the other half.
+  const uint32_t tmem = tmem_base_sh;
 
   if (warp == 0) {
     if (lane == 0 && n_items > 0) {
@@ -403,7 +448,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && n_items > 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
+      constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN / 2, 0, 0);  // 128 keys x 64 queries
       constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, D, 0, 1);
       uint32_t k_lo, k_hi, v_lo, v_hi, q_lo, q_hi, do_lo, do_hi, qmn_lo, qmn_hi, domn_lo, domn_hi;
       umma_desc_words(smem_desc_sw128(smem_u32(sK), 16, 1024), k_lo, k_hi);
@@ -412,37 +457,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       umma_desc_words(smem_desc_sw128(smem_u32(sDO), 16, 1024), do_lo, do_hi);
       umma_desc_words(smem_desc_sw128(smem_u32(sQ), L::kChunk, 1024), qmn_lo, qmn_hi);
       umma_desc_words(smem_desc_sw128(smem_u32(sDO), L::kChunk, 1024), domn_lo, domn_hi);
-      bool ok = mbar_wait(&kv_full, 0, &abort_flag);
+      // S^T_x = K Q_x^T and dP^T_x = V dO_x^T for query half x (rows 64x..64x+63
+      // of the stage's Q / dO tile: 64 rows of 128 bytes further in each panel)
+      auto issue_sdp = [&](int i, int x) {
+        const uint32_t so = ((i & 1) * L::kTile + x * 64 * 128) >> 4;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+          umma_ss_w(tmem + 64 * x, k_lo + off, k_hi, q_lo + so + off, q_hi, kIdS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+          umma_ss_w(tmem + 128 + 64 * x, v_lo + off, v_hi, do_lo + so + off, do_hi, kIdS, kk > 0);
+        }
+      };
+      // dV += P^T_x dO_x and dK += dS^T_x Q_x over the half's 64 queries
+      auto issue_dkdv = [&](int i, int x) {
+        const uint32_t so = ((i & 1) * L::kTile) >> 4;
+#pragma unroll
+        for (int kk = 4 * x; kk < 4 * x + 4; ++kk)
+          umma_ts_w(tmem + 256, tmem + 64 * x + (kk - 4 * x) * 8, domn_lo + so + ((kk * 16 * 128) >> 4), domn_hi,
+                    kIdO, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 4 * x; kk < 4 * x + 4; ++kk)
+          umma_ts_w(tmem + 256 + D, tmem + 128 + 64 * x + (kk - 4 * x) * 8, qmn_lo + so + ((kk * 16 * 128) >> 4),
+                    qmn_hi, kIdO, (i > 0 || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(&kv_full, 0, &abort_flag) && mbar_wait(&qdo_full[0], 0, &abort_flag);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_sdp(0, 0);
+        umma_commit(&sdp_full[0]);
+        issue_sdp(0, 1);
+        umma_commit(&sdp_full[1]);
+      }
       for (int i = 0; ok && i < n_items; ++i) {
-        const int st = i & 1;
-        const uint32_t so = (st * L::kTile) >> 4;
-        if (!mbar_wait(&qdo_full[st], (i >> 1) & 1, &abort_flag)) break;
-        tc_fence_after_sync();
+        const bool more = (i + 1 < n_items);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
-          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
-          umma_ss_w(tmem, k_lo + off, k_hi, q_lo + so + off, q_hi, kIdS, kk > 0);
+        for (int x = 0; x < 2; ++x) {
+          // P^T_x(i) and dS^T_x(i) are in TMEM
+          if (!mbar_wait(&pds_full[x], i & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after_sync();
+          issue_dkdv(i, x);
+          if (x == 1) umma_commit(&qdo_empty[i & 1]);  // Q(i), dO(i) and their column data are free
+          if (more) {
+            if (x == 0 && !mbar_wait(&qdo_full[(i + 1) & 1], ((i + 1) >> 1) & 1, &abort_flag)) { ok = false; break; }
+            tc_fence_after_sync();
+            issue_sdp(i + 1, x);  // overwrites half x only after its dV / dK MMAs (issue order)
+            umma_commit(&sdp_full[x]);
+          }
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
-          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
-          umma_ss_w(tmem + 128, v_lo + off, v_hi, do_lo + so + off, do_hi, kIdS, kk > 0);
-        }
-        umma_commit(&sdp_full);
-        if (!mbar_wait(&pds_full, i & 1, &abort_flag)) break;
-        tc_fence_after_sync();
-        const uint32_t acc0 = (i > 0) ? 1u : 0u;
-#pragma unroll
-        for (int kk = 0; kk < kBlockM / 16; ++kk) {  // dV += P^T dO
-          umma_ts_w(tmem + 256, tmem + kk * 8, domn_lo + so + ((kk * 16 * 128) >> 4), domn_hi, kIdO,
-                    kk > 0 ? 1u : acc0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < kBlockM / 16; ++kk) {  // dK += dS^T Q
-          umma_ts_w(tmem + 256 + D, tmem + 128 + kk * 8, qmn_lo + so + ((kk * 16 * 128) >> 4), qmn_hi, kIdO,
-                    kk > 0 ? 1u : acc0);
-        }
-        umma_commit(&qdo_empty[st]);
       }
       umma_commit(&kv_final);
       umma_commit(&drain);
@@ -457,54 +522,59 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t t_v = tmem + lane_off + 256, t_k = tmem + lane_off + 256 + D;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int i = 0; i < n_items; ++i) {
+    for (int i = 0; ok && i < n_items; ++i) {
       const int st = i & 1;
       // the column data arrived with Q/dO through the TMA barrier
       if (!warp_wait(&qdo_full[st], (i >> 1) & 1, &abort_flag)) { ok = false; break; }
-      if (!warp_wait(&sdp_full, i & 1, &abort_flag)) { ok = false; break; }
-      tc_fence_after_sync();
       const int* c_lo = reinterpret_cast<const int*>(sCol + st * L::kCol);
       const int* c_hi = c_lo + kBlockM;
       const float* c_l2 = reinterpret_cast<const float*>(c_lo + 2 * kBlockM);
       const float* c_d = c_l2 + kBlockM;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t sv[32], dp[32];
-        tmem_ld32(t_s + 32 * c4, sv);
-        tmem_ld32(t_dp + 32 * c4, dp);
-        tmem_ld_wait(sv);
-        tmem_ld_wait(dp);
-        uint32_t pp[16], pd[16];
+      for (int x = 0; x < 2; ++x) {
+        if (!warp_wait(&sdp_full[x], i & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after_sync();
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const int col = 32 * c4 + 4 * q4;
-          const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
-          const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
-          const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
-          const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
-          const int los[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
-          const int his[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
-          const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
-          const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dsv[4];
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int cb = 64 * x + 32 * c2;  // first query column of this 32-column slab
+          uint32_t sv[32], dp[32];
+          tmem_ld32(t_s + cb, sv);
+          tmem_ld32(t_dp + cb, dp);
+          tmem_ld_wait(sv);
+          tmem_ld_wait(dp);
+          uint32_t pp[16], pd[16];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float e = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
-            pv[u] = (key >= los[u] && key <= his[u]) ? e : 0.f;
-            dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const int col = cb + 4 * q4;
+            const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
+            const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
+            const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
+            const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
+            const int los[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
+            const int his[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+            const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
+            const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dsv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float e = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
+              pv[u] = (key >= los[u] && key <= his[u]) ? e : 0.f;
+              dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
+            }
+            pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
+            pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
+            pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+            pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
           }
-          pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
-          pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
-          pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-          pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          // bf16 pairs over the half's first 32 columns, already read
+          tmem_st16(t_s + 64 * x + 16 * c2, pp);
+          tmem_st16(t_dp + 64 * x + 16 * c2, pd);
         }
-        tmem_st16(t_s + 16 * c4, pp);
-        tmem_st16(t_dp + 16 * c4, pd);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pds_full[x]);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pds_full);
     }
     if (ok && n_items > 0) ok = warp_wait(&kv_final, 0, &abort_flag);
     ok = __all_sync(0xffffffffu, ok);
