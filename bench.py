@@ -588,10 +588,11 @@ def run_cuda(args):
     prep_total_ms = sum(med_prep)
     act = activation_reorder(cp, cfg, strategies[0], ranks, flush, dev, hbm_peak) if cfg.act_width else None
     dcs_st = [st for st in strategies if st.name == W.DUAL_CHUNK_SWAP]
-    restore = kv_restore(cp, cfg, dcs_st[0], flush, dev, hbm_peak) if dcs_st and not args.no_extras else None
-    two = dcs_two_launch(cp, cfg, dcs_st[0], ranks, flush) if dcs_st and not args.no_extras else None
-    bwd = backward(cp, cfg, strategies, ranks, flush, peak) if not args.no_extras else None
-    others = other_workloads(cp, cfg.name, dev, flush, peak) if not args.no_extras else None
+    extras = set() if args.no_extras else set(args.extras.split(","))
+    restore = kv_restore(cp, cfg, dcs_st[0], flush, dev, hbm_peak) if dcs_st and "restore" in extras else None
+    two = dcs_two_launch(cp, cfg, dcs_st[0], ranks, flush) if dcs_st and "two_launch" in extras else None
+    bwd = backward(cp, cfg, strategies, ranks, flush, peak) if "backward" in extras else None
+    others = other_workloads(cp, cfg.name, dev, flush, peak) if "others" in extras else None
 
 
     for st in strategies:
@@ -736,7 +737,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the K/V restore, one-vs-two-launch and backward measurements")
+                    help="skip the K/V restore, one-vs-two-launch, backward and other-workload measurements")
+    ap.add_argument("--extras", default="restore,two_launch,backward,others",
+                    help="comma-separated extras to run (restore, two_launch, backward, others)")
     ap.add_argument("--strategy", choices=list(W.ALL_STRATEGIES), default=None,
                     help="time one strategy only (profiling); the headline runs every strategy")
     ap.add_argument("--rank", type=int, default=None,
