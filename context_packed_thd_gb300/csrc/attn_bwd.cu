@@ -67,6 +67,8 @@ struct BwdParams {
 };
 
 // D = rowsum(dO * O) and lse * log2(e), laid out [Hq, rows_pad]; one warp per (row, head).
+// A row with no key (a pad row, LSE = -inf) or past the slice gets +inf, so
+// that 2^(s*scale*log2(e) - lse2) is exactly 0 for it without any mask.
 template <int D>
 static __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
                                                                   const __nv_bfloat16* __restrict__ dout,
@@ -77,13 +79,14 @@ static __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfl
   if (w >= (long long)rows_pad * Hq) return;
   const long long row = w / Hq;
   const int h = static_cast<int>(w - row * Hq);
-  float acc = 0.f, l2 = 0.f;
+  float acc = 0.f, l2 = INFINITY;
   if (row < t_local) {
     const __nv_bfloat16* o = out + (row * Hq + h) * D;
     const __nv_bfloat16* g = dout + (row * Hq + h) * D;
 #pragma unroll
     for (int e = lane; e < D; e += 32) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
-    l2 = lse[(long long)h * t_local + row] * 1.4426950408889634f;
+    const float l = lse[(long long)h * t_local + row];
+    l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -266,6 +269,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_dp = tmem + lane_off + 128, t_q = tmem + lane_off + 256;
     const float sl2 = p.scale_log2;
+    const int tmax_lo = ti.max_lo[0], tmin_hi = ti.min_hi[0];
     BlockCursor cur;
     cur.init(tile_iv, n_iv);
     bool ok = true;
@@ -275,7 +279,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!warp_wait(&sdp_full, j & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after_sync();
       const uint32_t t_s = tmem + lane_off + ((j & 1) ? 384u : 0u);
-      // allowed columns [c_lo, c_hi]; a pad row gets an empty range
+      // allowed columns [c_lo, c_hi]; a pad row gets an empty range. A block
+      // inside every real row's key interval needs no mask (a row without
+      // keys has lse2 = +inf, so its p are 0 anyway).
+      const bool full = (kstart >= tmax_lo) && (kstart + kBlockN - 1 <= min(tmin_hi, kend));
       const int c_lo = min(max(lo - kstart, 0), kBlockN);
       const int c_hi = max(min(min(hi, kend) - kstart, kBlockN - 1), -1);
 #pragma unroll
@@ -286,17 +293,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_wait(sv);
         tmem_ld_wait(dp);
         uint32_t pk[16];
+        if (full) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          float ds2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = 32 * c4 + 2 * q + u;
-            const float e = ex2(fmaf(__uint_as_float(sv[2 * q + u]), sl2, -lse2));
-            const float pv = (col >= c_lo && col <= c_hi) ? e : 0.f;
-            ds2[u] = pv * (__uint_as_float(dp[2 * q + u]) - drow);
+          for (int q = 0; q < 16; ++q) {
+            const float e0 = ex2(fmaf(__uint_as_float(sv[2 * q]), sl2, -lse2));
+            const float e1 = ex2(fmaf(__uint_as_float(sv[2 * q + 1]), sl2, -lse2));
+            pk[q] = pack_bf16x2(e0 * (__uint_as_float(dp[2 * q]) - drow), e1 * (__uint_as_float(dp[2 * q + 1]) - drow));
           }
-          pk[q] = pack_bf16x2(ds2[0], ds2[1]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            float ds2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int col = 32 * c4 + 2 * q + u;
+              const float e = ex2(fmaf(__uint_as_float(sv[2 * q + u]), sl2, -lse2));
+              const float pv = (col >= c_lo && col <= c_hi) ? e : 0.f;
+              ds2[u] = pv * (__uint_as_float(dp[2 * q + u]) - drow);
+            }
+            pk[q] = pack_bf16x2(ds2[0], ds2[1]);
+          }
         }
         tmem_st16(t_s + 16 * c4, pk);  // dS over S columns already read
       }
@@ -355,6 +371,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sDO = smem + 4 * L::kTile;  // two stages
   uint8_t* sCol = smem + 6 * L::kTile; // two stages of {row_lo, row_hi, lse2, D} x 128
   int* sList = reinterpret_cast<int*>(sCol + 2 * L::kCol);
+  __shared__ uint8_t sFull[kBwdMaxTiles];  // every real row of the listed tile sees all 128 keys
 
   __shared__ uint64_t kv_full, qdo_full[2], qdo_empty[2], sdp_full[2], pds_full[2], kv_final, drain;
   __shared__ uint32_t tmem_base_sh;
@@ -380,7 +397,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (rel) {
       const int slot = atomicAdd(&list_n, 1);
-      if (slot < kBwdMaxTiles) sList[slot] = t;
+      if (slot < kBwdMaxTiles) {
+        sList[slot] = t;
+        sFull[slot] = (ti.max_lo[0] <= K0 && ti.min_hi[0] >= K0 + kBlockN - 1) ? 1 : 0;
+      }
     }
   }
   __syncthreads();
@@ -530,6 +550,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int* c_hi = c_lo + kBlockM;
       const float* c_l2 = reinterpret_cast<const float*>(c_lo + 2 * kBlockM);
       const float* c_d = c_l2 + kBlockM;
+      const bool item_full = sFull[i / group] != 0;
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
         if (!warp_wait(&sdp_full[x], i & 1, &abort_flag)) { ok = false; break; }
@@ -543,28 +564,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_wait(sv);
           tmem_ld_wait(dp);
           uint32_t pp[16], pd[16];
+          if (item_full) {
+            // no mask: every real query of the tile sees every key of the
+            // tile, and rows without keys have lse2 = +inf (p = 0)
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const int col = cb + 4 * q4;
-            const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
-            const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
-            const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
-            const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
-            const int los[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
-            const int his[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
-            const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
-            const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dsv[4];
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const int col = cb + 4 * q4;
+              const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
+              const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
+              const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
+              const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
+              float pv[4], dsv[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float e = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
-              pv[u] = (key >= los[u] && key <= his[u]) ? e : 0.f;
-              dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
+              for (int u = 0; u < 4; ++u) {
+                pv[u] = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
+                dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
+              }
+              pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
+              pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
+              pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+              pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
             }
-            pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
-            pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
-            pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-            pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const int col = cb + 4 * q4;
+              const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
+              const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
+              const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
+              const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
+              const int los[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
+              const int his[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+              const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
+              const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
+              float pv[4], dsv[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float e = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
+                pv[u] = (key >= los[u] && key <= his[u]) ? e : 0.f;
+                dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
+              }
+              pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
+              pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
+              pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+              pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+            }
           }
           // bf16 pairs over the half's first 32 columns, already read
           tmem_st16(t_s + 64 * x + 16 * c2, pp);
