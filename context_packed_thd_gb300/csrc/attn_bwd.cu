@@ -286,27 +286,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int c_lo = min(max(lo - kstart, 0), kBlockN);
       const int c_hi = max(min(min(hi, kend) - kstart, kBlockN - 1), -1);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t sv[32], dp[32];
-        tmem_ld32(t_s + 32 * c4, sv);
-        tmem_ld32(t_dp + 32 * c4, dp);
-        tmem_ld_wait(sv);
-        tmem_ld_wait(dp);
-        uint32_t pk[16];
+      for (int c2 = 0; c2 < 2; ++c2) {  // 64 columns per load round trip
+        uint32_t sv[64], dp[64];
+        tmem_ld64(t_s + 64 * c2, sv);
+        tmem_ld64(t_dp + 64 * c2, dp);
+        tmem_ld_wait64(sv);
+        tmem_ld_wait64(dp);
+        uint32_t pk[32];
         if (full) {
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
+          for (int q = 0; q < 32; ++q) {
             const float e0 = ex2(fmaf(__uint_as_float(sv[2 * q]), sl2, -lse2));
             const float e1 = ex2(fmaf(__uint_as_float(sv[2 * q + 1]), sl2, -lse2));
             pk[q] = pack_bf16x2(e0 * (__uint_as_float(dp[2 * q]) - drow), e1 * (__uint_as_float(dp[2 * q + 1]) - drow));
           }
         } else {
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
+          for (int q = 0; q < 32; ++q) {
             float ds2[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const int col = 32 * c4 + 2 * q + u;
+              const int col = 64 * c2 + 2 * q + u;
               const float e = ex2(fmaf(__uint_as_float(sv[2 * q + u]), sl2, -lse2));
               const float pv = (col >= c_lo && col <= c_hi) ? e : 0.f;
               ds2[u] = pv * (__uint_as_float(dp[2 * q + u]) - drow);
@@ -314,7 +314,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pk[q] = pack_bf16x2(ds2[0], ds2[1]);
           }
         }
-        tmem_st16(t_s + 16 * c4, pk);  // dS over S columns already read
+        // dS over the first 64 S columns: columns 32 c2 .. 32 c2 + 31 hold
+        // S values already read (this slab's or the previous one's)
+        tmem_st32(t_s + 32 * c2, pk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -555,65 +557,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int x = 0; x < 2; ++x) {
         if (!warp_wait(&sdp_full[x], i & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after_sync();
+        // the whole half at once: one load round trip, 64 independent columns
+        uint32_t sv[64], dp[64];
+        tmem_ld64(t_s + 64 * x, sv);
+        tmem_ld64(t_dp + 64 * x, dp);
+        tmem_ld_wait64(sv);
+        tmem_ld_wait64(dp);
+        uint32_t pp[32], pd[32];
+        if (item_full) {
+          // no mask: every real query of the tile sees every key of the
+          // tile, and rows without keys have lse2 = +inf (p = 0)
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int cb = 64 * x + 32 * c2;  // first query column of this 32-column slab
-          uint32_t sv[32], dp[32];
-          tmem_ld32(t_s + cb, sv);
-          tmem_ld32(t_dp + cb, dp);
-          tmem_ld_wait(sv);
-          tmem_ld_wait(dp);
-          uint32_t pp[16], pd[16];
-          if (item_full) {
-            // no mask: every real query of the tile sees every key of the
-            // tile, and rows without keys have lse2 = +inf (p = 0)
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const int col = 64 * x + 4 * q4;
+            const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
+            const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
+            const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
+            const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dsv[4];
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const int col = cb + 4 * q4;
-              const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
-              const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
-              const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
-              const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
-              float pv[4], dsv[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                pv[u] = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
-                dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
-              }
-              pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
-              pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
-              pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-              pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+            for (int u = 0; u < 4; ++u) {
+              pv[u] = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
+              dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
             }
-          } else {
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const int col = cb + 4 * q4;
-              const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
-              const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
-              const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
-              const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
-              const int los[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
-              const int his[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
-              const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
-              const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
-              float pv[4], dsv[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float e = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
-                pv[u] = (key >= los[u] && key <= his[u]) ? e : 0.f;
-                dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
-              }
-              pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
-              pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
-              pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-              pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
-            }
+            pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
+            pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
+            pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+            pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
           }
-          // bf16 pairs over the half's first 32 columns, already read
-          tmem_st16(t_s + 64 * x + 16 * c2, pp);
-          tmem_st16(t_dp + 64 * x + 16 * c2, pd);
+        } else {
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const int col = 64 * x + 4 * q4;
+            const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
+            const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
+            const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
+            const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
+            const int los[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
+            const int his[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+            const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
+            const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dsv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float e = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
+              pv[u] = (key >= los[u] && key <= his[u]) ? e : 0.f;
+              dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
+            }
+            pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
+            pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
+            pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+            pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          }
         }
+        // bf16 pairs over the half's first 32 columns, already read
+        tmem_st32(t_s + 64 * x, pp);
+        tmem_st32(t_dp + 64 * x, pd);
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
