@@ -218,7 +218,7 @@ class Strategy:
         # reorder bytes per rank: read + write of every gathered row, plus the index list
         rb = hq * d * 2 + 3 * 8
         self.reorder_bytes = tl * (2 * rb + 4)
-        # launches per rank: partition index 1, one reorder of Q and the three
+        # launches per rank: partition index 1, one gather of Q and the three
         # id tensors 1, attention: row-group metadata 1, group order 1 (only
         # when the attention grid needs more than one wave of CTAs, one per
         # SM), attention 1
@@ -228,6 +228,10 @@ class Strategy:
         self.launches_per_rank = 4 + (1 if items > sms else 0)
 
     def run_prep(self, cp, r):
+        # The rank's index list, then one gather of Q and the three id
+        # tensors. (cp_partition_reorder_multi does both in one launch and is
+        # faster alone, but the step of all ranks back to back runs 2.5%
+        # slower with it on GB300: the two small launches chain better.)
         d = self.dev
         cp.cp_partition_index(self.name, d["cup"], self.T, self.cpsize, r, out=self.idx[r], err=self.err)
         cp.cp_reorder_multi([d["q"], d["ids"], d["labels"], d["pos"]], self.idx[r],
@@ -620,7 +624,7 @@ def run_cuda(args):
             "per_strategy": per_strategy,
             "reorder": {"GB/s": round(reorder_bytes / (prep_total_ms * 1e-3) / 1e9, 2),
                         "bytes_per_step": reorder_bytes,
-                        "note": "partition index + one reorder launch of Q and the int64 ids, timed together per rank"},
+                        "note": "partition index + one gather launch of Q and the int64 ids, timed together per rank"},
             "reorder_activations": act,
             "kv_restore": restore,
             "dcs_one_vs_two_launches": two,

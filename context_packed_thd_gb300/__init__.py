@@ -18,6 +18,7 @@ __all__ = [
     "DUAL_CHUNK_SWAP", "NO_LOAD_BALANCE", "PACKED_MIRRORED", "CpthdError", "LIB_PATH", "lib",
     "cpthd_status_string", "cp_local_tokens", "cp_partition_index", "cp_restore_index", "cp_reorder",
     "cp_reorder_multi",
+    "cp_partition_reorder_multi",
     "thd_causal_attn_workspace_size", "thd_causal_attn_fwd", "thd_causal_attn_fwd_static_scratch",
     "thd_causal_attn_bwd_workspace_size", "thd_causal_attn_bwd",
     "get_batch_on_this_cp_rank", "strategy_code",
@@ -65,6 +66,9 @@ lib.cp_reorder.restype = _i32
 lib.cp_reorder_multi.argtypes = [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_i64), _i64, _vp,
                                  _i64, _vp, _vp]
 lib.cp_reorder_multi.restype = _i32
+lib.cp_partition_reorder_multi.argtypes = [_i32, _vp, _i32, _i64, _i32, _i32, _i32, ctypes.POINTER(_vp),
+                                           ctypes.POINTER(_vp), ctypes.POINTER(_i64), _vp, _vp, _vp]
+lib.cp_partition_reorder_multi.restype = _i32
 lib.thd_causal_attn_workspace_size.argtypes = [_i64, _i32, _i32, _i32, ctypes.POINTER(_sz)]
 lib.thd_causal_attn_workspace_size.restype = _i32
 lib.thd_causal_attn_fwd.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _f32, _vp,
@@ -189,6 +193,32 @@ def cp_reorder_multi(srcs: Sequence[torch.Tensor], idx: torch.Tensor, outs=None,
     _check(lib.cp_reorder_multi(n, sp, dp, rb, rows, _ptr(idx), idx.numel(), _ptr(err), _stream(stream)),
            "cp_reorder_multi")
     return outs
+
+
+def cp_partition_reorder_multi(strategy, cu_seqlens_padded: torch.Tensor, T: int, cp_size: int, rank: int,
+                               srcs: Sequence[torch.Tensor], outs=None, idx_out: Optional[torch.Tensor] = None,
+                               err: Optional[torch.Tensor] = None, stream=None):
+    """The rank's partition index and every tensor of ``srcs`` (T rows each)
+    gathered by it, in one launch. Returns (idx int32 [T/cp_size], outs)."""
+    srcs = list(srcs)
+    _need_cuda(cu_seqlens_padded, idx_out, err, *srcs)
+    assert cu_seqlens_padded.dtype == torch.int32 and cu_seqlens_padded.is_contiguous()
+    assert all(s.shape[0] == T and s.is_contiguous() for s in srcs)
+    n_loc = cp_local_tokens(strategy, T, cp_size)
+    if idx_out is None:
+        idx_out = torch.empty(n_loc, dtype=torch.int32, device=cu_seqlens_padded.device)
+    assert idx_out.numel() >= n_loc and idx_out.dtype == torch.int32
+    if outs is None:
+        outs = [torch.empty((n_loc,) + tuple(s.shape[1:]), dtype=s.dtype, device=s.device) for s in srcs]
+    n = len(srcs)
+    sp = (_vp * n)(*[s.data_ptr() for s in srcs])
+    dp = (_vp * n)(*[o.data_ptr() for o in outs])
+    rb = (_i64 * n)(*[int(s[0].numel() * s.element_size()) if s.dim() > 1 else s.element_size() for s in srcs])
+    _check(lib.cp_partition_reorder_multi(strategy_code(strategy), _ptr(cu_seqlens_padded),
+                                          cu_seqlens_padded.numel() - 1, int(T), int(cp_size), int(rank), n, sp, dp,
+                                          rb, _ptr(idx_out), _ptr(err), _stream(stream)),
+           "cp_partition_reorder_multi")
+    return idx_out, outs
 
 
 def thd_causal_attn_workspace_size(t_local: int, Hq: int, Hkv: int, d: int) -> int:

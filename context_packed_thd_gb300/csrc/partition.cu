@@ -13,26 +13,14 @@
 // whole buffer taken as one sequence. The restore index inverts the
 // rank-major concatenation of all ranks' lists, which is what an all-gather
 // of the ranks' K/V slices produces.
-#include "common.cuh"
+#include "partition_math.cuh"
 
 namespace cpthd {
 
-// Offset-table checks shared by both index kernels: cup starts at 0, never
-// decreases and ends at T; under DualChunkSwap every padded length is a
-// multiple of 2*cp_size.
 __device__ __forceinline__ void check_offsets(const int32_t* __restrict__ cup, int num_docs, long long T, int cp,
                                               int dcs, int32_t* err) {
-  for (long long j = blockIdx.x * (long long)blockDim.x + threadIdx.x; j <= num_docs;
-       j += (long long)gridDim.x * blockDim.x) {
-    const int32_t a = cup[j];
-    if (j == 0 && a != 0) record_error(err, CPTHD_ERR_BAD_OFFSETS, 0);
-    if (j == num_docs && a != T) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
-    if (j < num_docs) {
-      const int32_t b = cup[j + 1];
-      if (b < a) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
-      else if (dcs && ((b - a) % (2 * cp)) != 0) record_error(err, CPTHD_ERR_NOT_DIVISIBLE, j);
-    }
-  }
+  check_offsets_range(cup, num_docs, T, cp, dcs, err, blockIdx.x * (long long)blockDim.x + threadIdx.x,
+                      (long long)gridDim.x * blockDim.x);
 }
 
 __global__ void dual_chunk_swap_index_kernel(const int32_t* __restrict__ cup, int num_docs, long long T, int cp,
@@ -46,17 +34,7 @@ __global__ void dual_chunk_swap_index_kernel(const int32_t* __restrict__ cup, in
     int r = rank;
     long long t = o;
     if (rank < 0) { r = static_cast<int>(o / t_local); t = o - (long long)r * t_local; }
-    // local offsets lp[j] = cup[j] / cp; find the document holding local slot t
-    int lo = 0, hi = num_docs;
-    while (hi - lo > 1) {
-      int mid = (lo + hi) >> 1;
-      if (static_cast<long long>(__ldg(cup + mid) / cp) <= t) lo = mid; else hi = mid;
-    }
-    long long start = __ldg(cup + lo);
-    long long chunk = (static_cast<long long>(__ldg(cup + lo + 1)) - start) / (2 * cp);
-    long long u = t - start / cp;
-    long long p = (u < chunk) ? start + r * chunk + u
-                              : start + (2LL * cp - 1 - r) * chunk + (u - chunk);
+    const long long p = dcs_slot(cup, num_docs, cp, r, t);
     idx[o] = static_cast<int32_t>(p);
   }
 }
@@ -69,7 +47,7 @@ __global__ void no_load_balance_index_kernel(const int32_t* __restrict__ cup, in
   check_offsets(cup, num_docs, T, cp, 0, err);
   for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
        o += (long long)gridDim.x * blockDim.x) {
-    long long p = (rank < 0) ? o : rank * t_local + o;
+    const long long p = (rank < 0) ? o : nlb_slot(rank, t_local, o);
     idx[o] = static_cast<int32_t>(p);
   }
 }
@@ -80,13 +58,12 @@ __global__ void packed_mirrored_index_kernel(const int32_t* __restrict__ cup, in
   grid_dependency_wait();
   grid_dependents_launch();
   check_offsets(cup, num_docs, T, cp, 0, err);
-  const long long chunk = T / (2LL * cp);
   for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
        o += (long long)gridDim.x * blockDim.x) {
     int r = rank;
     long long t = o;
     if (rank < 0) { r = static_cast<int>(o / t_local); t = o - (long long)r * t_local; }
-    const long long p = (t < chunk) ? r * chunk + t : (2LL * cp - 1 - r) * chunk + (t - chunk);
+    const long long p = mirrored_slot(T, cp, r, t);
     idx[o] = static_cast<int32_t>(p);
   }
 }

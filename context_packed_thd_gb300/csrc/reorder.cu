@@ -12,9 +12,36 @@
 // the SMs keep enough bytes outstanding to cover HBM latency. Narrow rows
 // (fewer than 32 vectors) use one thread per vector instead. Loads and stores
 // use the streaming cache hints: every byte is touched once.
-#include "common.cuh"
+//
+// The fused form (cp_partition_reorder_multi) takes the source rows from
+// the partition formulas instead of an index list: each row's physical slot
+// is computed where it is gathered, and the blocks of the first tensor also
+// write the rank's index list and check the offset table, so one launch
+// replaces the partition-index launch and the gather.
+#include "partition_math.cuh"
 
 namespace cpthd {
+
+// Source row of each gathered row: a caller's index list, or one rank's
+// partition index computed on the fly.
+struct IndexGen {
+  const int32_t* idx;  // non-null: read the list
+  int strategy;
+  const int32_t* cup;
+  int num_docs;
+  long long T;
+  int cp;
+  int rank;
+  long long t_local;
+  __device__ __forceinline__ int32_t at(long long row) const {
+    if (idx != nullptr) return __ldg(idx + row);
+    long long slot;
+    if (strategy == CPTHD_DUAL_CHUNK_SWAP) slot = dcs_slot(cup, num_docs, cp, rank, row);
+    else if (strategy == CPTHD_NO_LOAD_BALANCE) slot = nlb_slot(rank, t_local, row);
+    else slot = mirrored_slot(T, cp, rank, row);
+    return static_cast<int32_t>(slot);
+  }
+};
 
 struct ReorderTensor {
   const void* src;
@@ -40,11 +67,11 @@ constexpr int kUnroll = 4;
 
 template <typename V>
 __device__ __forceinline__ void gather_wide(const V* __restrict__ src, long long src_rows, long long vpr,
-                                            const int32_t* __restrict__ idx, long long n_rows,
+                                            const IndexGen& ig, long long n_rows,
                                             V* __restrict__ dst, int32_t* err, long long warp,
                                             long long nwarps, int lane) {
   for (long long row = warp; row < n_rows; row += nwarps) {
-    const int32_t s = __ldg(idx + row);
+    const int32_t s = ig.at(row);
     if (s < 0 || s >= src_rows) {
       if (lane == 0) record_error(err, CPTHD_ERR_INDEX_RANGE, row);
       continue;
@@ -65,14 +92,14 @@ __device__ __forceinline__ void gather_wide(const V* __restrict__ src, long long
 
 template <typename V>
 __device__ __forceinline__ void gather_narrow(const V* __restrict__ src, long long src_rows, int vpr,
-                                              const int32_t* __restrict__ idx, long long n_rows,
+                                              const IndexGen& ig, long long n_rows,
                                               V* __restrict__ dst, int32_t* err, long long tid,
                                               long long nthreads) {
   const long long total = n_rows * vpr;
   for (long long v = tid; v < total; v += nthreads) {
     const long long row = (vpr == 1) ? v : v / vpr;
     const int col = static_cast<int>(v - row * vpr);
-    const int32_t s = __ldg(idx + row);
+    const int32_t s = ig.at(row);
     if (s < 0 || s >= src_rows) {
       if (col == 0) record_error(err, CPTHD_ERR_INDEX_RANGE, row);
       continue;
@@ -83,36 +110,45 @@ __device__ __forceinline__ void gather_narrow(const V* __restrict__ src, long lo
 
 template <typename V>
 __device__ __forceinline__ void gather_one(const ReorderTensor& t, long long src_rows,
-                                           const int32_t* idx, long long n_rows, int32_t* err) {
+                                           const IndexGen& ig, long long n_rows, int32_t* err) {
   const long long vpr = t.row_bytes / static_cast<long long>(sizeof(V));
   const V* src = static_cast<const V*>(t.src);
   V* dst = static_cast<V*>(t.dst);
   if (vpr >= 32) {
     const long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-    gather_wide<V>(src, src_rows, vpr, idx, n_rows, dst, err, warp, nwarps, threadIdx.x & 31);
+    gather_wide<V>(src, src_rows, vpr, ig, n_rows, dst, err, warp, nwarps, threadIdx.x & 31);
   } else {
     const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
     const long long nthreads = (long long)gridDim.x * blockDim.x;
-    gather_narrow<V>(src, src_rows, static_cast<int>(vpr), idx, n_rows, dst, err, tid, nthreads);
+    gather_narrow<V>(src, src_rows, static_cast<int>(vpr), ig, n_rows, dst, err, tid, nthreads);
   }
 }
 
-// blockIdx.y selects the tensor of the batch.
-__global__ void __launch_bounds__(256) reorder_kernel(ReorderBatch batch, long long src_rows,
-                                                      const int32_t* __restrict__ idx, long long n_rows,
+// blockIdx.y selects the tensor of the batch. With a computed index, the
+// blocks of blockIdx.y == 0 also write the index list (idx_out) and check
+// the offset table.
+__global__ void __launch_bounds__(256) reorder_kernel(ReorderBatch batch, long long src_rows, IndexGen ig,
+                                                      long long n_rows, int32_t* __restrict__ idx_out,
                                                       int32_t* err) {
   // every block waits, even one with nothing to copy, so that this grid never
   // completes before the kernel it depends on
   grid_dependency_wait();
   grid_dependents_launch();
+  if (ig.idx == nullptr && blockIdx.y == 0) {
+    const long long first = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    check_offsets_range(ig.cup, ig.num_docs, ig.T, ig.cp, ig.strategy == CPTHD_DUAL_CHUNK_SWAP, err, first,
+                        stride);
+    for (long long row = first; row < n_rows; row += stride) idx_out[row] = ig.at(row);
+  }
   const ReorderTensor& t = batch.t[blockIdx.y];
   if (t.row_bytes == 0) return;
   switch (t.vec) {
-    case 16: gather_one<uint4>(t, src_rows, idx, n_rows, err); break;
-    case 8: gather_one<uint2>(t, src_rows, idx, n_rows, err); break;
-    case 4: gather_one<uint32_t>(t, src_rows, idx, n_rows, err); break;
-    default: gather_one<uint8_t>(t, src_rows, idx, n_rows, err); break;
+    case 16: gather_one<uint4>(t, src_rows, ig, n_rows, err); break;
+    case 8: gather_one<uint2>(t, src_rows, ig, n_rows, err); break;
+    case 4: gather_one<uint32_t>(t, src_rows, ig, n_rows, err); break;
+    default: gather_one<uint8_t>(t, src_rows, ig, n_rows, err); break;
   }
 }
 
@@ -125,9 +161,12 @@ static int vector_bytes(const void* src, const void* dst, long long row_bytes) {
   return 1;
 }
 
+// computed = false: ig.idx is the caller's index list (required when there
+// is anything to copy). computed = true: the partition index of ig's rank,
+// written to idx_out.
 static int launch_reorder(int n, const void* const* src, void* const* dst, const int64_t* row_bytes,
-                          int64_t src_rows, const int32_t* idx, int64_t n_rows, int32_t* err,
-                          cudaStream_t s) {
+                          int64_t src_rows, const IndexGen& ig, bool computed, int64_t n_rows, int32_t* idx_out,
+                          int32_t* err, cudaStream_t s) {
   if (n < 1 || n > 8 || src_rows < 0 || n_rows < 0) return CPTHD_ERR_INVALID_ARG;
   if (src_rows > INT32_MAX) return CPTHD_ERR_INVALID_ARG;
   ReorderBatch b{};
@@ -141,11 +180,12 @@ static int launch_reorder(int n, const void* const* src, void* const* dst, const
     b.t[i].vec = vector_bytes(src[i], dst[i], row_bytes[i]);
     max_bytes = row_bytes[i] > max_bytes ? row_bytes[i] : max_bytes;
   }
-  if (n_rows == 0 || max_bytes == 0) return CPTHD_OK;
-  if (idx == nullptr) return CPTHD_ERR_INVALID_ARG;
+  if (n_rows == 0 || (max_bytes == 0 && !computed)) return CPTHD_OK;
+  if (!computed && ig.idx == nullptr) return CPTHD_ERR_INVALID_ARG;
+  if (computed && (ig.idx != nullptr || idx_out == nullptr)) return CPTHD_ERR_INVALID_ARG;
   // a warp per row for wide rows, a thread per vector for narrow rows;
   // capped at 8 resident 256-thread blocks on each of the 152 SMs
-  long long work = 0;
+  long long work = computed ? n_rows : 0;  // the index list is written by one thread per row
   for (int i = 0; i < n; ++i) {
     const long long vpr = b.t[i].row_bytes / b.t[i].vec;
     const long long w = (vpr >= 32) ? n_rows * 32 : n_rows * vpr;
@@ -153,9 +193,15 @@ static int launch_reorder(int n, const void* const* src, void* const* dst, const
   }
   const int grid = grid_for(work, 256, 152 * 8);
   dim3 g(grid, n);
-  CPTHD_TRY_CUDA(launch_pdl(reorder_kernel, g, dim3(256), 0, s, b, static_cast<long long>(src_rows), idx,
-                            static_cast<long long>(n_rows), err));
+  CPTHD_TRY_CUDA(launch_pdl(reorder_kernel, g, dim3(256), 0, s, b, static_cast<long long>(src_rows), ig,
+                            static_cast<long long>(n_rows), idx_out, err));
   return CPTHD_OK;
+}
+
+static IndexGen list_gen(const int32_t* idx) {
+  IndexGen g{};
+  g.idx = idx;
+  return g;
 }
 
 }  // namespace cpthd
@@ -165,8 +211,8 @@ extern "C" int cp_reorder(const void* src_dev, int64_t src_rows, int64_t row_byt
   const void* srcs[1] = {src_dev};
   void* dsts[1] = {dst_dev};
   const int64_t rb[1] = {row_bytes};
-  return cpthd::launch_reorder(1, srcs, dsts, rb, src_rows, idx_dev, n_rows, err_dev,
-                               reinterpret_cast<cudaStream_t>(stream));
+  return cpthd::launch_reorder(1, srcs, dsts, rb, src_rows, cpthd::list_gen(idx_dev), false, n_rows, nullptr,
+                               err_dev, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int cp_reorder_multi(int n_tensors, const void* const* src_dev_host, void* const* dst_dev_host,
@@ -174,6 +220,32 @@ extern "C" int cp_reorder_multi(int n_tensors, const void* const* src_dev_host, 
                                 int64_t n_rows, int32_t* err_dev, cpthd_stream_t stream) {
   if (src_dev_host == nullptr || dst_dev_host == nullptr || row_bytes_host == nullptr)
     return CPTHD_ERR_INVALID_ARG;
-  return cpthd::launch_reorder(n_tensors, src_dev_host, dst_dev_host, row_bytes_host, src_rows, idx_dev,
-                               n_rows, err_dev, reinterpret_cast<cudaStream_t>(stream));
+  return cpthd::launch_reorder(n_tensors, src_dev_host, dst_dev_host, row_bytes_host, src_rows,
+                               cpthd::list_gen(idx_dev), false, n_rows, nullptr, err_dev,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int cp_partition_reorder_multi(int strategy, const int32_t* cu_seqlens_padded_dev, int num_docs,
+                                          int64_t T, int cp_size, int rank, int n_tensors,
+                                          const void* const* src_dev_host, void* const* dst_dev_host,
+                                          const int64_t* row_bytes_host, int32_t* idx_out_dev, int32_t* err_dev,
+                                          cpthd_stream_t stream) {
+  int64_t t_local = 0;
+  const int st = cp_local_tokens(strategy, T, cp_size, &t_local);
+  if (st != CPTHD_OK) return st;
+  if (rank < 0 || rank >= cp_size || num_docs < 0 || T > INT32_MAX) return CPTHD_ERR_INVALID_ARG;
+  if (src_dev_host == nullptr || dst_dev_host == nullptr || row_bytes_host == nullptr) return CPTHD_ERR_INVALID_ARG;
+  if (t_local > 0 && (cu_seqlens_padded_dev == nullptr || num_docs == 0 || idx_out_dev == nullptr))
+    return CPTHD_ERR_INVALID_ARG;
+  cpthd::IndexGen g{};
+  g.idx = nullptr;
+  g.strategy = strategy;
+  g.cup = cu_seqlens_padded_dev;
+  g.num_docs = num_docs;
+  g.T = T;
+  g.cp = cp_size;
+  g.rank = rank;
+  g.t_local = t_local;
+  return cpthd::launch_reorder(n_tensors, src_dev_host, dst_dev_host, row_bytes_host, T, g, true, t_local,
+                               idx_out_dev, err_dev, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -142,6 +142,28 @@ CPTHD_API int cp_reorder_multi(int n_tensors, const void* const* src_dev_host, v
                      const int64_t* row_bytes_host, int64_t src_rows, const int32_t* idx_dev,
                      int64_t n_rows, int32_t* err_dev, cpthd_stream_t stream);
 
+/* Partition and gather in one launch: the index list of `rank` under
+ * `strategy` (as cp_partition_index computes it, written to idx_out_dev),
+ * and every tensor of the batch gathered by it (as cp_reorder_multi), with
+ * each row's physical slot computed where the row is copied. One launch
+ * replaces the partition-index launch and the gather that a rank's slicing
+ * (TE PR "How to use": get_batch_on_this_cp_rank over input_ids, labels,
+ * position_ids) otherwise takes; results are identical to the two calls.
+ * The tensors have T rows each (the physical buffer); rank must be in
+ * [0, cp_size).
+ * cu_seqlens_padded_dev: int32 [num_docs+1] device; idx_out_dev: int32
+ * [T/cp_size] device, caller-allocated; src_dev_host / dst_dev_host /
+ * row_bytes_host: host arrays of n_tensors (1..8) device pointers and row
+ * widths, dst [T/cp_size, row_bytes].
+ * Host checks: as cp_local_tokens, rank range, null pointers.
+ * Device checks (err_dev): as cp_partition_index, and INDEX_RANGE for a
+ * computed slot outside [0, T) (only with malformed offsets). */
+CPTHD_API int cp_partition_reorder_multi(int strategy, const int32_t* cu_seqlens_padded_dev, int num_docs,
+                                         int64_t T, int cp_size, int rank, int n_tensors,
+                                         const void* const* src_dev_host, void* const* dst_dev_host,
+                                         const int64_t* row_bytes_host, int32_t* idx_out_dev, int32_t* err_dev,
+                                         cpthd_stream_t stream);
+
 /* Device workspace thd_causal_attn_fwd needs for a slice of t_local rows
  * (per-row key bounds, per-tile key intervals and the tile schedule).
  * Host only. */

@@ -73,6 +73,14 @@ def test_host_validation_launches_nothing(cp):
     assert L.cp_partition_index(1, ctypes.c_void_p(16), 1, 9, 2, 0, ctypes.c_void_p(16), None, None) == -2
     # reorder: too many tensors, negative rows
     assert L.cp_reorder(ctypes.c_void_p(16), -1, 16, ctypes.c_void_p(16), 4, ctypes.c_void_p(16), None, None) == -1
+    # fused partition + gather: rank out of range, NLB with T % cp != 0, missing index output
+    vp = ctypes.c_void_p
+    srcs = (vp * 1)(vp(16)); dsts = (vp * 1)(vp(16)); rb = (ctypes.c_int64 * 1)(16)
+    pr = L.cp_partition_reorder_multi
+    assert pr(0, vp(16), 1, 8, 2, 2, 1, srcs, dsts, rb, vp(16), None, None) == -1
+    assert pr(1, vp(16), 1, 9, 2, 0, 1, srcs, dsts, rb, vp(16), None, None) == -2
+    assert pr(1, vp(16), 1, 8, 2, 0, 1, srcs, dsts, rb, None, None, None) == -1
+    assert pr(0, None, 1, 8, 2, 0, 1, srcs, dsts, rb, vp(16), None, None) == -1
     # attention: unsupported head dim, GQA mismatch, missing workspace
     f = L.thd_causal_attn_fwd
     p = ctypes.c_void_p(256)

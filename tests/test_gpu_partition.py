@@ -138,3 +138,59 @@ def test_many_documents(n_docs):
             ref = np.asarray(P.restore_index(s, lay.cu_seqlens_padded.tolist(), cpsize), dtype=np.int32)
             assert np.array_equal(got, ref), (s, cpsize)
         assert err.cpu().tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("cfg", W.CONFIGS, ids=lambda c: c.name)
+def test_fused_partition_reorder_every_config(cfg):
+    """cp_partition_reorder_multi: the index list equals the oracle's and the
+    gathered Q / ids equal the oracle's byte gather, bit exact, for every
+    strategy and rank (the packed mirrored split where T allows it)."""
+    from oracle import reorder as R
+    dev = cuda_or_skip(); cp = load_lib()
+    strategies = list(cfg.strategies) + ([] if "mirrored" in cfg.strategies else ["mirrored"])
+    for s in strategies:
+        lay = W.layout_for(cfg, s)
+        if s == "mirrored" and lay.T % (2 * cfg.cp):
+            continue
+        inp = W.make_attn_inputs(cfg, s)
+        ids = torch.arange(lay.T, dtype=torch.int64) * 7 + 3
+        cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
+        q = inp.q.to(dev)
+        idv = ids.to(dev)
+        err = new_err(dev)
+        for r in range(cfg.cp):
+            idx, (q_loc, ids_loc) = cp.cp_partition_reorder_multi(s, cup, lay.T, cfg.cp, r, [q, idv], err=err)
+            ref_idx = np.asarray(P.partition_index(s, lay.cu_seqlens_padded.tolist(), cfg.cp, r), dtype=np.int32)
+            assert np.array_equal(idx.cpu().numpy(), ref_idx), (s, r)
+            assert q_loc.cpu().view(torch.int16).numpy().tobytes() == \
+                R.reorder(inp.q.view(torch.int16).numpy().reshape(lay.T, -1), ref_idx).tobytes(), (s, r)
+            assert np.array_equal(ids_loc.cpu().numpy(), ids.numpy()[ref_idx]), (s, r)
+        assert err.cpu().tolist() == [0, 0]
+
+
+def test_fused_partition_reorder_random_packs_and_checks():
+    """Random packs with empty documents (bit exact against the separate
+    calls), and the device check of non-divisible DualChunkSwap lengths."""
+    dev = cuda_or_skip(); cp = load_lib()
+    rng = np.random.default_rng(11)
+    for cpsize in (1, 2, 3, 5):
+        for _ in range(4):
+            lay = W.random_layout(rng, int(rng.integers(1, 60)), 300, 2 * cpsize, allow_empty=True)
+            if lay.T == 0:
+                continue
+            cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
+            x = torch.from_numpy(rng.integers(0, 1 << 30, size=(lay.T, 3), dtype=np.int32)).to(dev)
+            for s in ("dcs", "nlb"):
+                if lay.T % cpsize:
+                    continue
+                for r in range(cpsize):
+                    idx, (got,) = cp.cp_partition_reorder_multi(s, cup, lay.T, cpsize, r, [x])
+                    ref = cp.cp_partition_index(s, cup, lay.T, cpsize, r)
+                    assert torch.equal(idx, ref)
+                    assert torch.equal(got, x[ref.long()])
+    # document 1 has padded length 6, not divisible by 2*cp_size = 4
+    cup = torch.tensor([0, 8, 14, 16], dtype=torch.int32, device=dev)
+    x = torch.zeros((16, 4), dtype=torch.int32, device=dev)
+    err = new_err(dev)
+    cp.cp_partition_reorder_multi("dcs", cup, 16, 2, 0, [x], err=err)
+    assert err.cpu().tolist()[0] == -2
