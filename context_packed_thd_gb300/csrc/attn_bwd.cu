@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && n_items > 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN / 2, 0, 0);  // 128 keys x 64 queries
+      constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, D, 0, 1);
       uint32_t k_lo, k_hi, v_lo, v_hi, q_lo, q_hi, do_lo, do_hi, qmn_lo, qmn_hi, domn_lo, domn_hi;
       umma_desc_words(smem_desc_sw128(smem_u32(sK), 16, 1024), k_lo, k_hi);
@@ -479,56 +479,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       umma_desc_words(smem_desc_sw128(smem_u32(sDO), 16, 1024), do_lo, do_hi);
       umma_desc_words(smem_desc_sw128(smem_u32(sQ), L::kChunk, 1024), qmn_lo, qmn_hi);
       umma_desc_words(smem_desc_sw128(smem_u32(sDO), L::kChunk, 1024), domn_lo, domn_hi);
-      // S^T_x = K Q_x^T and dP^T_x = V dO_x^T for query half x (rows 64x..64x+63
-      // of the stage's Q / dO tile: 64 rows of 128 bytes further in each panel)
-      auto issue_sdp = [&](int i, int x) {
-        const uint32_t so = ((i & 1) * L::kTile + x * 64 * 128) >> 4;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
-          umma_ss_w(tmem + 64 * x, k_lo + off, k_hi, q_lo + so + off, q_hi, kIdS, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
-          umma_ss_w(tmem + 128 + 64 * x, v_lo + off, v_hi, do_lo + so + off, do_hi, kIdS, kk > 0);
-        }
-      };
-      // dV += P^T_x dO_x and dK += dS^T_x Q_x over the half's 64 queries
-      auto issue_dkdv = [&](int i, int x) {
+      auto issue_s = [&](int i) {  // S^T = K Q^T into [0, 128)
         const uint32_t so = ((i & 1) * L::kTile) >> 4;
 #pragma unroll
-        for (int kk = 4 * x; kk < 4 * x + 4; ++kk)
-          umma_ts_w(tmem + 256, tmem + 64 * x + (kk - 4 * x) * 8, domn_lo + so + ((kk * 16 * 128) >> 4), domn_hi,
-                    kIdO, (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+          umma_ss_w(tmem, k_lo + off, k_hi, q_lo + so + off, q_hi, kIdS, kk > 0);
+        }
+      };
+      auto issue_dp = [&](int i) {  // dP^T = V dO^T into [128, 256)
+        const uint32_t so = ((i & 1) * L::kTile) >> 4;
 #pragma unroll
-        for (int kk = 4 * x; kk < 4 * x + 4; ++kk)
-          umma_ts_w(tmem + 256 + D, tmem + 128 + 64 * x + (kk - 4 * x) * 8, qmn_lo + so + ((kk * 16 * 128) >> 4),
-                    qmn_hi, kIdO, (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
+          umma_ss_w(tmem + 128, v_lo + off, v_hi, do_lo + so + off, do_hi, kIdS, kk > 0);
+        }
+      };
+      auto issue_dv = [&](int i) {  // dV += P^T dO, P^T (bf16) in [0, 64)
+        const uint32_t so = ((i & 1) * L::kTile) >> 4;
+#pragma unroll
+        for (int kk = 0; kk < kBlockM / 16; ++kk)
+          umma_ts_w(tmem + 256, tmem + kk * 8, domn_lo + so + ((kk * 16 * 128) >> 4), domn_hi, kIdO,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+      };
+      auto issue_dk = [&](int i) {  // dK += dS^T Q, dS^T (bf16) in [128, 192)
+        const uint32_t so = ((i & 1) * L::kTile) >> 4;
+#pragma unroll
+        for (int kk = 0; kk < kBlockM / 16; ++kk)
+          umma_ts_w(tmem + 256 + D, tmem + 128 + kk * 8, qmn_lo + so + ((kk * 16 * 128) >> 4), qmn_hi, kIdO,
+                    (i > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(&kv_full, 0, &abort_flag) && mbar_wait(&qdo_full[0], 0, &abort_flag);
       if (ok) {
         tc_fence_after_sync();
-        issue_sdp(0, 0);
+        issue_s(0);
         umma_commit(&sdp_full[0]);
-        issue_sdp(0, 1);
+        issue_dp(0);
         umma_commit(&sdp_full[1]);
       }
       for (int i = 0; ok && i < n_items; ++i) {
         const bool more = (i + 1 < n_items);
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          // P^T_x(i) and dS^T_x(i) are in TMEM
-          if (!mbar_wait(&pds_full[x], i & 1, &abort_flag)) { ok = false; break; }
+        // phase 1 of item i done: P^T(i) in [0, 64)
+        if (!mbar_wait(&pds_full[0], i & 1, &abort_flag)) break;
+        tc_fence_after_sync();
+        issue_dv(i);
+        if (more) {  // S^T(i+1) overwrites [0, 128) only after dV(i) (issue order)
+          if (!mbar_wait(&qdo_full[(i + 1) & 1], ((i + 1) >> 1) & 1, &abort_flag)) break;
           tc_fence_after_sync();
-          issue_dkdv(i, x);
-          if (x == 1) umma_commit(&qdo_empty[i & 1]);  // Q(i), dO(i) and their column data are free
-          if (more) {
-            if (x == 0 && !mbar_wait(&qdo_full[(i + 1) & 1], ((i + 1) >> 1) & 1, &abort_flag)) { ok = false; break; }
-            tc_fence_after_sync();
-            issue_sdp(i + 1, x);  // overwrites half x only after its dV / dK MMAs (issue order)
-            umma_commit(&sdp_full[x]);
-          }
+          issue_s(i + 1);
+          umma_commit(&sdp_full[0]);
+        }
+        // phase 2 of item i done: dS^T(i) in [128, 192)
+        if (!mbar_wait(&pds_full[1], i & 1, &abort_flag)) break;
+        tc_fence_after_sync();
+        issue_dk(i);
+        umma_commit(&qdo_empty[i & 1]);  // Q(i), dO(i) and their column data are free
+        if (more) {  // dP^T(i+1) overwrites [128, 256) only after dK(i)
+          issue_dp(i + 1);
+          umma_commit(&sdp_full[1]);
         }
       }
       umma_commit(&kv_final);
@@ -536,6 +544,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_wait_drain(&drain, 0);
     }
   } else {
+    // Elementwise, one thread per key (TMEM lane), in two phases per item:
+    // phase 1 turns S^T into P^T (bf16, over the first 64 columns of S^T) and
+    // keeps P as bf16 pairs in registers; phase 2 turns dP^T into
+    // dS^T = P (dP^T - D) (bf16, over the first 64 columns of dP^T). The
+    // issuer runs dV(i) and S^T(i+1) during phase 2, and dK(i) and
+    // dP^T(i+1) during the next phase 1.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int key = K0 + r;
@@ -553,71 +567,71 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* c_l2 = reinterpret_cast<const float*>(c_lo + 2 * kBlockM);
       const float* c_d = c_l2 + kBlockM;
       const bool item_full = sFull[i / group] != 0;
+      uint32_t pp[64];  // P of the 128 queries, bf16 pairs
+      // ---- phase 1: P = 2^(S scale log2(e) - lse2), masked
+      if (!warp_wait(&sdp_full[0], i & 1, &abort_flag)) { ok = false; break; }
+      tc_fence_after_sync();
 #pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (!warp_wait(&sdp_full[x], i & 1, &abort_flag)) { ok = false; break; }
-        tc_fence_after_sync();
-        // the whole half at once: one load round trip, 64 independent columns
-        uint32_t sv[64], dp[64];
-        tmem_ld64(t_s + 64 * x, sv);
-        tmem_ld64(t_dp + 64 * x, dp);
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t sv[64];
+        tmem_ld64(t_s + 64 * c2, sv);
         tmem_ld_wait64(sv);
-        tmem_ld_wait64(dp);
-        uint32_t pp[32], pd[32];
-        if (item_full) {
-          // no mask: every real query of the tile sees every key of the
-          // tile, and rows without keys have lse2 = +inf (p = 0)
 #pragma unroll
-          for (int q4 = 0; q4 < 16; ++q4) {
-            const int col = 64 * x + 4 * q4;
-            const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
-            const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
-            const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
-            const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dsv[4];
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const int col = 64 * c2 + 4 * q4;
+          const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
+          const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
+          float pv[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              pv[u] = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
-              dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
-            }
-            pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
-            pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
-            pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-            pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
-          }
-        } else {
-#pragma unroll
-          for (int q4 = 0; q4 < 16; ++q4) {
-            const int col = 64 * x + 4 * q4;
+          for (int u = 0; u < 4; ++u) pv[u] = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
+          if (!item_full) {
             const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
             const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
-            const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
-            const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
             const int los[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
             const int his[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
-            const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
-            const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dsv[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float e = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
-              pv[u] = (key >= los[u] && key <= his[u]) ? e : 0.f;
-              dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
-            }
-            pp[2 * q4] = pack_bf16x2(pv[0], pv[1]);
-            pp[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
-            pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-            pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+            for (int u = 0; u < 4; ++u) pv[u] = (key >= los[u] && key <= his[u]) ? pv[u] : 0.f;
           }
+          pp[32 * c2 + 2 * q4] = pack_bf16x2(pv[0], pv[1]);
+          pp[32 * c2 + 2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
         }
-        // bf16 pairs over the half's first 32 columns, already read
-        tmem_st32(t_s + 64 * x, pp);
-        tmem_st32(t_dp + 64 * x, pd);
-        tmem_st_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pds_full[x]);
+        // P^T of these 64 queries over columns 32 c2 .. 32 c2 + 31, already read
+        uint32_t (&half)[32] = *reinterpret_cast<uint32_t(*)[32]>(pp + 32 * c2);
+        tmem_st32(t_s + 32 * c2, half);
       }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pds_full[0]);
+      // ---- phase 2: dS = P (dP - D)
+      if (!warp_wait(&sdp_full[1], i & 1, &abort_flag)) { ok = false; break; }
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t dp[64];
+        tmem_ld64(t_dp + 64 * c2, dp);
+        tmem_ld_wait64(dp);
+        uint32_t pd[32];
+#pragma unroll
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const int col = 64 * c2 + 4 * q4;
+          const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
+          const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
+          const uint32_t w0 = pp[32 * c2 + 2 * q4], w1 = pp[32 * c2 + 2 * q4 + 1];
+          const float pv[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u),
+                               __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u)};
+          float dsv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
+          pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+          pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+        }
+        tmem_st32(t_dp + 32 * c2, pd);  // dS^T over columns already read
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pds_full[1]);
     }
     if (ok && n_items > 0) ok = warp_wait(&kv_final, 0, &abort_flag);
     ok = __all_sync(0xffffffffu, ok);
