@@ -15,12 +15,16 @@
 //  * dQ pass, one CTA per (128-row query tile, query head), walking the
 //    tile's key blocks exactly as the forward does: S = Q K^T and
 //    dP = dO V^T into TMEM, the elementwise warps turn them into dS (bf16,
-//    written back over S), then dQ += dS K with dS read from TMEM.
+//    written back over S), then dQ += dS K with dS read from TMEM. Two S
+//    buffers let S(j+1) and dQ(j) run while the elementwise warps work.
 //  * dK/dV pass, one CTA per (128-key tile, KV head), over every query tile
 //    whose key intervals reach the key tile and every query head of the
 //    group: S^T = K Q^T and dP^T = V dO^T into TMEM, the elementwise warps
-//    write P^T and dS^T (bf16) back over them, then dV += P^T dO and
-//    dK += dS^T Q, both accumulated in TMEM and written once.
+//    write P^T and then dS^T (bf16) back over them in two phases, and
+//    dV += P^T dO and dK += dS^T Q, both accumulated in TMEM and written
+//    once, run during the other phase.
+// Rows without keys get lse2 = +inf in the pre-pass (p = 0 without a mask);
+// blocks and items the query tile's bounds cover fully skip the mask.
 // Warp roles as in the forward: warp 0 TMA producer, warp 1 MMA issuer
 // (owns TMEM), warps 2-5 elementwise (thread = TMEM lane). Every wait is
 // bounded; a timeout drains, frees TMEM and records CPTHD_ERR_TIMEOUT.
