@@ -15,7 +15,9 @@ launching stream. The step's library calls are captured once into a CUDA
 graph and replayed, so host launch overhead does not enter the device time.
 L2 (129 MB) is flushed between timed steps by writing a 256 MB buffer
 outside the timed region. Each (strategy, rank) part is also replayed alone
-to report per-rank attention times and the attention roofline. The
+to report per-rank attention times, and the attention kernel is replayed
+alone (its plan, the row-group metadata, replayed outside the events) for
+the roofline. The
 end-to-end figure adds, every step, the host-to-device copy of all inputs
 from pinned memory and the device-to-host copy of every output and LSE.
 
@@ -184,6 +186,7 @@ class Strategy:
 
     def __init__(self, cp, cfg, strategy, dev):
         self.name = strategy
+        self.cfg = cfg
         inp = W.make_attn_inputs(cfg, strategy)
         lay = inp.layout
         self.lay = lay
@@ -241,6 +244,17 @@ class Strategy:
         d = self.dev
         cp.thd_causal_attn_fwd(self.idx[r], self.q_loc[r], d["k"], d["v"], d["cu"], d["cup"], out=self.out[r],
                                lse=self.lse[r], workspace=self.ws, err=self.err)
+
+    def run_plan(self, cp, r):
+        d = self.dev
+        cp.thd_causal_attn_plan(self.idx[r], self.T, d["cu"], d["cup"], self.cfg.hq, self.cfg.hkv, workspace=self.ws,
+                                err=self.err)
+
+    def run_kernel(self, cp, r):
+        """The attention kernel alone, against the plan run_plan wrote."""
+        d = self.dev
+        cp.thd_causal_attn_fwd_planned(self.q_loc[r], d["k"], d["v"], self.ws, out=self.out[r], lse=self.lse[r],
+                                       err=self.err)
 
     def run_rank(self, cp, r):
         self.run_prep(cp, r)
@@ -457,16 +471,22 @@ def run_cuda(args):
     g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step):
         step()
-    g_prep, g_attn = [], []
+    g_prep, g_attn, g_plan, g_kern = [], [], [], []
     for st in strategies:
         for r in ranks:
-            gp, ga = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            gp, ga, gl, gk = (torch.cuda.CUDAGraph() for _ in range(4))
             with torch.cuda.graph(gp):
                 st.run_prep(cp, r)
             with torch.cuda.graph(ga):
                 st.run_attn(cp, r)
+            with torch.cuda.graph(gl):
+                st.run_plan(cp, r)
+            with torch.cuda.graph(gk):
+                st.run_kernel(cp, r)
             g_prep.append(gp)
             g_attn.append(ga)
+            g_plan.append(gl)
+            g_kern.append(gk)
     torch.cuda.synchronize()
     for _ in range(2):
         g_step.replay()
@@ -552,9 +572,13 @@ def run_cuda(args):
 
     # ---- each part of the step alone (graph replays, L2 flushed before each) --
     reps = 20  # median of 20 replays per (strategy, rank) part
+    # The attention kernel is timed alone for the roofline: the plan (row-
+    # group metadata, group order) is replayed outside the events, then the
+    # planned attention launch between them.
     attn_ms = [[0.0] * reps for _ in range(n_ranks)]
     prep_ms = [[0.0] * reps for _ in range(n_ranks)]
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    kern_ms = [[0.0] * reps for _ in range(n_ranks)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
     for k in range(n_ranks):
         for i in range(reps):
             flush.zero_()
@@ -565,26 +589,36 @@ def run_cuda(args):
             ev[2].record(stream)
             g_attn[k].replay()
             ev[3].record(stream)
+            g_plan[k].replay()
+            flush.zero_()
+            ev[4].record(stream)
+            g_kern[k].replay()
+            ev[5].record(stream)
             torch.cuda.synchronize()
             prep_ms[k][i] = ev[0].elapsed_time(ev[1])
             attn_ms[k][i] = ev[2].elapsed_time(ev[3])
+            kern_ms[k][i] = ev[4].elapsed_time(ev[5])
 
     # per-rank attention times (median over replays) and the dominant-kernel roofline
     med_attn = [statistics.median(x) for x in attn_ms]
+    med_kern = [statistics.median(x) for x in kern_ms]
     med_prep = [statistics.median(x) for x in prep_ms]
     per_strategy = {}
     k = 0
     for st in strategies:
         ms = med_attn[k:k + len(ranks)]
+        kms = med_kern[k:k + len(ranks)]
         fl = [st.flops[r] for r in ranks]
         pr = [st.pairs[r] for r in ranks]
         per_strategy[st.name] = {
             "attn_ms_per_rank_max": round(max(ms), 5), "attn_ms_per_rank_min": round(min(ms), 5),
+            "kernel_ms_per_rank_max": round(max(kms), 5), "kernel_ms_per_rank_min": round(min(kms), 5),
             "attn_tflops": round(sum(fl) / (sum(ms) * 1e-3) / 1e12, 3),
             "pairs_per_rank_max": max(pr), "pairs_per_rank_min": min(pr),
         }
         k += len(ranks)
-    achieved = flops_step / (sum(med_attn) * 1e-3) / 1e12
+    achieved = flops_step / (sum(med_kern) * 1e-3) / 1e12
+    call_tflops = flops_step / (sum(med_attn) * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -633,7 +667,10 @@ def run_cuda(args):
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4),
                          "traffic": measured_traffic(cfg.name, args.strategy is not None or args.rank is not None),
-                         "kernel": "thd_causal_attn_fwd (timed per call: row-group metadata, group order, attention kernel)",
+                         "kernel": "attn_fwd_tc_kernel (thd_causal_attn_fwd_planned, timed per launch; the plan "
+                                   "is replayed outside the events)",
+                         "launch_us_mean": round(sum(med_kern) / len(med_kern) * 1e3, 3),
+                         "whole_call_tflops": round(call_tflops, 3),
                          "peak_source": f"{peak_src} bf16_tflops (burst)"},
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4),

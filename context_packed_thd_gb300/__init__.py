@@ -19,7 +19,8 @@ __all__ = [
     "cpthd_status_string", "cp_local_tokens", "cp_partition_index", "cp_restore_index", "cp_reorder",
     "cp_reorder_multi",
     "cp_partition_reorder_multi",
-    "thd_causal_attn_workspace_size", "thd_causal_attn_fwd", "thd_causal_attn_fwd_static_scratch",
+    "thd_causal_attn_workspace_size", "thd_causal_attn_fwd", "thd_causal_attn_plan", "thd_causal_attn_fwd_planned",
+    "thd_causal_attn_fwd_static_scratch",
     "thd_causal_attn_bwd_workspace_size", "thd_causal_attn_bwd",
     "get_batch_on_this_cp_rank", "strategy_code",
 ]
@@ -74,6 +75,11 @@ lib.thd_causal_attn_workspace_size.restype = _i32
 lib.thd_causal_attn_fwd.argtypes = [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _f32, _vp,
                                     _vp, _vp, _sz, _vp, _vp]
 lib.thd_causal_attn_fwd.restype = _i32
+lib.thd_causal_attn_plan.argtypes = [_vp, _i64, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _sz, _vp, _vp]
+lib.thd_causal_attn_plan.restype = _i32
+lib.thd_causal_attn_fwd_planned.argtypes = [_i64, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _sz,
+                                            _vp, _vp]
+lib.thd_causal_attn_fwd_planned.restype = _i32
 lib.thd_causal_attn_bwd_workspace_size.argtypes = [_i64, _i32, _i32, _i32, ctypes.POINTER(_sz)]
 lib.thd_causal_attn_bwd_workspace_size.restype = _i32
 lib.thd_causal_attn_bwd.argtypes = [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32,
@@ -253,6 +259,47 @@ def thd_causal_attn_fwd(q_slice_idx: torch.Tensor, q: torch.Tensor, k: torch.Ten
                                    float(softmax_scale) if softmax_scale else 0.0, _ptr(out), _ptr(lse),
                                    _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)),
            "thd_causal_attn_fwd")
+    return out, lse
+
+
+def thd_causal_attn_plan(q_slice_idx: torch.Tensor, T: int, cu_seqlens: torch.Tensor,
+                         cu_seqlens_padded: Optional[torch.Tensor], Hq: int, Hkv: int,
+                         workspace: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None, stream=None):
+    """Row-group metadata of a query slice (the first half of
+    thd_causal_attn_fwd). Returns the workspace holding the plan; pass it to
+    thd_causal_attn_fwd_planned for every attention over this slice."""
+    _need_cuda(q_slice_idx, cu_seqlens, cu_seqlens_padded, workspace, err)
+    assert q_slice_idx.dtype == torch.int32
+    t_local = q_slice_idx.numel()
+    if workspace is None:
+        workspace = torch.empty(thd_causal_attn_workspace_size(t_local, Hq, Hkv, 128), dtype=torch.uint8,
+                                device=q_slice_idx.device)
+    _check(lib.thd_causal_attn_plan(_ptr(q_slice_idx), t_local, int(T), _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
+                                    cu_seqlens.numel() - 1, int(Hq), int(Hkv), _ptr(workspace), workspace.numel(),
+                                    _ptr(err), _stream(stream)), "thd_causal_attn_plan")
+    return workspace
+
+
+def thd_causal_attn_fwd_planned(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, workspace: torch.Tensor,
+                                softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                                lse: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None,
+                                stream=None):
+    """The attention kernel alone, against a plan written by
+    thd_causal_attn_plan for the same slice, T, Hq and Hkv. Returns
+    (out bf16 [t_local, Hq, d], lse fp32 [Hq, t_local])."""
+    _need_cuda(q, k, v, workspace, out, lse, err)
+    t_local, Hq, d = q.shape
+    T, Hkv, _ = k.shape
+    for t in (q, k, v):
+        assert t.dtype == torch.bfloat16 and t.is_contiguous()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, t_local), dtype=torch.float32, device=q.device)
+    _check(lib.thd_causal_attn_fwd_planned(t_local, _ptr(q), _ptr(k), _ptr(v), T, Hq, Hkv, d,
+                                           float(softmax_scale) if softmax_scale else 0.0, _ptr(out), _ptr(lse),
+                                           _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)),
+           "thd_causal_attn_fwd_planned")
     return out, lse
 
 

@@ -551,34 +551,42 @@ extern "C" int thd_causal_attn_workspace_size(int64_t t_local, int Hq, int Hkv, 
   return CPTHD_OK;
 }
 
-extern "C" int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_local, const void* q_dev,
-                                   const void* k_dev, const void* v_dev, int64_t T,
-                                   const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_padded_dev,
-                                   int num_docs, int Hq, int Hkv, int d, float softmax_scale, void* out_dev,
-                                   float* lse_dev, void* workspace_dev, size_t workspace_bytes,
-                                   int32_t* err_dev, cpthd_stream_t stream) {
-  using namespace cpthd;
+namespace cpthd {
+
+// Host checks shared by the three entry points.
+static int check_attn_shape(int64_t t_local, int64_t T, int num_docs, int Hq, int Hkv) {
   if (t_local < 0 || T < 0 || T > INT32_MAX || t_local > INT32_MAX || num_docs < 0 || Hq < 1 || Hkv < 1)
     return CPTHD_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return CPTHD_ERR_UNSUPPORTED;
   if (Hq % Hkv != 0 || Hq > 65535) return CPTHD_ERR_UNSUPPORTED;
-  if (t_local == 0) return CPTHD_OK;
-  if (q_slice_idx_dev == nullptr || q_dev == nullptr || k_dev == nullptr || v_dev == nullptr ||
-      cu_seqlens_dev == nullptr || out_dev == nullptr || lse_dev == nullptr || num_docs < 1 || T < 1)
-    return CPTHD_ERR_INVALID_ARG;
-  const uintptr_t align = reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(k_dev) |
-                          reinterpret_cast<uintptr_t>(v_dev) | reinterpret_cast<uintptr_t>(out_dev);
-  if (align & 15) return CPTHD_ERR_UNSUPPORTED;
+  return CPTHD_OK;
+}
+
+static int check_workspace(int64_t t_local, int Hq, int Hkv, const void* workspace_dev, size_t workspace_bytes) {
   const int rows = group_rows_for(Hq, Hkv);
   const long long ngroups = (t_local + rows - 1) / rows;
   if (workspace_dev == nullptr || workspace_bytes < attn_workspace_bytes(ngroups, rows) ||
       (reinterpret_cast<uintptr_t>(workspace_dev) & 255))
     return CPTHD_ERR_WORKSPACE;
+  return CPTHD_OK;
+}
+
+}  // namespace cpthd
+
+extern "C" int thd_causal_attn_plan(const int32_t* q_slice_idx_dev, int64_t t_local, int64_t T,
+                                    const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_padded_dev,
+                                    int num_docs, int Hq, int Hkv, void* workspace_dev, size_t workspace_bytes,
+                                    int32_t* err_dev, cpthd_stream_t stream) {
+  using namespace cpthd;
+  int st = check_attn_shape(t_local, T, num_docs, Hq, Hkv);
+  if (st != CPTHD_OK) return st;
+  if (t_local == 0) return CPTHD_OK;
+  if (q_slice_idx_dev == nullptr || cu_seqlens_dev == nullptr || num_docs < 1 || T < 1) return CPTHD_ERR_INVALID_ARG;
+  st = check_workspace(t_local, Hq, Hkv, workspace_dev, workspace_bytes);
+  if (st != CPTHD_OK) return st;
+  const int rows = group_rows_for(Hq, Hkv);
+  const long long ngroups = (t_local + rows - 1) / rows;
   const int32_t* cup = cu_seqlens_padded_dev ? cu_seqlens_padded_dev : cu_seqlens_dev;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
-  const float scale_log2 = scale * 1.4426950408889634f;
-
   AttnWorkspace ws = carve_workspace(workspace_dev, ngroups, rows);
   if (rows == kBlockM) {
     CPTHD_TRY_CUDA(launch_pdl(attn_group_meta_kernel<kBlockM>, dim3(static_cast<unsigned>(ngroups)), dim3(kBlockM), 0,
@@ -593,13 +601,65 @@ extern "C" int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loc
   // CTA per SM); within a single wave the order makes no difference and the
   // ordering launch is skipped.
   const long long items = ngroups * ((rows == kBlockM) ? Hq / 2 : Hq);
-  const bool ordered = items > sm_count();
-  if (ordered)
+  if (items > sm_count())
     CPTHD_TRY_CUDA(launch_pdl(attn_group_order_kernel, dim3(1), dim3(1024), 0, s, static_cast<int>(ngroups), ws));
+  return CPTHD_OK;
+}
+
+extern "C" int thd_causal_attn_fwd_planned(int64_t t_local, const void* q_dev, const void* k_dev, const void* v_dev,
+                                           int64_t T, int Hq, int Hkv, int d, float softmax_scale, void* out_dev,
+                                           float* lse_dev, const void* workspace_dev, size_t workspace_bytes,
+                                           int32_t* err_dev, cpthd_stream_t stream) {
+  using namespace cpthd;
+  int st = check_attn_shape(t_local, T, 0, Hq, Hkv);
+  if (st != CPTHD_OK) return st;
+  if (d != 64 && d != 128) return CPTHD_ERR_UNSUPPORTED;
+  if (t_local == 0) return CPTHD_OK;
+  if (q_dev == nullptr || k_dev == nullptr || v_dev == nullptr || out_dev == nullptr || lse_dev == nullptr || T < 1)
+    return CPTHD_ERR_INVALID_ARG;
+  const uintptr_t align = reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(k_dev) |
+                          reinterpret_cast<uintptr_t>(v_dev) | reinterpret_cast<uintptr_t>(out_dev);
+  if (align & 15) return CPTHD_ERR_UNSUPPORTED;
+  st = check_workspace(t_local, Hq, Hkv, workspace_dev, workspace_bytes);
+  if (st != CPTHD_OK) return st;
+  const int rows = group_rows_for(Hq, Hkv);
+  const long long ngroups = (t_local + rows - 1) / rows;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
+  const float scale_log2 = scale * 1.4426950408889634f;
+  AttnWorkspace ws = carve_workspace(const_cast<void*>(workspace_dev), ngroups, rows);
+  // the plan launched the group order exactly when the grid exceeds a wave
+  const long long items = ngroups * ((rows == kBlockM) ? Hq / 2 : Hq);
+  const bool ordered = items > sm_count();
   if (d == 128)
     return launch_attn<128>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ngroups, rows, ordered, out_dev,
                             lse_dev, err_dev, s);
   return launch_attn<64>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ngroups, rows, ordered, out_dev,
-                         lse_dev,
-                         err_dev, s);
+                         lse_dev, err_dev, s);
+}
+
+extern "C" int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_local, const void* q_dev,
+                                   const void* k_dev, const void* v_dev, int64_t T,
+                                   const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_padded_dev,
+                                   int num_docs, int Hq, int Hkv, int d, float softmax_scale, void* out_dev,
+                                   float* lse_dev, void* workspace_dev, size_t workspace_bytes,
+                                   int32_t* err_dev, cpthd_stream_t stream) {
+  using namespace cpthd;
+  int st = check_attn_shape(t_local, T, num_docs, Hq, Hkv);
+  if (st != CPTHD_OK) return st;
+  if (d != 64 && d != 128) return CPTHD_ERR_UNSUPPORTED;
+  if (t_local == 0) return CPTHD_OK;
+  if (q_slice_idx_dev == nullptr || q_dev == nullptr || k_dev == nullptr || v_dev == nullptr ||
+      cu_seqlens_dev == nullptr || out_dev == nullptr || lse_dev == nullptr || num_docs < 1 || T < 1)
+    return CPTHD_ERR_INVALID_ARG;
+  const uintptr_t align = reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(k_dev) |
+                          reinterpret_cast<uintptr_t>(v_dev) | reinterpret_cast<uintptr_t>(out_dev);
+  if (align & 15) return CPTHD_ERR_UNSUPPORTED;
+  st = check_workspace(t_local, Hq, Hkv, workspace_dev, workspace_bytes);
+  if (st != CPTHD_OK) return st;
+  st = thd_causal_attn_plan(q_slice_idx_dev, t_local, T, cu_seqlens_dev, cu_seqlens_padded_dev, num_docs, Hq, Hkv,
+                            workspace_dev, workspace_bytes, err_dev, stream);
+  if (st != CPTHD_OK) return st;
+  return thd_causal_attn_fwd_planned(t_local, q_dev, k_dev, v_dev, T, Hq, Hkv, d, softmax_scale, out_dev, lse_dev,
+                                     workspace_dev, workspace_bytes, err_dev, stream);
 }

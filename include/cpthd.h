@@ -197,6 +197,25 @@ CPTHD_API int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loca
                         float* lse_dev, void* workspace_dev, size_t workspace_bytes,
                         int32_t* err_dev, cpthd_stream_t stream);
 
+/* The forward in two parts, for callers that run several attentions over
+ * the same slice (every layer of a model step shares q_slice_idx and the
+ * offsets): thd_causal_attn_plan writes the row-group metadata (per-row key
+ * bounds, per-group key intervals, the group order) into the workspace once;
+ * thd_causal_attn_fwd_planned runs the attention kernel against it as often
+ * as needed. thd_causal_attn_fwd is the two in sequence. The planned call
+ * must get the same t_local, T, Hq, Hkv and the workspace the plan wrote
+ * (caller's contract; the workspace is read only); q, k, v, d and the scale
+ * may differ between planned calls.
+ * Arguments, layouts, errors: as thd_causal_attn_fwd. */
+CPTHD_API int thd_causal_attn_plan(const int32_t* q_slice_idx_dev, int64_t t_local, int64_t T,
+                                   const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_padded_dev, int num_docs,
+                                   int Hq, int Hkv, void* workspace_dev, size_t workspace_bytes, int32_t* err_dev,
+                                   cpthd_stream_t stream);
+CPTHD_API int thd_causal_attn_fwd_planned(int64_t t_local, const void* q_dev, const void* k_dev, const void* v_dev,
+                                          int64_t T, int Hq, int Hkv, int d, float softmax_scale, void* out_dev,
+                                          float* lse_dev, const void* workspace_dev, size_t workspace_bytes,
+                                          int32_t* err_dev, cpthd_stream_t stream);
+
 /* Device workspace thd_causal_attn_bwd needs (per-row key bounds, per-tile key
  * intervals, lse * log2(e) and rowsum(dO * O) per row and query head). Host only. */
 CPTHD_API int thd_causal_attn_bwd_workspace_size(int64_t t_local, int Hq, int Hkv, int d, size_t* bytes_host);

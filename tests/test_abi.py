@@ -87,6 +87,19 @@ def test_host_validation_launches_nothing(cp):
     assert f(p, 4, p, p, p, 8, p, None, 1, 2, 2, 96, 0.0, p, p, p, 1 << 20, None, None) == -3
     assert f(p, 4, p, p, p, 8, p, None, 1, 3, 2, 64, 0.0, p, p, p, 1 << 20, None, None) == -3
     assert f(p, 4, p, p, p, 8, p, None, 1, 2, 2, 64, 0.0, p, p, None, 0, None, None) == -4
+    # plan / planned run: same host checks as the one-call forward
+    pl = L.thd_causal_attn_plan
+    assert pl(p, 4, 8, p, None, 1, 3, 2, p, 1 << 20, None, None) == -3        # GQA mismatch
+    assert pl(p, 4, 8, p, None, 1, 2, 2, None, 0, None, None) == -4           # missing workspace
+    assert pl(p, 4, 8, None, None, 1, 2, 2, p, 1 << 20, None, None) == -1     # missing offsets
+    assert pl(p, 4, 8, p, None, 1, 2, 2, vp(260), 1 << 20, None, None) == -4  # workspace not 256-B aligned
+    assert pl(None, 0, 8, None, None, 1, 2, 2, None, 0, None, None) == 0
+    fp = L.thd_causal_attn_fwd_planned
+    assert fp(4, p, p, p, 8, 2, 2, 96, 0.0, p, p, p, 1 << 20, None, None) == -3
+    assert fp(4, p, p, p, 8, 2, 2, 64, 0.0, p, p, None, 0, None, None) == -4
+    assert fp(4, vp(264), p, p, 8, 2, 2, 64, 0.0, p, p, p, 1 << 20, None, None) == -3  # q not 16-B aligned
+    assert fp(4, p, None, p, 8, 2, 2, 64, 0.0, p, p, p, 1 << 20, None, None) == -1
+    assert fp(0, None, None, None, 8, 2, 2, 64, 0.0, None, None, None, 0, None, None) == 0
     # empty slice: nothing to do
     assert f(None, 0, None, None, None, 8, None, None, 1, 2, 2, 64, 0.0, None, None, None, 0, None, None) == 0
 

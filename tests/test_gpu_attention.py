@@ -184,6 +184,32 @@ def test_custom_scale_and_permuted_rows():
     assert_attn_matches(out, lse, ro, rl, "permuted")
 
 
+@pytest.mark.parametrize("hq,hkv,strategy", [(16, 16, "dcs"), (32, 8, "nlb"), (32, 8, "dcs")])
+def test_plan_once_run_many(hq, hkv, strategy):
+    """One plan serves several attentions over the same slice (as the layers
+    of a step do): each planned run is bit-identical to the one-call forward
+    on the same inputs, for both head dims and for grids of one wave (MHA,
+    2048 rows) and of several waves (GQA 32/8, ordered groups)."""
+    dev = cuda_or_skip(); cp = load_lib()
+    lengths = [2500, 700, 1800, 1, 3191]          # 8192 tokens, 8208 once padded to multiples of 2 * cp_size
+    cpsize = 4
+    runs = []
+    for dd, seed in ((128, 11), (64, 12), (128, 13)):
+        inp = _custom(lengths, 2 * cpsize, hq, hkv, dd, seed)
+        runs.append(DevInputs(inp, dev))
+    lay = runs[0].inp.layout
+    for r in range(cpsize):
+        err = new_err(dev)
+        idx = cp.cp_partition_index(strategy, runs[0].cup, lay.T, cpsize, r, err=err)
+        ws = cp.thd_causal_attn_plan(idx, lay.T, runs[0].cu, runs[0].cup, hq, hkv, err=err)
+        for d in runs:
+            q_loc = cp.cp_reorder(d.q, idx, err=err)
+            o1, l1 = cp.thd_causal_attn_fwd_planned(q_loc, d.k, d.v, ws, err=err)
+            o2, l2 = cp.thd_causal_attn_fwd(idx, q_loc, d.k, d.v, d.cu, d.cup, err=err)
+            assert torch.equal(o1, o2) and torch.equal(l1, l2), (strategy, r, d.q.shape)
+        assert err.cpu().tolist() == [0, 0]
+
+
 def test_both_layouts_agree_per_token():
     """Matched inputs: the DualChunkSwap (padded) and NO_LOAD_BALANCE
     (unpadded) runs give each real token the same result within tolerance."""
