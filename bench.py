@@ -5,8 +5,9 @@ over packed THD (libcpthd on one GB300).
 One *step* runs the whole path for one packed workload: for every strategy
 the workload names and every context-parallel rank (sequentially, on one
 GPU): partition index -> reorder of the Q slice and of the int64
-input_ids / labels / position_ids -> causal THD attention forward (tile
-metadata + attention kernel).
+input_ids / labels / position_ids, with the attention plan (row-group
+metadata) beside it on a side stream -> the planned causal THD attention
+kernel.
 
 The headline metric is attention TFLOPS over unmasked pairs only
 (4 * d * pairs * Hq per step, pairs counted from the rank's index list)
@@ -210,6 +211,7 @@ class Strategy:
         self.lse = [torch.empty((hq, tl), dtype=torch.float32, device=dev) for _ in range(cfg.cp)]
         self.ws = torch.empty(cp.thd_causal_attn_workspace_size(tl, hq, cfg.hkv, d), dtype=torch.uint8, device=dev)
         self.err = torch.zeros(2, dtype=torch.int32, device=dev)
+        self.side = torch.cuda.Stream(device=dev)
         self.out_host = [torch.empty_like(o, device="cpu").pin_memory() for o in self.out]
         self.lse_host = [torch.empty_like(x, device="cpu").pin_memory() for x in self.lse]
         # algorithmic work, from the index lists the library itself returns
@@ -257,8 +259,20 @@ class Strategy:
                                        err=self.err)
 
     def run_rank(self, cp, r):
-        self.run_prep(cp, r)
-        self.run_attn(cp, r)
+        """One rank slice as a caller would run it: the plan (row-group
+        metadata) needs only the partition index, so it runs on a side
+        stream while the gather runs on the current one, and the attention
+        kernel waits for both."""
+        d = self.dev
+        main = torch.cuda.current_stream()
+        cp.cp_partition_index(self.name, d["cup"], self.T, self.cpsize, r, out=self.idx[r], err=self.err)
+        self.side.wait_stream(main)
+        with torch.cuda.stream(self.side):
+            self.run_plan(cp, r)
+        cp.cp_reorder_multi([d["q"], d["ids"], d["labels"], d["pos"]], self.idx[r],
+                            outs=[self.q_loc[r]] + self.ids_loc[r], err=self.err)
+        main.wait_stream(self.side)
+        self.run_kernel(cp, r)
 
 
 def _graph_ms(fn, flush, reps=5):
