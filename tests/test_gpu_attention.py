@@ -210,6 +210,47 @@ def test_plan_once_run_many(hq, hkv, strategy):
         assert err.cpu().tolist() == [0, 0]
 
 
+def test_plan_on_side_stream_beside_the_gather():
+    """The order a caller overlaps the path in: partition index, then the
+    gather on the current stream and the plan on a side stream (the plan
+    needs only the index), then the planned attention after both; checked
+    against the oracle on every rank of both strategies, with the slices run
+    back to back through one workspace."""
+    dev = cuda_or_skip(); cp = load_lib()
+    cfg = W.CONFIG_BY_NAME["t8192_mha16"]
+    side = torch.cuda.Stream()
+    rng = np.random.default_rng(7)
+    for s in ("dcs", "nlb"):
+        inp = W.make_attn_inputs(cfg, s)
+        d = DevInputs(inp, dev)
+        lay = inp.layout
+        err = new_err(dev)
+        tl = cp.cp_local_tokens(s, lay.T, cfg.cp)
+        ws = torch.empty(cp.thd_causal_attn_workspace_size(tl, cfg.hq, cfg.hkv, cfg.d), dtype=torch.uint8,
+                         device=dev)
+        results = []
+        main = torch.cuda.current_stream()
+        for r in range(cfg.cp):
+            idx = cp.cp_partition_index(s, d.cup, lay.T, cfg.cp, r, err=err)
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                cp.thd_causal_attn_plan(idx, lay.T, d.cu, d.cup, cfg.hq, cfg.hkv, workspace=ws, err=err)
+            q_loc = cp.cp_reorder(d.q, idx, err=err)
+            main.wait_stream(side)
+            out, lse = cp.thd_causal_attn_fwd_planned(q_loc, d.k, d.v, ws, err=err)
+            results.append((idx, out.clone(), lse.clone()))
+        torch.cuda.synchronize()
+        for r, (idx, out, lse) in enumerate(results):
+            ref_idx = np.asarray(P.partition_index(s, lay.cu_seqlens_padded, cfg.cp, r), dtype=np.int64)
+            assert np.array_equal(idx.cpu().numpy(), ref_idx)
+            rows = _sample_rows(lay, ref_idx, cfg.cp, rng)
+            ro, rl = A.attention_fwd(inp.q[torch.from_numpy(ref_idx)], inp.k, inp.v, lay.cu_seqlens,
+                                     lay.cu_seqlens_padded, ref_idx, rows=rows)
+            rows_t = torch.from_numpy(rows).to(dev)
+            assert_attn_matches(out[rows_t], lse[:, rows_t], ro, rl, f"{s}/rank{r}")
+        assert err.cpu().tolist() == [0, 0]
+
+
 def test_both_layouts_agree_per_token():
     """Matched inputs: the DualChunkSwap (padded) and NO_LOAD_BALANCE
     (unpadded) runs give each real token the same result within tolerance."""
