@@ -300,9 +300,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (full) {
 #pragma unroll
           for (int q = 0; q < 32; ++q) {
-            const float e0 = ex2(fmaf(__uint_as_float(sv[2 * q]), sl2, -lse2));
-            const float e1 = ex2(fmaf(__uint_as_float(sv[2 * q + 1]), sl2, -lse2));
-            pk[q] = pack_bf16x2(e0 * (__uint_as_float(dp[2 * q]) - drow), e1 * (__uint_as_float(dp[2 * q + 1]) - drow));
+            // packed pairs: the same roundings as the scalar fma, sub and mul
+            float a0, a1, t0, t1, d0, d1;
+            fma2(a0, a1, __uint_as_float(sv[2 * q]), __uint_as_float(sv[2 * q + 1]), sl2, -lse2);
+            fma2(t0, t1, __uint_as_float(dp[2 * q]), __uint_as_float(dp[2 * q + 1]), 1.f, -drow);
+            mul2(d0, d1, ex2(a0), ex2(a1), t0, t1);
+            pk[q] = pack_bf16x2(d0, d1);
           }
         } else {
 #pragma unroll
@@ -587,7 +590,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
           float pv[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) pv[u] = ex2(fmaf(__uint_as_float(sv[4 * q4 + u]), sl2, -l2s[u]));
+          for (int u = 0; u < 4; u += 2) {
+            float a0, a1;
+            fma2(a0, a1, __uint_as_float(sv[4 * q4 + u]), __uint_as_float(sv[4 * q4 + u + 1]), sl2, -l2s[u],
+                 -l2s[u + 1]);
+            pv[u] = ex2(a0);
+            pv[u + 1] = ex2(a1);
+          }
           if (!item_full) {
             const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
             const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
@@ -626,7 +635,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u)};
           float dsv[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) dsv[u] = pv[u] * (__uint_as_float(dp[4 * q4 + u]) - ds[u]);
+          for (int u = 0; u < 4; u += 2) {
+            float t0, t1;
+            fma2(t0, t1, __uint_as_float(dp[4 * q4 + u]), __uint_as_float(dp[4 * q4 + u + 1]), 1.f, -ds[u],
+                 -ds[u + 1]);
+            mul2(dsv[u], dsv[u + 1], pv[u], pv[u + 1], t0, t1);
+          }
           pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
           pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
