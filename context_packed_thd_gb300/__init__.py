@@ -20,6 +20,7 @@ __all__ = [
     "cp_reorder_multi",
     "cp_partition_reorder_multi",
     "thd_causal_attn_workspace_size", "thd_causal_attn_fwd", "thd_causal_attn_plan", "thd_causal_attn_fwd_planned",
+    "thd_causal_attn_plan_partition",
     "thd_causal_attn_fwd_static_scratch",
     "thd_causal_attn_bwd_workspace_size", "thd_causal_attn_bwd",
     "get_batch_on_this_cp_rank", "strategy_code",
@@ -80,6 +81,9 @@ lib.thd_causal_attn_plan.restype = _i32
 lib.thd_causal_attn_fwd_planned.argtypes = [_i64, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _sz,
                                             _vp, _vp]
 lib.thd_causal_attn_fwd_planned.restype = _i32
+lib.thd_causal_attn_plan_partition.argtypes = [_i32, _i64, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp,
+                                               _vp]
+lib.thd_causal_attn_plan_partition.restype = _i32
 lib.thd_causal_attn_bwd_workspace_size.argtypes = [_i64, _i32, _i32, _i32, ctypes.POINTER(_sz)]
 lib.thd_causal_attn_bwd_workspace_size.restype = _i32
 lib.thd_causal_attn_bwd.argtypes = [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32, _i32, _i32, _i32,
@@ -277,6 +281,26 @@ def thd_causal_attn_plan(q_slice_idx: torch.Tensor, T: int, cu_seqlens: torch.Te
     _check(lib.thd_causal_attn_plan(_ptr(q_slice_idx), t_local, int(T), _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
                                     cu_seqlens.numel() - 1, int(Hq), int(Hkv), _ptr(workspace), workspace.numel(),
                                     _ptr(err), _stream(stream)), "thd_causal_attn_plan")
+    return workspace
+
+
+def thd_causal_attn_plan_partition(strategy, T: int, cu_seqlens: torch.Tensor,
+                                   cu_seqlens_padded: Optional[torch.Tensor], cp_size: int, rank: int, Hq: int,
+                                   Hkv: int, workspace: Optional[torch.Tensor] = None,
+                                   err: Optional[torch.Tensor] = None, stream=None):
+    """The plan of rank ``rank``'s slice under ``strategy`` with the row slots
+    computed from the partition formulas (no index list needed). Returns the
+    workspace, as thd_causal_attn_plan does for the same slice."""
+    _need_cuda(cu_seqlens, cu_seqlens_padded, workspace, err)
+    code = strategy_code(strategy)
+    t_local = cp_local_tokens(code, T, cp_size)
+    if workspace is None:
+        workspace = torch.empty(thd_causal_attn_workspace_size(t_local, Hq, Hkv, 128), dtype=torch.uint8,
+                                device=cu_seqlens.device)
+    _check(lib.thd_causal_attn_plan_partition(code, int(T), _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
+                                              cu_seqlens.numel() - 1, int(cp_size), int(rank), int(Hq), int(Hkv),
+                                              _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)),
+           "thd_causal_attn_plan_partition")
     return workspace
 
 

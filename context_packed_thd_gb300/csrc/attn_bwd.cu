@@ -786,7 +786,7 @@ extern "C" int thd_causal_attn_bwd(const int32_t* q_slice_idx_dev, int64_t t_loc
   float* lse2 = reinterpret_cast<float*>(extra);
   float* dvec = reinterpret_cast<float*>(extra + align256(sizeof(float) * ntiles * kBlockM * Hq));
   attn_group_meta_kernel<kBlockM><<<static_cast<unsigned>(ntiles), kBlockM, 0, s>>>(
-      q_slice_idx_dev, t_local, cu_seqlens_dev, cup, num_docs, T, ws, err_dev);
+      index_list(q_slice_idx_dev), t_local, cu_seqlens_dev, cup, num_docs, T, ws, err_dev);
   CPTHD_TRY_CUDA(cudaGetLastError());
   if (d == 128)
     return launch_bwd<128>(q_dev, k_dev, v_dev, out_dev, dout_dev, lse_dev, t_local, T, Hq, Hkv, scale, ws, lse2,

@@ -572,6 +572,34 @@ static int check_workspace(int64_t t_local, int Hq, int Hkv, const void* workspa
 
 }  // namespace cpthd
 
+namespace cpthd {
+
+// Metadata of the slice's row groups (and, past one wave, their order) into
+// the workspace; shape and workspace already checked.
+static int launch_plan(const IndexGen& slots, long long t_local, long long T, const int32_t* cu,
+                       const int32_t* cup, int num_docs, int Hq, int Hkv, void* workspace, int32_t* err,
+                       cudaStream_t s) {
+  const int rows = group_rows_for(Hq, Hkv);
+  const long long ngroups = (t_local + rows - 1) / rows;
+  AttnWorkspace ws = carve_workspace(workspace, ngroups, rows);
+  if (rows == kBlockM) {
+    CPTHD_TRY_CUDA(launch_pdl(attn_group_meta_kernel<kBlockM>, dim3(static_cast<unsigned>(ngroups)), dim3(kBlockM), 0,
+                              s, slots, t_local, cu, cup, num_docs, T, ws, err));
+  } else {
+    CPTHD_TRY_CUDA(launch_pdl(attn_group_meta_kernel<2 * kBlockM>, dim3(static_cast<unsigned>(ngroups)),
+                              dim3(2 * kBlockM), 0, s, slots, t_local, cu, cup, num_docs, T, ws, err));
+  }
+  // The longest groups go first when the grid needs more than one wave (one
+  // CTA per SM); within a single wave the order makes no difference and the
+  // ordering launch is skipped.
+  const long long items = ngroups * ((rows == kBlockM) ? Hq / 2 : Hq);
+  if (items > sm_count())
+    CPTHD_TRY_CUDA(launch_pdl(attn_group_order_kernel, dim3(1), dim3(1024), 0, s, static_cast<int>(ngroups), ws));
+  return CPTHD_OK;
+}
+
+}  // namespace cpthd
+
 extern "C" int thd_causal_attn_plan(const int32_t* q_slice_idx_dev, int64_t t_local, int64_t T,
                                     const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_padded_dev,
                                     int num_docs, int Hq, int Hkv, void* workspace_dev, size_t workspace_bytes,
@@ -583,27 +611,29 @@ extern "C" int thd_causal_attn_plan(const int32_t* q_slice_idx_dev, int64_t t_lo
   if (q_slice_idx_dev == nullptr || cu_seqlens_dev == nullptr || num_docs < 1 || T < 1) return CPTHD_ERR_INVALID_ARG;
   st = check_workspace(t_local, Hq, Hkv, workspace_dev, workspace_bytes);
   if (st != CPTHD_OK) return st;
-  const int rows = group_rows_for(Hq, Hkv);
-  const long long ngroups = (t_local + rows - 1) / rows;
   const int32_t* cup = cu_seqlens_padded_dev ? cu_seqlens_padded_dev : cu_seqlens_dev;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  AttnWorkspace ws = carve_workspace(workspace_dev, ngroups, rows);
-  if (rows == kBlockM) {
-    CPTHD_TRY_CUDA(launch_pdl(attn_group_meta_kernel<kBlockM>, dim3(static_cast<unsigned>(ngroups)), dim3(kBlockM), 0,
-                              s, q_slice_idx_dev, static_cast<long long>(t_local), cu_seqlens_dev, cup, num_docs,
-                              static_cast<long long>(T), ws, err_dev));
-  } else {
-    CPTHD_TRY_CUDA(launch_pdl(attn_group_meta_kernel<2 * kBlockM>, dim3(static_cast<unsigned>(ngroups)),
-                              dim3(2 * kBlockM), 0, s, q_slice_idx_dev, static_cast<long long>(t_local),
-                              cu_seqlens_dev, cup, num_docs, static_cast<long long>(T), ws, err_dev));
-  }
-  // The longest groups go first when the grid needs more than one wave (one
-  // CTA per SM); within a single wave the order makes no difference and the
-  // ordering launch is skipped.
-  const long long items = ngroups * ((rows == kBlockM) ? Hq / 2 : Hq);
-  if (items > sm_count())
-    CPTHD_TRY_CUDA(launch_pdl(attn_group_order_kernel, dim3(1), dim3(1024), 0, s, static_cast<int>(ngroups), ws));
-  return CPTHD_OK;
+  return launch_plan(index_list(q_slice_idx_dev), t_local, T, cu_seqlens_dev, cup, num_docs, Hq, Hkv, workspace_dev,
+                     err_dev, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int thd_causal_attn_plan_partition(int strategy, int64_t T, const int32_t* cu_seqlens_dev,
+                                              const int32_t* cu_seqlens_padded_dev, int num_docs, int cp_size,
+                                              int rank, int Hq, int Hkv, void* workspace_dev,
+                                              size_t workspace_bytes, int32_t* err_dev, cpthd_stream_t stream) {
+  using namespace cpthd;
+  int64_t t_local = 0;
+  int st = cp_local_tokens(strategy, T, cp_size, &t_local);
+  if (st != CPTHD_OK) return st;
+  if (rank < 0 || rank >= cp_size) return CPTHD_ERR_INVALID_ARG;
+  st = check_attn_shape(t_local, T, num_docs, Hq, Hkv);
+  if (st != CPTHD_OK) return st;
+  if (t_local == 0) return CPTHD_OK;
+  if (cu_seqlens_dev == nullptr || num_docs < 1) return CPTHD_ERR_INVALID_ARG;
+  st = check_workspace(t_local, Hq, Hkv, workspace_dev, workspace_bytes);
+  if (st != CPTHD_OK) return st;
+  const int32_t* cup = cu_seqlens_padded_dev ? cu_seqlens_padded_dev : cu_seqlens_dev;
+  return launch_plan(index_formula(strategy, cup, num_docs, T, cp_size, rank, t_local), t_local, T, cu_seqlens_dev,
+                     cup, num_docs, Hq, Hkv, workspace_dev, err_dev, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int thd_causal_attn_fwd_planned(int64_t t_local, const void* q_dev, const void* k_dev, const void* v_dev,

@@ -21,7 +21,7 @@
 // work to the SMs first.
 #pragma once
 
-#include "common.cuh"
+#include "partition_math.cuh"
 
 namespace cpthd {
 
@@ -70,12 +70,14 @@ inline AttnWorkspace carve_workspace(void* base, long long ngroups, int group_ro
 }
 
 // One block of ROWS threads per row group; thread t owns local row
-// group * ROWS + t. The blocks also check the document table (offsets start
-// at 0 and never decrease, padded offsets end at T, L_j <= P_j) in a
-// grid-stride loop over documents.
+// group * ROWS + t, whose physical slot comes from the slice's index list or
+// from the partition formulas. The blocks also check the document table
+// (offsets start at 0 and never decrease, padded offsets end at T,
+// L_j <= P_j, and under a computed DualChunkSwap slice every padded length
+// is a multiple of 2*cp_size) in a grid-stride loop over documents.
 template <int ROWS>
 static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
-    const int32_t* __restrict__ idx, long long t_local, const int32_t* __restrict__ cu,
+    IndexGen slots, long long t_local, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ cup, int num_docs, long long T, AttnWorkspace ws, int32_t* err) {
   constexpr int kWarps = ROWS / 32;
   __shared__ unsigned long long xbuf[2][ROWS];
@@ -89,7 +91,7 @@ static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
   const int lane = t & 31, wid = t >> 5;
   const long long group = blockIdx.x;
   const long long row = group * ROWS + t;
-  const int p = (row < t_local) ? idx[row] : 0;  // issued before anything waits
+  const int p = (row < t_local) ? slots.at(row) : 0;  // issued before anything waits
 
   for (long long j = blockIdx.x * (long long)ROWS + t; j <= num_docs; j += (long long)gridDim.x * ROWS) {
     if (j == 0 && (cu[0] != 0 || cup[0] != 0)) record_error(err, CPTHD_ERR_BAD_OFFSETS, 0);
@@ -99,6 +101,8 @@ static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
       const int P = cup[j + 1] - cup[j];
       if (L < 0 || P < 0) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
       else if (L > P) record_error(err, CPTHD_ERR_PAD_LENGTH, j);
+      else if (slots.idx == nullptr && slots.strategy == CPTHD_DUAL_CHUNK_SWAP && P % (2 * slots.cp) != 0)
+        record_error(err, CPTHD_ERR_NOT_DIVISIBLE, j);
     }
   }
 

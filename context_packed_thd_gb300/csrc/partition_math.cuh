@@ -1,5 +1,5 @@
-// Closed forms of the partition index, shared by the index kernels and the
-// fused partition-and-gather kernel.
+// Closed forms of the partition index, shared by the index kernels, the
+// fused partition-and-gather kernel and the attention metadata kernel.
 //
 // TransformerEngine PR #3221 ("Why", "What changed"): DualChunkSwap cuts
 // every document into 2*cp_size chunks and rank r owns chunks r and
@@ -56,6 +56,47 @@ __device__ __forceinline__ long long nlb_slot(int r, long long t_local, long lon
 __device__ __forceinline__ long long mirrored_slot(long long T, int cp, int r, long long t) {
   const long long chunk = T / (2LL * cp);
   return (t < chunk) ? r * chunk + t : (2LL * cp - 1 - r) * chunk + (t - chunk);
+}
+
+// Where row t of a rank's slice lives in the physical buffer: read from an
+// index list, or computed from one of the closed forms above.
+struct IndexGen {
+  const int32_t* idx;  // non-null: read the list
+  int strategy;
+  const int32_t* cup;
+  int num_docs;
+  long long T;
+  int cp;
+  int rank;
+  long long t_local;
+  __device__ __forceinline__ int32_t at(long long row) const {
+    if (idx != nullptr) return __ldg(idx + row);
+    long long slot;
+    if (strategy == CPTHD_DUAL_CHUNK_SWAP) slot = dcs_slot(cup, num_docs, cp, rank, row);
+    else if (strategy == CPTHD_NO_LOAD_BALANCE) slot = nlb_slot(rank, t_local, row);
+    else slot = mirrored_slot(T, cp, rank, row);
+    return static_cast<int32_t>(slot);
+  }
+};
+
+inline IndexGen index_list(const int32_t* idx) {
+  IndexGen g{};
+  g.idx = idx;
+  return g;
+}
+
+inline IndexGen index_formula(int strategy, const int32_t* cup, int num_docs, long long T, int cp, int rank,
+                              long long t_local) {
+  IndexGen g{};
+  g.idx = nullptr;
+  g.strategy = strategy;
+  g.cup = cup;
+  g.num_docs = num_docs;
+  g.T = T;
+  g.cp = cp;
+  g.rank = rank;
+  g.t_local = t_local;
+  return g;
 }
 
 }  // namespace cpthd

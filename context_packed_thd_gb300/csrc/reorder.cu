@@ -24,25 +24,6 @@ namespace cpthd {
 
 // Source row of each gathered row: a caller's index list, or one rank's
 // partition index computed on the fly.
-struct IndexGen {
-  const int32_t* idx;  // non-null: read the list
-  int strategy;
-  const int32_t* cup;
-  int num_docs;
-  long long T;
-  int cp;
-  int rank;
-  long long t_local;
-  __device__ __forceinline__ int32_t at(long long row) const {
-    if (idx != nullptr) return __ldg(idx + row);
-    long long slot;
-    if (strategy == CPTHD_DUAL_CHUNK_SWAP) slot = dcs_slot(cup, num_docs, cp, rank, row);
-    else if (strategy == CPTHD_NO_LOAD_BALANCE) slot = nlb_slot(rank, t_local, row);
-    else slot = mirrored_slot(T, cp, rank, row);
-    return static_cast<int32_t>(slot);
-  }
-};
-
 struct ReorderTensor {
   const void* src;
   void* dst;
@@ -198,12 +179,6 @@ static int launch_reorder(int n, const void* const* src, void* const* dst, const
   return CPTHD_OK;
 }
 
-static IndexGen list_gen(const int32_t* idx) {
-  IndexGen g{};
-  g.idx = idx;
-  return g;
-}
-
 }  // namespace cpthd
 
 extern "C" int cp_reorder(const void* src_dev, int64_t src_rows, int64_t row_bytes, const int32_t* idx_dev,
@@ -211,7 +186,7 @@ extern "C" int cp_reorder(const void* src_dev, int64_t src_rows, int64_t row_byt
   const void* srcs[1] = {src_dev};
   void* dsts[1] = {dst_dev};
   const int64_t rb[1] = {row_bytes};
-  return cpthd::launch_reorder(1, srcs, dsts, rb, src_rows, cpthd::list_gen(idx_dev), false, n_rows, nullptr,
+  return cpthd::launch_reorder(1, srcs, dsts, rb, src_rows, cpthd::index_list(idx_dev), false, n_rows, nullptr,
                                err_dev, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -221,7 +196,7 @@ extern "C" int cp_reorder_multi(int n_tensors, const void* const* src_dev_host, 
   if (src_dev_host == nullptr || dst_dev_host == nullptr || row_bytes_host == nullptr)
     return CPTHD_ERR_INVALID_ARG;
   return cpthd::launch_reorder(n_tensors, src_dev_host, dst_dev_host, row_bytes_host, src_rows,
-                               cpthd::list_gen(idx_dev), false, n_rows, nullptr, err_dev,
+                               cpthd::index_list(idx_dev), false, n_rows, nullptr, err_dev,
                                reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -237,15 +212,8 @@ extern "C" int cp_partition_reorder_multi(int strategy, const int32_t* cu_seqlen
   if (src_dev_host == nullptr || dst_dev_host == nullptr || row_bytes_host == nullptr) return CPTHD_ERR_INVALID_ARG;
   if (t_local > 0 && (cu_seqlens_padded_dev == nullptr || num_docs == 0 || idx_out_dev == nullptr))
     return CPTHD_ERR_INVALID_ARG;
-  cpthd::IndexGen g{};
-  g.idx = nullptr;
-  g.strategy = strategy;
-  g.cup = cu_seqlens_padded_dev;
-  g.num_docs = num_docs;
-  g.T = T;
-  g.cp = cp_size;
-  g.rank = rank;
-  g.t_local = t_local;
+  const cpthd::IndexGen g =
+      cpthd::index_formula(strategy, cu_seqlens_padded_dev, num_docs, T, cp_size, rank, t_local);
   return cpthd::launch_reorder(n_tensors, src_dev_host, dst_dev_host, row_bytes_host, T, g, true, t_local,
                                idx_out_dev, err_dev, reinterpret_cast<cudaStream_t>(stream));
 }

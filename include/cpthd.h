@@ -216,6 +216,25 @@ CPTHD_API int thd_causal_attn_fwd_planned(int64_t t_local, const void* q_dev, co
                                           float* lse_dev, const void* workspace_dev, size_t workspace_bytes,
                                           int32_t* err_dev, cpthd_stream_t stream);
 
+/* The plan of rank `rank`'s slice under `strategy` (CPTHD_DUAL_CHUNK_SWAP,
+ * CPTHD_NO_LOAD_BALANCE or CPTHD_PACKED_MIRRORED), with each row's physical
+ * slot computed from the partition formulas (TransformerEngine PR #3221,
+ * "What changed"; as cp_partition_index) instead of read from an index
+ * list: the workspace it writes equals that of thd_causal_attn_plan given
+ * the list cp_partition_index returns for the same rank, so the plan can run
+ * before, or beside, the partition and the gather of the slice.
+ *   cu_seqlens_dev / cu_seqlens_padded_dev / num_docs: as thd_causal_attn_fwd
+ *     (the padded offsets define the partition; null = unpadded);
+ *   t_local = T / cp_size (cp_local_tokens); the workspace is sized for it.
+ * Host checks: as cp_local_tokens (T divisible), rank in [0, cp_size), and
+ * the checks of thd_causal_attn_plan. Device checks (recorded in err): the
+ * offset table as in thd_causal_attn_fwd and, under DualChunkSwap, padded
+ * lengths that are not multiples of 2*cp_size (CPTHD_ERR_NOT_DIVISIBLE). */
+CPTHD_API int thd_causal_attn_plan_partition(int strategy, int64_t T, const int32_t* cu_seqlens_dev,
+                                             const int32_t* cu_seqlens_padded_dev, int num_docs, int cp_size,
+                                             int rank, int Hq, int Hkv, void* workspace_dev, size_t workspace_bytes,
+                                             int32_t* err_dev, cpthd_stream_t stream);
+
 /* Device workspace thd_causal_attn_bwd needs (per-row key bounds, per-tile key
  * intervals, lse * log2(e) and rowsum(dO * O) per row and query head). Host only. */
 CPTHD_API int thd_causal_attn_bwd_workspace_size(int64_t t_local, int Hq, int Hkv, int d, size_t* bytes_host);

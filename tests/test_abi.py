@@ -100,6 +100,16 @@ def test_host_validation_launches_nothing(cp):
     assert fp(4, vp(264), p, p, 8, 2, 2, 64, 0.0, p, p, p, 1 << 20, None, None) == -3  # q not 16-B aligned
     assert fp(4, p, None, p, 8, 2, 2, 64, 0.0, p, p, p, 1 << 20, None, None) == -1
     assert fp(0, None, None, None, 8, 2, 2, 64, 0.0, None, None, None, 0, None, None) == 0
+    # plan from the partition formulas: rank out of range, T not divisible,
+    # GQA mismatch, missing workspace, missing offsets; T = 0 is empty
+    pp = L.thd_causal_attn_plan_partition
+    assert pp(0, 8, p, p, 1, 2, 2, 2, 2, p, 1 << 20, None, None) == -1
+    assert pp(1, 9, p, p, 1, 2, 0, 2, 2, p, 1 << 20, None, None) == -2
+    assert pp(0, 8, p, p, 1, 2, 0, 3, 2, p, 1 << 20, None, None) == -3
+    assert pp(0, 8, p, p, 1, 2, 0, 2, 2, None, 0, None, None) == -4
+    assert pp(0, 8, None, None, 1, 2, 0, 2, 2, p, 1 << 20, None, None) == -1
+    assert pp(7, 8, p, p, 1, 2, 0, 2, 2, p, 1 << 20, None, None) == -1
+    assert pp(0, 0, None, None, 1, 2, 0, 2, 2, None, 0, None, None) == 0
     # empty slice: nothing to do
     assert f(None, 0, None, None, None, 8, None, None, 1, 2, 2, 64, 0.0, None, None, None, 0, None, None) == 0
 

@@ -210,6 +210,55 @@ def test_plan_once_run_many(hq, hkv, strategy):
         assert err.cpu().tolist() == [0, 0]
 
 
+@pytest.mark.parametrize("name", ["t8192_mha16", "t32768_lognormal_gqa32x8"])
+def test_plan_from_partition_formulas_equals_plan_from_list(name):
+    """thd_causal_attn_plan_partition (row slots from the partition formulas)
+    writes the same workspace bytes as thd_causal_attn_plan given the index
+    list, for every strategy and rank, and the attention run on either plan
+    is identical."""
+    dev = cuda_or_skip(); cp = load_lib()
+    cfg = W.CONFIG_BY_NAME[name]
+    for s in ("dcs", "nlb", "mirrored"):
+        strat = "dcs" if s == "dcs" else "nlb"      # the mirrored split runs on the unpadded buffer
+        inp = W.make_attn_inputs(cfg, strat)
+        d = DevInputs(inp, dev)
+        lay = inp.layout
+        if s == "mirrored" and lay.T % (2 * cfg.cp) != 0:
+            continue
+        err = new_err(dev)
+        tl = cp.cp_local_tokens(s, lay.T, cfg.cp)
+        nb = cp.thd_causal_attn_workspace_size(tl, cfg.hq, cfg.hkv, cfg.d)
+        for r in range(cfg.cp):
+            ws_list = torch.zeros(nb, dtype=torch.uint8, device=dev)
+            ws_form = torch.zeros(nb, dtype=torch.uint8, device=dev)
+            idx = cp.cp_partition_index(s, d.cup, lay.T, cfg.cp, r, err=err)
+            cp.thd_causal_attn_plan(idx, lay.T, d.cu, d.cup, cfg.hq, cfg.hkv, workspace=ws_list, err=err)
+            cp.thd_causal_attn_plan_partition(s, lay.T, d.cu, d.cup, cfg.cp, r, cfg.hq, cfg.hkv, workspace=ws_form,
+                                              err=err)
+            assert torch.equal(ws_list, ws_form), (name, s, r)
+            if r in (0, cfg.cp - 1):
+                q_loc = cp.cp_reorder(d.q, idx, err=err)
+                o1, l1 = cp.thd_causal_attn_fwd_planned(q_loc, d.k, d.v, ws_form, err=err)
+                o2, l2 = cp.thd_causal_attn_fwd(idx, q_loc, d.k, d.v, d.cu, d.cup, err=err)
+                assert torch.equal(o1, o2) and torch.equal(l1, l2), (name, s, r)
+        assert err.cpu().tolist() == [0, 0], (name, s)
+
+
+def test_plan_from_partition_checks_divisibility():
+    """Under DualChunkSwap a padded length that is not a multiple of
+    2*cp_size is recorded by the plan itself (no index list was built)."""
+    dev = cuda_or_skip(); cp = load_lib()
+    cu = torch.tensor([0, 12, 24], dtype=torch.int32, device=dev)   # 12 % (2 * 2) == 0, fine
+    cup = torch.tensor([0, 12, 24], dtype=torch.int32, device=dev)
+    err = new_err(dev)
+    cp.thd_causal_attn_plan_partition("dcs", 24, cu, cup, 2, 0, 2, 2, err=err)
+    assert err.cpu().tolist() == [0, 0]
+    cu = torch.tensor([0, 10, 24], dtype=torch.int32, device=dev)   # 10 % 4 != 0
+    err = new_err(dev)
+    cp.thd_causal_attn_plan_partition("dcs", 24, cu, cu, 2, 0, 2, 2, err=err)
+    assert err.cpu().tolist()[0] == -2
+
+
 def test_plan_on_side_stream_beside_the_gather():
     """The order a caller overlaps the path in: partition index, then the
     gather on the current stream and the plan on a side stream (the plan
