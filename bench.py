@@ -542,13 +542,15 @@ def run_cuda(args):
     h2d = sum(sum(t.numel() * t.element_size() for t in st.host.values()) for st in strategies)
     d2h = sum(st.out[r].numel() * st.out[r].element_size() + st.lse[r].numel() * st.lse[r].element_size()
               for st in strategies for r in ranks)
-    g_strat = []
+    g_rank = []
     for st in strategies:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for r in ranks:
+        gs = []
+        for r in ranks:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
                 st.run_rank(cp, r)
-        g_strat.append(g)
+            gs.append(g)
+        g_rank.append(gs)
     up_stream, down_stream = torch.cuda.Stream(), torch.cuda.Stream()
 
     def e2e_step():
@@ -560,11 +562,12 @@ def run_cuda(args):
                 inputs_in.append(up_stream.record_event())
         for k, st in enumerate(strategies):
             stream.wait_event(inputs_in[k])
-            g_strat[k].replay()
-            computed = stream.record_event()
-            with torch.cuda.stream(down_stream):
-                down_stream.wait_event(computed)
-                for r in ranks:
+            for i, r in enumerate(ranks):
+                g_rank[k][i].replay()
+                computed = stream.record_event()
+                # each rank's results go down while the next rank computes
+                with torch.cuda.stream(down_stream):
+                    down_stream.wait_event(computed)
                     st.out_host[r].copy_(st.out[r], non_blocking=True)
                     st.lse_host[r].copy_(st.lse[r], non_blocking=True)
         torch.cuda.synchronize()
@@ -688,8 +691,8 @@ def run_cuda(args):
                          "peak_source": f"{peak_src} bf16_tflops (burst)"},
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4),
-                    "timing": f"wall clock, median of {e2e_steps} steps after 2 untimed ones; uploads, "
-                              "compute and downloads overlapped per strategy on three streams"},
+                    "timing": f"wall clock, median of {e2e_steps} steps after 2 untimed ones; uploads per "
+                              "strategy, compute, and downloads per rank slice overlapped on three streams"},
             "gpu_launches": sum(st.launches_per_rank for st in strategies) * len(ranks) * args.steps,
             "gpu_launches_note": "library kernels inside the timed step replays; the L2 flush between steps is a torch fill",
             "clocks": clocks,
