@@ -200,7 +200,8 @@ CPTHD_API int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loca
 /* The forward in two parts, for callers that run several attentions over
  * the same slice (every layer of a model step shares q_slice_idx and the
  * offsets): thd_causal_attn_plan writes the row-group metadata (per-row key
- * bounds, per-group key intervals, the group order) into the workspace once;
+ * bounds, per-group key intervals and, when the grid needs more CTAs than
+ * the GPU has SMs, the group order) into the workspace once;
  * thd_causal_attn_fwd_planned runs the attention kernel against it as often
  * as needed. thd_causal_attn_fwd is the two in sequence. The planned call
  * must get the same t_local, T, Hq, Hkv and the workspace the plan wrote
