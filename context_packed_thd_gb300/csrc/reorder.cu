@@ -6,12 +6,16 @@
 // activations). It is a pure copy, bound by HBM bandwidth for wide rows and
 // by launch latency for the 8-byte id rows.
 //
-// Layout: one warp copies one row per step; its lanes move 16-byte vectors
-// (8- or 4-byte when the row or a base pointer is less aligned, bytes
-// otherwise) with UNROLL independent loads in flight before the stores, so
-// the SMs keep enough bytes outstanding to cover HBM latency. Narrow rows
-// (fewer than 32 vectors) use one thread per vector instead. Loads and stores
-// use the streaming cache hints: every byte is touched once.
+// Layout: wide rows are cut into units of 32 x UNROLL vectors (2 KB with
+// 16-byte vectors), and the warps of the grid take units in turn: a warp's
+// lanes move one unit per step with UNROLL independent loads in flight
+// before the stores, so the SMs keep enough bytes outstanding to cover HBM
+// latency, and every warp gets nearly the same number of units whatever the
+// row count (one row per warp left up to half of the warps idle for the
+// last row). Vectors are 16 bytes (8 or 4 when the row or a base pointer is
+// less aligned, bytes otherwise). Narrow rows (fewer than 32 vectors) use
+// one thread per vector instead. Loads and stores use the streaming cache
+// hints: every byte is touched once.
 //
 // The fused form (cp_partition_reorder_multi) takes the source rows from
 // the partition formulas instead of an index list: each row's physical slot
@@ -22,8 +26,6 @@
 
 namespace cpthd {
 
-// Source row of each gathered row: a caller's index list, or one rank's
-// partition index computed on the fly.
 struct ReorderTensor {
   const void* src;
   void* dst;
@@ -46,28 +48,34 @@ __device__ __forceinline__ void store_stream<uint8_t>(uint8_t* p, uint8_t v) { *
 
 constexpr int kUnroll = 4;
 
+constexpr int kUnitVecs = 32 * kUnroll;  // vectors per unit of work
+
 template <typename V>
 __device__ __forceinline__ void gather_wide(const V* __restrict__ src, long long src_rows, long long vpr,
                                             const IndexGen& ig, long long n_rows,
                                             V* __restrict__ dst, int32_t* err, long long warp,
                                             long long nwarps, int lane) {
-  for (long long row = warp; row < n_rows; row += nwarps) {
+  const long long upr = (vpr + kUnitVecs - 1) / kUnitVecs;  // units per row
+  const long long units = n_rows * upr;
+  for (long long unit = warp; unit < units; unit += nwarps) {
+    const long long row = unit / upr;
+    const long long c0 = (unit - row * upr) * kUnitVecs;
     const int32_t s = ig.at(row);
     if (s < 0 || s >= src_rows) {
-      if (lane == 0) record_error(err, CPTHD_ERR_INDEX_RANGE, row);
+      if (lane == 0 && c0 == 0) record_error(err, CPTHD_ERR_INDEX_RANGE, row);
       continue;
     }
     const V* sp = src + static_cast<long long>(s) * vpr;
     V* dp = dst + row * vpr;
-    long long c = lane;
-    for (; c + (kUnroll - 1) * 32 < vpr; c += kUnroll * 32) {
+    if (c0 + kUnitVecs <= vpr) {
       V tmp[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) tmp[u] = load_stream(sp + c + u * 32);
+      for (int u = 0; u < kUnroll; ++u) tmp[u] = load_stream(sp + c0 + lane + u * 32);
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) store_stream(dp + c + u * 32, tmp[u]);
+      for (int u = 0; u < kUnroll; ++u) store_stream(dp + c0 + lane + u * 32, tmp[u]);
+    } else {
+      for (long long c = c0 + lane; c < vpr; c += 32) store_stream(dp + c, load_stream(sp + c));
     }
-    for (; c < vpr; c += 32) store_stream(dp + c, load_stream(sp + c));
   }
 }
 
@@ -164,12 +172,21 @@ static int launch_reorder(int n, const void* const* src, void* const* dst, const
   if (n_rows == 0 || (max_bytes == 0 && !computed)) return CPTHD_OK;
   if (!computed && ig.idx == nullptr) return CPTHD_ERR_INVALID_ARG;
   if (computed && (ig.idx != nullptr || idx_out == nullptr)) return CPTHD_ERR_INVALID_ARG;
-  // a warp per row for wide rows, a thread per vector for narrow rows;
-  // capped at 8 resident 256-thread blocks on each of the 152 SMs
+  // Wide rows: a warp per unit (32 x kUnroll vectors) for large gathers, a
+  // warp per row for small ones (the warps then share the rows' units); a
+  // thread per vector for narrow rows; capped at 8 resident 256-thread
+  // blocks on each of the 152 SMs. Sized by units, the small Q gather of a
+  // rank slice held more SMs for longer and the attention launch after it
+  // started later; sized by rows, the large activation gathers left SMs
+  // idle (82% vs 79% of the copy bandwidth on [131072, 8192] bf16).
+  long long total_bytes = 0;
+  for (int i = 0; i < n; ++i) total_bytes += n_rows * b.t[i].row_bytes;
+  const bool by_units = total_bytes >= (32LL << 20);
   long long work = computed ? n_rows : 0;  // the index list is written by one thread per row
   for (int i = 0; i < n; ++i) {
     const long long vpr = b.t[i].row_bytes / b.t[i].vec;
-    const long long w = (vpr >= 32) ? n_rows * 32 : n_rows * vpr;
+    const long long upr = by_units ? (vpr + kUnitVecs - 1) / kUnitVecs : 1;
+    const long long w = (vpr >= 32) ? n_rows * upr * 32 : n_rows * vpr;
     work = w > work ? w : work;
   }
   const int grid = grid_for(work, 256, 152 * 8);
