@@ -313,6 +313,15 @@ def other_workloads(cp, current, dev, flush, peak):
                     st.run_attn(cp, r)
 
         ms = _graph_ms(attn_all, flush, reps=3)
+        # each strategy's slices alone as well: DualChunkSwap balances the
+        # ranks, NO_LOAD_BALANCE leaves them as uneven as the pack makes them
+        by_strategy = {}
+        if len(sts) > 1:
+            for st in sts:
+                ms_s = _graph_ms(lambda st=st: [st.run_attn(cp, r) for r in range(cfg.cp)], flush, reps=3)
+                tf_s = sum(st.flops) / (ms_s * 1e-3) / 1e12
+                by_strategy[st.name] = {"attn_tflops": round(tf_s, 3), "frac_of_peak": round(tf_s / peak, 4),
+                                        "ms": round(ms_s, 4)}
         for st in sts:
             e = st.err.cpu().tolist()
             if e[0] != 0:
@@ -320,7 +329,8 @@ def other_workloads(cp, current, dev, flush, peak):
         flops = sum(sum(st.flops) for st in sts)
         tf = flops / (ms * 1e-3) / 1e12
         out[cfg.name] = {"attn_tflops": round(tf, 3), "frac_of_peak": round(tf / peak, 4), "ms": round(ms, 4),
-                         "rank_slices": cfg.cp * len(sts), "strategies": list(cfg.strategies)}
+                         "rank_slices": cfg.cp * len(sts), "strategies": list(cfg.strategies),
+                         "per_strategy": by_strategy or None}
         del sts
         torch.cuda.empty_cache()
     return out
