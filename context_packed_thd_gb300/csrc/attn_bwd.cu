@@ -53,6 +53,7 @@ struct BwdParams {
   const int32_t* row_hi;
   const GroupInfo* tile_info;
   const int2* intervals;
+  const int32_t* order;  // dQ grid: query tiles by decreasing block count; null = natural order
   const float* lse2;  // [Hq, rows_pad]: lse * log2(e)
   const float* dvec;  // [Hq, rows_pad]: rowsum(dO * O)
   float* dq;
@@ -130,7 +131,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x / p.Hq;
+  // with more CTAs than SMs the costliest query tiles go first
+  const int tile = p.order ? __ldg(p.order + blockIdx.x / p.Hq) : static_cast<int>(blockIdx.x / p.Hq);
   const int h = blockIdx.x % p.Hq;
   const int kvh = h / (p.Hq / p.Hkv);
   const GroupInfo ti = p.tile_info[tile];
@@ -705,11 +707,16 @@ static int launch_bwd(const void* q, const void* k, const void* v, const void* o
   attn_bwd_pre_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, t_local, Hq, rows_pad,
       lse2, dvec);
+  // The dQ grid runs in decreasing-cost order (the forward's group order
+  // over the query tiles) when it needs more than one wave of CTAs.
+  const bool ordered = ntiles * Hq > sm_count();
+  if (ordered) attn_group_order_kernel<<<1, 1024, 0, s>>>(static_cast<int>(ntiles), ws);
   BwdParams p;
   p.row_lo = ws.row_lo;
   p.row_hi = ws.row_hi;
   p.tile_info = ws.group_info;
   p.intervals = ws.intervals;
+  p.order = ordered ? ws.order : nullptr;
   p.lse2 = lse2;
   p.dvec = dvec;
   p.dq = dq;
