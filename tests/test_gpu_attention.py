@@ -259,6 +259,42 @@ def test_plan_from_partition_checks_divisibility():
     assert err.cpu().tolist()[0] == -2
 
 
+@pytest.mark.parametrize("seed", [101, 102, 103, 104, 105, 106, 107, 122, 124])
+def test_random_packs_every_row(seed):
+    """Seeded random packs (empty and one-token documents included, DCS
+    padding, cp_size 1-8, GQA group sizes 1-4, d = 64 or 128), every rank of
+    every partition that the pack allows, every row against the oracle."""
+    dev = cuda_or_skip(); cp = load_lib()
+    rng = np.random.default_rng(seed)
+    cpsize = int(rng.choice([1, 2, 4, 8]))
+    hkv = int(rng.choice([1, 2, 4]))
+    hq = hkv * int(rng.choice([1, 2, 3, 4]))
+    dd = int(rng.choice([64, 128]))
+    lay = W.random_layout(rng, int(rng.integers(1, 24)), 700, 2 * cpsize, allow_empty=True)
+    total = int(lay.cu_seqlens[-1])
+    if total == 0:
+        pytest.skip("empty pack")
+    q, k, v = W.make_qkv_logical(seed, total, hq, hkv, dd)
+    if lay.T != total:
+        q, k, v = (W.to_physical(t, lay, 0) for t in (q, k, v))
+    cu = torch.from_numpy(lay.cu_seqlens).to(dev)
+    cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    strategies = ["dcs", "nlb"] + (["mirrored"] if lay.T % (2 * cpsize) == 0 else [])
+    err = new_err(dev)
+    for s in strategies:
+        for r in range(cpsize):
+            idx = cp.cp_partition_index(s, cup, lay.T, cpsize, r, err=err)
+            q_loc = cp.cp_reorder(qd, idx, err=err)
+            out, lse = cp.thd_causal_attn_fwd(idx, q_loc, kd, vd, cu, cup, err=err)
+            ref_idx = np.asarray(P.partition_index(s, lay.cu_seqlens_padded.tolist(), cpsize, r), dtype=np.int64)
+            assert np.array_equal(idx.cpu().numpy(), ref_idx)
+            ro, rl = A.attention_fwd(q[torch.from_numpy(ref_idx)], k, v, lay.cu_seqlens, lay.cu_seqlens_padded,
+                                     ref_idx)
+            assert_attn_matches(out, lse, ro, rl, f"seed {seed}/{s}/rank{r}")
+    assert err.cpu().tolist() == [0, 0]
+
+
 def test_plan_on_side_stream_beside_the_gather():
     """The order a caller overlaps the path in: partition index, then the
     gather on the current stream and the plan on a side stream (the plan
