@@ -108,3 +108,36 @@ def test_backward_edge_cases(case):
             for n, g, e, z in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, (zq, zk, zk)):
                 _check(f"{case}/{s}/r{r}/{n}", g, e, z)
     assert err.cpu().tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("seed", [201, 202, 203, 204])
+def test_backward_random_packs(seed):
+    """Seeded random packs (empty and one-token documents included, DCS
+    padding, cp_size 1-8, GQA group sizes 1-4, d = 64 or 128): every rank of
+    both partitions against the oracle."""
+    dev = cuda_or_skip(); cp = load_lib()
+    rng = np.random.default_rng(seed)
+    cpsize = int(rng.choice([1, 2, 4, 8]))
+    hkv = int(rng.choice([1, 2, 4]))
+    hq = hkv * int(rng.choice([1, 2, 3, 4]))
+    dd = int(rng.choice([64, 128]))
+    lay = W.random_layout(rng, int(rng.integers(1, 16)), 500, 2 * cpsize, allow_empty=True)
+    total = int(lay.cu_seqlens[-1])
+    if total == 0:
+        pytest.skip("empty pack")
+    q, k, v = W.make_qkv_logical(seed, total, hq, hkv, dd)
+    if lay.T != total:
+        q, k, v = (W.to_physical(t, lay, 0) for t in (q, k, v))
+    cfg = W.Config("random", seed, tuple(np.diff(lay.cu_seqlens).tolist()), hq, hkv, dd, cpsize, ("dcs", "nlb"),
+                   2 * cpsize)
+    inp = W.AttnInputs(cfg, "dcs", lay, q, k, v)
+    dout_phys = W.randn_bf16(seed, 6, (lay.T, hq, dd))
+    err = new_err(dev)
+    for s in ("dcs", "nlb"):
+        for r in range(cpsize):
+            idx, dq, dk, dv, dout = _rank_bwd(cp, inp, s, cpsize, r, dev, dout_phys, err)
+            ref = A.attention_bwd(q[torch.from_numpy(idx)], k, v, lay.cu_seqlens, lay.cu_seqlens_padded, idx, dout)
+            zq, zk = _structural_zero(lay, idx)
+            for n, g, e, z in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, (zq, zk, zk)):
+                _check(f"seed {seed}/{s}/r{r}/{n}", g, e, z)
+    assert err.cpu().tolist() == [0, 0]
