@@ -125,6 +125,8 @@ def _custom(lengths, pad_multiple, hq, hkv, dd, seed):
     dict(lengths=[37, 91, 250, 3], pad=8, hq=6, hkv=2, d=128, cp=4),       # pad rows, GQA 3
     dict(lengths=[129, 127, 128, 256, 1], pad=2, hq=2, hkv=2, d=64, cp=1),  # docs at tile edges, pads
     dict(lengths=[700, 53, 1200], pad=16, hq=8, hkv=8, d=128, cp=8),       # several ranks, chunk < tile
+    dict(lengths=[517, 1, 260, 900], pad=4, hq=32, hkv=1, d=64, cp=2),     # one KV head for 32 query heads
+    dict(lengths=[2000, 3, 1500], pad=2, hq=5, hkv=5, d=128, cp=1),        # odd head count, one rank
 ])
 def test_edge_cases(case):
     dev = cuda_or_skip(); cp = load_lib()
