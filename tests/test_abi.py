@@ -121,3 +121,39 @@ def test_workspace_size(cp):
     e = cp.thd_causal_attn_workspace_size(129, 32, 8, 128)
     assert 0 < a < b and 0 < c < e
     assert cp.thd_causal_attn_workspace_size(0, 8, 8, 128) >= 0
+
+
+def test_host_validation_restore_multi_reorder_backward(cp):
+    """Host checks of the remaining entry points: each call returns its
+    status before any launch or device call (no GPU needed)."""
+    L = cp.lib
+    vp = ctypes.c_void_p
+    p = vp(256)
+    # restore index: T not divisible, negative document count, missing offsets / output
+    assert L.cp_restore_index(1, p, 1, 9, 2, p, None, None) == -2
+    assert L.cp_restore_index(0, p, -1, 8, 2, p, None, None) == -1
+    assert L.cp_restore_index(0, None, 1, 8, 2, p, None, None) == -1
+    assert L.cp_restore_index(0, p, 1, 8, 2, None, None, None) == -1
+    # multi-tensor gather: tensor count out of [1, 8], missing arrays, negative row width,
+    # missing index list while rows are to be copied
+    srcs = (vp * 9)(*([p] * 9)); dsts = (vp * 9)(*([p] * 9)); rb = (ctypes.c_int64 * 9)(*([16] * 9))
+    rm = L.cp_reorder_multi
+    assert rm(0, srcs, dsts, rb, 8, p, 4, None, None) == -1
+    assert rm(9, srcs, dsts, rb, 8, p, 4, None, None) == -1
+    assert rm(1, None, dsts, rb, 8, p, 4, None, None) == -1
+    neg = (ctypes.c_int64 * 1)(-16)
+    assert rm(1, srcs, dsts, neg, 8, p, 4, None, None) == -1
+    assert rm(1, srcs, dsts, rb, 8, None, 4, None, None) == -1
+    assert rm(1, srcs, dsts, rb, 8, p, 0, None, None) == 0  # nothing to gather
+    # backward: negative rows, head dim, GQA mismatch, too many query tiles, missing dK/dV
+    bw = L.thd_causal_attn_bwd
+    args = lambda t_local, hq, hkv, d, dk: (p, t_local, p, p, p, p, p, p, 8, p, None, 1, hq, hkv, d, 0.0, p, dk, p,
+                                             p, 1 << 20, None, None)
+    assert bw(*args(-1, 2, 2, 64, p)) == -1
+    assert bw(*args(4, 2, 2, 96, p)) == -3
+    assert bw(*args(4, 3, 2, 64, p)) == -3
+    assert bw(*args(2048 * 128 + 1, 2, 2, 64, p)) == -3
+    assert bw(*args(4, 2, 2, 64, None)) == -1
+    size = ctypes.c_size_t(0)
+    assert L.thd_causal_attn_bwd_workspace_size(-1, 2, 2, 64, ctypes.byref(size)) == -1
+    assert L.thd_causal_attn_bwd_workspace_size(256, 2, 2, 64, ctypes.byref(size)) == 0 and size.value > 0
