@@ -50,9 +50,18 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "causal-THD attn fwd TFLOPS (unmasked pairs) & % BF16 peak; reorder GB/s"
-DEFAULT_WORKLOAD = "t8192_mha16"
+DEFAULT_WORKLOAD = "long131072_h8"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+
+# DRAM bytes per launch of the attention kernel on the default workload
+# (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture of the 32
+# rank-slice launches of one step, averaged over them). The figure holds for
+# the kernel sources that hash to ATTN_TRAFFIC["source_sha256"]; once they
+# change, the line reports null until it is captured again.
+ATTN_SOURCES = ("csrc/attn_fwd.cu", "csrc/attn_common.cuh", "csrc/attn_meta.cuh", "csrc/sm100.cuh",
+                "csrc/common.cuh")
+ATTN_TRAFFIC = {"workload": "long131072_h8", "bytes_per_launch": None, "source_sha256": None}
 
 
 def load_peaks():
@@ -87,26 +96,22 @@ def replica_value(units_per_replica: float, world: int, seconds: float) -> float
     return world * units_per_replica / seconds
 
 
-def measured_traffic(workload: str, subset: bool):
-    """Per-launch DRAM bytes of the attention kernel from the committed ncu
-    summary, or None when the workload differs or the kernel sources changed
-    since the capture."""
-    path = os.path.join(ROOT, "profiles", "attn_fwd_tc_t8192_traffic.md")
-    if subset or workload != DEFAULT_WORKLOAD or not os.path.exists(path):
-        return None
-    txt = open(path).read()
-    try:
-        traffic = int(txt.split("traffic_bytes_per_launch:")[1].split()[0])
-        want = txt.split("source_sha256:")[1].split()[0]
-        files = txt.split("source_files:")[1].splitlines()[0].split()
-    except (IndexError, ValueError):
-        return None
+def attn_source_sha() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in files:
+    for f in ATTN_SOURCES:
         with open(os.path.join(ROOT, "context_packed_thd_gb300", f), "rb") as fh:
             h.update(fh.read())
-    return traffic if h.hexdigest() == want else None
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, subset: bool):
+    """Per-launch DRAM bytes of the attention kernel (ATTN_TRAFFIC), or None
+    when the workload differs, only part of the step runs, or the kernel
+    sources changed since the capture."""
+    if subset or workload != ATTN_TRAFFIC["workload"] or ATTN_TRAFFIC["bytes_per_launch"] is None:
+        return None
+    return ATTN_TRAFFIC["bytes_per_launch"] if attn_source_sha() == ATTN_TRAFFIC["source_sha256"] else None
 
 
 def rank_pairs(idx: np.ndarray, lay: W.Layout) -> int:
@@ -117,6 +122,30 @@ def rank_pairs(idx: np.ndarray, lay: W.Layout) -> int:
     pos = idx - cup[j]
     valid = pos < lay.lengths[j]
     return int((pos[valid] + 1).sum())
+
+
+def kernel_pairs(idx: np.ndarray, lay: W.Layout, hq: int, hkv: int) -> int:
+    """(query row, key) products per head that the attention kernel's
+    schedule computes for one slice: consecutive local rows form row groups
+    (128 rows when the GQA group size is even, else 256), and a group walks,
+    for every document among its real rows, the 128-key blocks from the
+    document start to its largest row slot. Useful pairs / this = the
+    fraction of the tensor work that is unmasked."""
+    rows = 128 if (hq // hkv) % 2 == 0 else 256
+    cup = lay.cu_seqlens_padded.astype(np.int64)
+    j = np.searchsorted(cup, idx, side="right") - 1
+    pos = idx - cup[j]
+    valid = pos < lay.lengths[j]
+    grp = np.arange(len(idx)) // rows
+    total = 0
+    gv, jv, pv = grp[valid], j[valid], pos[valid]
+    if gv.size:
+        key = gv * (lay.num_docs + 1) + jv
+        order = np.lexsort((pv, key))
+        k_sorted, p_sorted = key[order], pv[order]
+        last = np.r_[k_sorted[1:] != k_sorted[:-1], True]
+        total = int(((p_sorted[last] + 128) // 128).sum())
+    return total * 128 * rows
 
 
 # ----------------------------------------------------------------------------
@@ -215,10 +244,12 @@ class Strategy:
         self.out_host = [torch.empty_like(o, device="cpu").pin_memory() for o in self.out]
         self.lse_host = [torch.empty_like(x, device="cpu").pin_memory() for x in self.lse]
         # algorithmic work, from the index lists the library itself returns
-        self.pairs = []
+        self.pairs, self.kpairs = [], []
         for r in range(cfg.cp):
             cp.cp_partition_index(strategy, self.dev["cup"], self.T, cfg.cp, r, out=self.idx[r], err=self.err)
-            self.pairs.append(rank_pairs(self.idx[r].cpu().numpy().astype(np.int64), lay))
+            idx_h = self.idx[r].cpu().numpy().astype(np.int64)
+            self.pairs.append(rank_pairs(idx_h, lay))
+            self.kpairs.append(kernel_pairs(idx_h, lay, hq, cfg.hkv))
         self.flops = [4.0 * d * p * hq for p in self.pairs]
         # reorder bytes per rank: read + write of every gathered row, plus the index list
         rb = hq * d * 2 + 3 * 8
@@ -294,7 +325,7 @@ def _graph_ms(fn, flush, reps=5):
     return statistics.median(ms)
 
 
-def other_workloads(cp, current, dev, flush, peak, peak_sustained):
+def other_workloads(cp, current, dev, flush, peak, peak_sustained, hbm_peak):
     """Attention throughput of every other multi-rank workload: all ranks of
     all its strategies in one CUDA graph (L2 flushed before each replay), so
     that the line also carries the long-context and many-document figures.
@@ -326,23 +357,28 @@ def other_workloads(cp, current, dev, flush, peak, peak_sustained):
                 tf_s = sum(st.flops) / (ms_s * 1e-3) / 1e12
                 by_strategy[st.name] = {"attn_tflops": round(tf_s, 3), "frac_of_peak": round(tf_s / peak, 4),
                                         "frac_of_sustained_peak": round(tf_s / peak_sustained, 4),
-                                        "ms": round(ms_s, 4)}
+                                        "ms": round(ms_s, 4),
+                                        "useful_pair_frac": round(sum(st.pairs) / sum(st.kpairs), 4)}
+        dcs = [st for st in sts if st.name == W.DUAL_CHUNK_SWAP]
+        restore = kv_restore(cp, cfg, dcs[0], flush, hbm_peak) if dcs else None
         for st in sts:
             e = st.err.cpu().tolist()
             if e[0] != 0:
                 raise RuntimeError(f"device check failed on {cfg.name}: {cp.cpthd_status_string(e[0])} ({e})")
         flops = sum(sum(st.flops) for st in sts)
         tf = flops / (ms * 1e-3) / 1e12
+        useful = sum(sum(st.pairs) for st in sts) / sum(sum(st.kpairs) for st in sts)
         out[cfg.name] = {"attn_tflops": round(tf, 3), "frac_of_peak": round(tf / peak, 4),
                          "frac_of_sustained_peak": round(tf / peak_sustained, 4), "ms": round(ms, 4),
                          "rank_slices": cfg.cp * len(sts), "strategies": list(cfg.strategies),
-                         "per_strategy": by_strategy or None}
+                         "useful_pair_frac": round(useful, 4),
+                         "per_strategy": by_strategy or None, "kv_restore": restore}
         del sts
         torch.cuda.empty_cache()
     return out
 
 
-def kv_restore(cp, cfg, st, flush, dev, hbm_peak):
+def kv_restore(cp, cfg, st, flush, hbm_peak):
     """Restore of all-gathered K and V (rank-major) to token order: the
     gathered buffers are simulated on one GPU, the restore is one reorder
     launch of both tensors through cp_restore_index."""
@@ -364,7 +400,9 @@ def kv_restore(cp, cfg, st, flush, dev, hbm_peak):
 def dcs_two_launch(cp, cfg, st, ranks, flush):
     """Matched-input comparison: a DualChunkSwap rank's attention as one launch
     over its whole slice against two launches, one per owned chunk (the two
-    attention steps the pages describe), on the same inputs."""
+    attention steps the pages describe), on the same inputs. The two
+    launches' outputs, put back in slice order, are compared with the one
+    launch's (max |difference|), and the device checks are read."""
     d = st.dev
     lay = st.lay
     lcu = lay.cu_seqlens_padded.astype(np.int64) // cfg.cp
@@ -374,10 +412,11 @@ def dcs_two_launch(cp, cfg, st, ranks, flush):
         halves[0].append(np.arange(lcu[j], lcu[j] + c))
         halves[1].append(np.arange(lcu[j] + c, lcu[j + 1]))
     rows = [np.concatenate(h).astype(np.int64) for h in halves]
-    fused, split = [], []
+    fused, split, max_diff, identical = [], [], 0.0, True
     for r in ranks:
-        idx_h = [st.idx[r][torch.from_numpy(x).to(st.idx[r].device)].contiguous() for x in rows]
-        q_h = [st.q_loc[r][torch.from_numpy(x).to(st.q_loc[r].device)].contiguous() for x in rows]
+        rows_d = [torch.from_numpy(x).to(st.idx[r].device) for x in rows]
+        idx_h = [st.idx[r][x].contiguous() for x in rows_d]
+        q_h = [st.q_loc[r][x].contiguous() for x in rows_d]
         out_h = [torch.empty_like(q) for q in q_h]
         lse_h = [torch.empty((cfg.hq, q.shape[0]), dtype=torch.float32, device=q.device) for q in q_h]
         ws_h = [torch.empty(cp.thd_causal_attn_workspace_size(q.shape[0], cfg.hq, cfg.hkv, cfg.d), dtype=torch.uint8,
@@ -389,8 +428,25 @@ def dcs_two_launch(cp, cfg, st, ranks, flush):
                                        lse=lse_h[h], workspace=ws_h[h], err=st.err)
         fused.append(_graph_ms(lambda: st.run_attn(cp, r), flush, reps=3))
         split.append(_graph_ms(two, flush, reps=3))
+        torch.cuda.synchronize()
+        e = st.err.cpu().tolist()
+        if e[0] != 0:
+            raise RuntimeError(f"device check failed in the two-launch run: {cp.cpthd_status_string(e[0])} ({e})")
+        out_one, lse_one = st.out[r], st.lse[r]
+        for h in range(2):
+            do = (out_h[h].float() - out_one[rows_d[h]].float()).abs().max().item()
+            fin = torch.isfinite(lse_one[:, rows_d[h]])
+            if not torch.equal(fin, torch.isfinite(lse_h[h])):
+                raise RuntimeError("two-launch run: pad rows differ from the one-launch run")
+            dl = (lse_h[h][fin] - lse_one[:, rows_d[h]][fin]).abs().max().item() if fin.any() else 0.0
+            max_diff = max(max_diff, do, dl)
+            identical = identical and torch.equal(out_h[h], out_one[rows_d[h]]) and torch.equal(
+                lse_h[h][fin], lse_one[:, rows_d[h]][fin])
+    if max_diff > 2e-2:
+        raise RuntimeError(f"two-launch outputs differ from the one-launch outputs by {max_diff}")
     return {"attn_ms_one_launch": round(sum(fused), 5), "attn_ms_two_launches": round(sum(split), 5),
-            "two_over_one": round(sum(split) / sum(fused), 3), "ranks": len(ranks)}
+            "two_over_one": round(sum(split) / sum(fused), 3), "ranks": len(ranks),
+            "max_abs_diff_vs_one_launch": max_diff, "bit_identical_to_one_launch": bool(identical)}
 
 
 def backward(cp, cfg, strategies, ranks, flush, peak):
@@ -643,11 +699,18 @@ def run_cuda(args):
         kms = med_kern[k:k + len(ranks)]
         fl = [st.flops[r] for r in ranks]
         pr = [st.pairs[r] for r in ranks]
+        kp = [st.kpairs[r] for r in ranks]
         per_strategy[st.name] = {
             "attn_ms_per_rank_max": round(max(ms), 5), "attn_ms_per_rank_min": round(min(ms), 5),
             "kernel_ms_per_rank_max": round(max(kms), 5), "kernel_ms_per_rank_min": round(min(kms), 5),
+            "kernel_ms_max_over_min": round(max(kms) / min(kms), 3),
+            "rank_of_max": ranks[kms.index(max(kms))], "rank_of_min": ranks[kms.index(min(kms))],
+            "kernel_ms_per_rank": [round(x, 5) for x in kms],
             "attn_tflops": round(sum(fl) / (sum(ms) * 1e-3) / 1e12, 3),
+            "kernel_tflops": round(sum(fl) / (sum(kms) * 1e-3) / 1e12, 3),
             "pairs_per_rank_max": max(pr), "pairs_per_rank_min": min(pr),
+            "pairs_max_over_min": round(max(pr) / min(pr), 3),
+            "useful_pair_frac": round(sum(pr) / sum(kp), 4),
         }
         k += len(ranks)
     achieved = flops_step / (sum(med_kern) * 1e-3) / 1e12
@@ -655,16 +718,16 @@ def run_cuda(args):
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    peak_sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     reorder_bytes = sum(st.reorder_bytes * len(ranks) for st in strategies)
     prep_total_ms = sum(med_prep)
     act = activation_reorder(cp, cfg, strategies[0], ranks, flush, dev, hbm_peak) if cfg.act_width else None
     dcs_st = [st for st in strategies if st.name == W.DUAL_CHUNK_SWAP]
     extras = set() if args.no_extras else set(args.extras.split(","))
-    restore = kv_restore(cp, cfg, dcs_st[0], flush, dev, hbm_peak) if dcs_st and "restore" in extras else None
+    restore = kv_restore(cp, cfg, dcs_st[0], flush, hbm_peak) if dcs_st and "restore" in extras else None
     two = dcs_two_launch(cp, cfg, dcs_st[0], ranks, flush) if dcs_st and "two_launch" in extras else None
     bwd = backward(cp, cfg, strategies, ranks, flush, peak) if "backward" in extras else None
-    peak_sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    others = other_workloads(cp, cfg.name, dev, flush, peak, peak_sustained) if "others" in extras else None
+    others = other_workloads(cp, cfg.name, dev, flush, peak, peak_sustained, hbm_peak) if "others" in extras else None
 
 
     for st in strategies:
@@ -686,7 +749,7 @@ def run_cuda(args):
                        "ranks_per_step": n_ranks, "flops_per_step": flops_step,
                        "subset": None if (args.strategy is None and args.rank is None)
                        else {"strategy": args.strategy, "rank": args.rank},
-                       "l2": "flushed between timed steps (256 MB write, untimed)",
+                       "l2": "flushed between timed steps (256 MB write, untimed); K/V and Q exceed L2",
                        "launch": "one CUDA graph per step (the library calls, captured once)",
                        "parallelism": f"replicas{world}"},
             "per_strategy": per_strategy,
@@ -698,14 +761,18 @@ def run_cuda(args):
             "dcs_one_vs_two_launches": two,
             "backward": bwd,
             "attention_other_workloads": others,
+            "useful_pair_frac": round(sum(sum(st.pairs) for st in strategies)
+                                      / sum(sum(st.kpairs) for st in strategies), 4),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4),
+                         "frac_of_sustained_peak": round(achieved / peak_sustained, 4),
                          "traffic": measured_traffic(cfg.name, args.strategy is not None or args.rank is not None),
                          "kernel": "attn_fwd_tc_kernel (thd_causal_attn_fwd_planned, timed per launch; the plan "
                                    "is replayed outside the events)",
                          "launch_us_mean": round(sum(med_kern) / len(med_kern) * 1e3, 3),
                          "whole_call_tflops": round(call_tflops, 3),
-                         "peak_source": f"{peak_src} bf16_tflops (burst)"},
+                         "peak_source": f"{peak_src} bf16_tflops (burst); sustained = {peak_src} "
+                                        "bf16_tflops_sustained"},
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4),
                     "timing": f"wall clock, median of {e2e_steps} steps after 2 untimed ones; uploads per "
@@ -723,19 +790,43 @@ def run_cuda(args):
 # ----------------------------------------------------------------------------
 # the float64 oracle on host cores
 # ----------------------------------------------------------------------------
-def _oracle_rank(cfg, strategy, r, cache):
-    from oracle import attention as A
-    from oracle import partition as P
-    if strategy not in cache:
-        cache[strategy] = W.make_attn_inputs(cfg, strategy)
-    inp = cache[strategy]
-    lay = inp.layout
-    t0 = time.perf_counter()
-    idx = np.asarray(P.partition_index(strategy, lay.cu_seqlens_padded.tolist(), cfg.cp, r), dtype=np.int64)
-    q_loc = inp.q[torch.from_numpy(idx)]
-    A.attention_fwd(q_loc, inp.k, inp.v, lay.cu_seqlens, lay.cu_seqlens_padded, idx)
-    dt = time.perf_counter() - t0
-    return dt, 4.0 * cfg.d * cfg.hq * rank_pairs(idx, lay)
+class OracleSlices:
+    """The oracle's inputs and partitions of one workload, built once (not
+    timed), and the oracle's forward of one rank slice, timed: the partition
+    index, the gather of the Q slice and the attention of all its rows, or of
+    ``n_rows`` evenly spaced rows."""
+
+    def __init__(self, cfg):
+        from oracle import partition as P
+        self.cfg = cfg
+        self.inputs = {s: W.make_attn_inputs(cfg, s) for s in cfg.strategies}
+        self.pairs = {}
+        for s in cfg.strategies:
+            lay = self.inputs[s].layout
+            for r in range(cfg.cp):
+                idx = np.asarray(P.partition_index(s, lay.cu_seqlens_padded.tolist(), cfg.cp, r), dtype=np.int64)
+                self.pairs[(s, r)] = rank_pairs(idx, lay)
+
+    def flops(self, key) -> float:
+        return 4.0 * self.cfg.d * self.cfg.hq * self.pairs[key]
+
+    def run(self, strategy, r, n_rows=None):
+        """Returns (seconds, unmasked-pair FLOPs computed, rows computed)."""
+        from oracle import attention as A
+        from oracle import partition as P
+        cfg = self.cfg
+        inp = self.inputs[strategy]
+        lay = inp.layout
+        t0 = time.perf_counter()
+        idx = np.asarray(P.partition_index(strategy, lay.cu_seqlens_padded.tolist(), cfg.cp, r), dtype=np.int64)
+        q_loc = inp.q[torch.from_numpy(idx)]
+        rows = None
+        if n_rows is not None and n_rows < len(idx):
+            rows = np.unique(np.linspace(0, len(idx) - 1, max(int(n_rows), 1)).round().astype(np.int64))
+        A.attention_fwd(q_loc, inp.k, inp.v, lay.cu_seqlens, lay.cu_seqlens_padded, idx, rows=rows)
+        dt = time.perf_counter() - t0
+        sel = idx if rows is None else idx[rows]
+        return dt, 4.0 * cfg.d * cfg.hq * rank_pairs(sel, lay), len(sel)
 
 
 def cpu_model() -> str:
@@ -752,24 +843,49 @@ def cpu_model() -> str:
 
 
 def cpu_baseline(cfg, seconds):
-    """Time the oracle as it stands on a bounded sample: whole rank slices in
-    (strategy, rank) order until about ``seconds`` of CPU work."""
-    cache = {}
+    """Time the oracle as it stands on a bounded sample of the workload (about
+    ``seconds`` of CPU work): whole rank slices from the cheapest up while
+    they fit, then evenly spaced rows of each strategy's costliest slice not
+    yet timed, sized by the rate measured so far to fill the rest."""
+    orc = OracleSlices(cfg)
+    order = sorted(orc.pairs, key=lambda k: (orc.pairs[k], k))
     t_sum, f_sum, done = 0.0, 0.0, []
-    for s in cfg.strategies:
-        for r in range(cfg.cp):
-            dt, f = _oracle_rank(cfg, s, r, cache)
-            t_sum += dt
-            f_sum += f
-            done.append(f"{s}:{r}")
-            if t_sum >= seconds:
-                break
+    timed = set()
+    for key in order:
+        if t_sum > 0 and orc.flops(key) / (f_sum / t_sum) > seconds - t_sum:
+            break
+        dt, f, _ = orc.run(*key)
+        t_sum, f_sum = t_sum + dt, f_sum + f
+        done.append(f"{key[0]}:{key[1]} (all rows)")
+        timed.add(key)
         if t_sum >= seconds:
             break
+    rest = [k for k in order if k not in timed]
+    costliest = []
+    for s in cfg.strategies:
+        ks = [k for k in rest if k[0] == s]
+        if ks:
+            costliest.append(ks[-1])
+    for i, key in enumerate(costliest):
+        left = seconds - t_sum
+        if left <= 0.5:
+            break
+        share = left / (len(costliest) - i)
+        t_local = W.layout_for(cfg, key[0]).T // cfg.cp
+        n = max(16, int(t_local * share * (f_sum / t_sum) / orc.flops(key)))
+        dt, f, rows = orc.run(*key, n_rows=n)
+        t_sum, f_sum = t_sum + dt, f_sum + f
+        done.append(f"{key[0]}:{key[1]} ({rows} evenly spaced rows of {W.layout_for(cfg, key[0]).T // cfg.cp})")
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": round(f_sum / t_sum / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "cpu_model": cpu_model(),
-            "sample": f"{cfg.name}: rank slices {','.join(done)} (all heads, float64 numpy), {t_sum:.1f} s"}
+            "sample": f"{cfg.name}: rank slices {', '.join(done)}; all heads, float64 numpy, partition + Q gather "
+                      f"+ attention timed, {t_sum:.1f} s"}
+
+
+# FLOPs of oracle work per reference-arm step: a whole rank slice when it is
+# smaller, else this many FLOPs' worth of its rows (evenly spaced).
+REFERENCE_STEP_FLOPS = 4e10
 
 
 def run_reference(args):
@@ -777,18 +893,28 @@ def run_reference(args):
     if rank != 0:
         return
     cfg = W.CONFIG_BY_NAME[args.workload]
+    orc = OracleSlices(cfg)
     order = [(s, r) for s in cfg.strategies for r in range(cfg.cp)]
-    cache = {}
+    t_local = {s: W.layout_for(cfg, s).T // cfg.cp for s in cfg.strategies}
+
+    def one(i):
+        key = order[i % len(order)]
+        f_slice = orc.flops(key)
+        n = None if f_slice <= REFERENCE_STEP_FLOPS else max(16, int(t_local[key[0]] * REFERENCE_STEP_FLOPS / f_slice))
+        return orc.run(*key, n_rows=n)
+
     for i in range(args.warmup):
-        _oracle_rank(cfg, *order[i % len(order)], cache)
+        one(i)
     t_sum, f_sum = 0.0, 0.0
     for i in range(args.steps):
-        dt, f = _oracle_rank(cfg, *order[i % len(order)], cache)
+        dt, f, _ = one(i)
         t_sum += dt
         f_sum += f
     value = f_sum / t_sum / 1e12
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    sample = f"{cfg.name}: one rank slice per step, cycling {len(order)} (strategy, rank) slices, float64 numpy"
+    sample = (f"{cfg.name}: one rank slice per step, cycling the {len(order)} (strategy, rank) slices; a slice of "
+              f"more than {REFERENCE_STEP_FLOPS:.0e} unmasked-pair FLOP is cut to that many FLOPs' worth of evenly "
+              "spaced rows; partition + Q gather + attention in float64 numpy")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_sum / args.steps, 3),
@@ -809,7 +935,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.CONFIG_BY_NAME))
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0, help="CPU-oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the K/V restore, one-vs-two-launch, backward and other-workload measurements")

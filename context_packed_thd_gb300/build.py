@@ -54,21 +54,23 @@ def _fingerprint(extra=()) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libcpthd.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
-    stamp = os.path.join(BUILD, "fingerprint")
+def build(force: bool = False, verbose: bool = False, extra_flags=(), build_dir: str = BUILD,
+          lib: str = LIB) -> str:
+    """Compile and link libcpthd.so (or, with another build_dir / lib, a
+    variant of it built with extra_flags); returns its path."""
+    os.makedirs(build_dir, exist_ok=True)
+    stamp = os.path.join(build_dir, "fingerprint")
     fp = _fingerprint(extra_flags)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == fp:
-                return LIB
+                return lib
     nvcc = _nvcc()
     flags = NVCC_FLAGS + list(extra_flags)
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -79,15 +81,26 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(fp)
-    return LIB
+    return lib
+
+
+def build_wait_test() -> str:
+    """A test-only variant of the library, built with CPTHD_WAIT_TEST: its
+    pipeline waits give up after 5 ms instead of 2 s, and the attention
+    forward's data-relay warp withholds its arrivals for key block 1, so every
+    CTA with more than one key block must leave through the timeout path
+    (CPTHD_ERR_TIMEOUT). Kept apart from libcpthd.so under _build/; only the
+    timeout test loads it."""
+    d = os.path.join(BUILD, "wait_test")
+    return build(extra_flags=("-DCPTHD_WAIT_TEST",), build_dir=d, lib=os.path.join(d, "libcpthd_wait_test.so"))
 
 
 if __name__ == "__main__":

@@ -769,23 +769,27 @@ extern "C" int thd_causal_attn_bwd(const int32_t* q_slice_idx_dev, int64_t t_loc
   const long long ntiles = (t_local + kBlockM - 1) / kBlockM;
   if (ntiles > kBwdMaxTiles) return CPTHD_ERR_UNSUPPORTED;
   if (dk_dev == nullptr || dv_dev == nullptr || (T > 0 && k_dev == nullptr)) return CPTHD_ERR_INVALID_ARG;
+  // every host check comes before the first thing queued on the stream: a
+  // call that returns an error has touched nothing
+  if (t_local > 0) {
+    if (q_slice_idx_dev == nullptr || q_dev == nullptr || v_dev == nullptr || out_dev == nullptr ||
+        dout_dev == nullptr || lse_dev == nullptr || cu_seqlens_dev == nullptr || dq_dev == nullptr ||
+        num_docs < 1 || T < 1)
+      return CPTHD_ERR_INVALID_ARG;
+    const uintptr_t align = reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(k_dev) |
+                            reinterpret_cast<uintptr_t>(v_dev) | reinterpret_cast<uintptr_t>(dout_dev) |
+                            reinterpret_cast<uintptr_t>(dq_dev) | reinterpret_cast<uintptr_t>(dk_dev) |
+                            reinterpret_cast<uintptr_t>(dv_dev);
+    if (align & 15) return CPTHD_ERR_UNSUPPORTED;
+    if (workspace_dev == nullptr || workspace_bytes < bwd_workspace_bytes(ntiles, Hq) ||
+        (reinterpret_cast<uintptr_t>(workspace_dev) & 255))
+      return CPTHD_ERR_WORKSPACE;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // this rank's dK/dV contribution: keys its queries do not reach stay zero
   CPTHD_TRY_CUDA(cudaMemsetAsync(dk_dev, 0, sizeof(float) * static_cast<size_t>(T) * Hkv * d, s));
   CPTHD_TRY_CUDA(cudaMemsetAsync(dv_dev, 0, sizeof(float) * static_cast<size_t>(T) * Hkv * d, s));
   if (t_local == 0) return CPTHD_OK;
-  if (q_slice_idx_dev == nullptr || q_dev == nullptr || v_dev == nullptr || out_dev == nullptr ||
-      dout_dev == nullptr || lse_dev == nullptr || cu_seqlens_dev == nullptr || dq_dev == nullptr || num_docs < 1 ||
-      T < 1)
-    return CPTHD_ERR_INVALID_ARG;
-  const uintptr_t align = reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(k_dev) |
-                          reinterpret_cast<uintptr_t>(v_dev) | reinterpret_cast<uintptr_t>(dout_dev) |
-                          reinterpret_cast<uintptr_t>(dq_dev) | reinterpret_cast<uintptr_t>(dk_dev) |
-                          reinterpret_cast<uintptr_t>(dv_dev);
-  if (align & 15) return CPTHD_ERR_UNSUPPORTED;
-  if (workspace_dev == nullptr || workspace_bytes < bwd_workspace_bytes(ntiles, Hq) ||
-      (reinterpret_cast<uintptr_t>(workspace_dev) & 255))
-    return CPTHD_ERR_WORKSPACE;
   const int32_t* cup = cu_seqlens_padded_dev ? cu_seqlens_padded_dev : cu_seqlens_dev;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
   AttnWorkspace ws = carve_workspace(workspace_dev, ntiles, kBlockM);

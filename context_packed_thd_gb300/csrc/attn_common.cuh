@@ -74,6 +74,16 @@ static inline bool make_rows_heads_map(EncodeTiledFn enc, CUtensorMap* m, const 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Host checks of the scalar shape arguments shared by the forward entry
+// points (the workspace and static-scratch forms run the same checks in the
+// same order).
+static inline int check_attn_shape(int64_t t_local, int64_t T, int num_docs, int Hq, int Hkv) {
+  if (t_local < 0 || T < 0 || T > INT32_MAX || t_local > INT32_MAX || num_docs < 0 || Hq < 1 || Hkv < 1)
+    return CPTHD_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || Hq > 65535) return CPTHD_ERR_UNSUPPORTED;
+  return CPTHD_OK;
+}
+
 // Two query tiles per CTA: two heads of one KV head when the GQA group size is
 // even, else two consecutive 128-row tiles of one head.
 static inline int group_rows_for(int Hq, int Hkv) { return ((Hq / Hkv) % 2 == 0) ? kBlockM : 2 * kBlockM; }

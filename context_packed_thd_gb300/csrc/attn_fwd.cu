@@ -299,6 +299,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, &abort_flag)) break;
         if (j + 1 < n_blocks && !mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, &abort_flag)) break;
+#ifdef CPTHD_WAIT_TEST
+        // Test build only: block 1's arrivals are withheld, so the waits for
+        // P(1) can never complete and must run out into the abort path.
+        if (j == 1) continue;
+#endif
         mbar_arrive(&p_full[0]);
         mbar_arrive(&p_full[1]);
       }
@@ -552,14 +557,6 @@ extern "C" int thd_causal_attn_workspace_size(int64_t t_local, int Hq, int Hkv, 
 }
 
 namespace cpthd {
-
-// Host checks shared by the three entry points.
-static int check_attn_shape(int64_t t_local, int64_t T, int num_docs, int Hq, int Hkv) {
-  if (t_local < 0 || T < 0 || T > INT32_MAX || t_local > INT32_MAX || num_docs < 0 || Hq < 1 || Hkv < 1)
-    return CPTHD_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0 || Hq > 65535) return CPTHD_ERR_UNSUPPORTED;
-  return CPTHD_OK;
-}
 
 static int check_workspace(int64_t t_local, int Hq, int Hkv, const void* workspace_dev, size_t workspace_bytes) {
   const int rows = group_rows_for(Hq, Hkv);

@@ -10,14 +10,17 @@
 // loaded, so the call itself allocates nothing.
 //
 // The array's name is only a host-side stand-in for the device object: host
-// code must not pass it to a kernel. The first call on each device asks the
-// runtime for the array's device address (cudaGetSymbolAddress, with that
-// device current), checks the result and caches it; every call then passes
-// that address down as the workspace of the regular entry point, which runs
-// unchanged.
+// code must not pass it to a kernel. A call asks the runtime for the array's
+// device address on the current device (cudaGetSymbolAddress, with that
+// device current), checks the result, and passes that address down as the
+// workspace of the regular entry point, which runs unchanged. The address is
+// looked up again on every call whose stream is not capturing, so a device
+// reset or another context made current is picked up; a call inside a stream
+// capture uses the address the last uncaptured call on that device found,
+// which is why the first call on a device must come before any capture.
 #include <mutex>
 
-#include "common.cuh"
+#include "attn_common.cuh"
 
 namespace cpthd {
 
@@ -32,16 +35,24 @@ constexpr int kMaxDevices = 64;
 static void* g_scratch_addr[kMaxDevices] = {};
 static std::mutex g_scratch_mutex;
 
-// Device address of g_attn_scratch on the current device (looked up once per
-// device). Returns nullptr when the runtime cannot provide it.
-static void* static_scratch_address(int* status) {
+// Device address of g_attn_scratch on the current device. Outside a stream
+// capture it is looked up afresh (and remembered for the device); inside one
+// the remembered address is used. Returns nullptr (and a status) when the
+// runtime cannot provide it, or when a capture comes before any uncaptured
+// call on this device.
+static void* static_scratch_address(cudaStream_t stream, int* status) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     *status = CPTHD_ERR_CUDA;
     return nullptr;
   }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    *status = CPTHD_ERR_CUDA;
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_attn_scratch) != cudaSuccess || ptr == nullptr) {
       *status = CPTHD_ERR_CUDA;
@@ -49,7 +60,7 @@ static void* static_scratch_address(int* status) {
     }
     g_scratch_addr[dev] = ptr;
   }
-  *status = CPTHD_OK;
+  *status = (g_scratch_addr[dev] != nullptr) ? CPTHD_OK : CPTHD_ERR_CUDA;
   return g_scratch_addr[dev];
 }
 
@@ -61,18 +72,24 @@ extern "C" int thd_causal_attn_fwd_static_scratch(const int32_t* q_slice_idx_dev
                                                   const int32_t* cu_seqlens_padded_dev, int num_docs, int Hq,
                                                   int Hkv, int d, float softmax_scale, void* out_dev,
                                                   float* lse_dev, int32_t* err_dev, cpthd_stream_t stream) {
-  size_t need = 0;
-  const int st = thd_causal_attn_workspace_size(t_local, Hq, Hkv, d, &need);
+  using namespace cpthd;
+  // the same host checks, in the same order, as thd_causal_attn_fwd; then
+  // the scratch limit
+  int st = check_attn_shape(t_local, T, num_docs, Hq, Hkv);
   if (st != CPTHD_OK) return st;
-  if (need > cpthd::kStaticScratchBytes) return CPTHD_ERR_SCRATCH_LIMIT;
+  if (d != 64 && d != 128) return CPTHD_ERR_UNSUPPORTED;
   if (t_local == 0) return CPTHD_OK;
+  size_t need = 0;
+  st = thd_causal_attn_workspace_size(t_local, Hq, Hkv, d, &need);
+  if (st != CPTHD_OK) return st;
+  if (need > kStaticScratchBytes) return CPTHD_ERR_SCRATCH_LIMIT;
   int status = CPTHD_OK;
-  void* scratch = cpthd::static_scratch_address(&status);
+  void* scratch = static_scratch_address(reinterpret_cast<cudaStream_t>(stream), &status);
   if (scratch == nullptr) return status;
   // The regular entry point's metadata kernel writes every scratch byte the
   // attention kernel later reads, so the previous call's contents need no
   // clearing.
   return thd_causal_attn_fwd(q_slice_idx_dev, t_local, q_dev, k_dev, v_dev, T, cu_seqlens_dev,
                              cu_seqlens_padded_dev, num_docs, Hq, Hkv, d, softmax_scale, out_dev, lse_dev, scratch,
-                             cpthd::kStaticScratchBytes, err_dev, stream);
+                             kStaticScratchBytes, err_dev, stream);
 }

@@ -127,7 +127,9 @@ extern "C" int cp_partition_index(int strategy, const int32_t* cu_seqlens_padded
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool dcs = (strategy == CPTHD_DUAL_CHUNK_SWAP);
   const long long work = total > num_docs + 1 ? total : num_docs + 1;
-  const int grid = cpthd::grid_for(work, 256, 152 * 16);
+  const int sms = cpthd::sm_count();
+  if (sms < 1) return CPTHD_ERR_CUDA;
+  const int grid = cpthd::grid_for(work, 256, sms * 16);
   auto kernel = dcs ? cpthd::dual_chunk_swap_index_kernel
                     : (strategy == CPTHD_NO_LOAD_BALANCE ? cpthd::no_load_balance_index_kernel
                                                          : cpthd::packed_mirrored_index_kernel);
@@ -146,7 +148,9 @@ extern "C" int cp_restore_index(int strategy, const int32_t* cu_seqlens_padded_d
   if (T > 0 && (restore_idx_out_dev == nullptr || num_docs == 0)) return CPTHD_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const long long work = T > num_docs + 1 ? T : num_docs + 1;
-  CPTHD_TRY_CUDA(cpthd::launch_pdl(cpthd::restore_index_kernel, dim3(cpthd::grid_for(work, 256, 152 * 16)),
+  const int sms = cpthd::sm_count();
+  if (sms < 1) return CPTHD_ERR_CUDA;
+  CPTHD_TRY_CUDA(cpthd::launch_pdl(cpthd::restore_index_kernel, dim3(cpthd::grid_for(work, 256, sms * 16)),
                                    dim3(256), 0, s, strategy, cu_seqlens_padded_dev, num_docs,
                                    static_cast<long long>(T), cp_size, restore_idx_out_dev, err_dev));
   return CPTHD_OK;

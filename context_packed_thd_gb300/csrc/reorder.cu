@@ -175,7 +175,7 @@ static int launch_reorder(int n, const void* const* src, void* const* dst, const
   // Wide rows: a warp per unit (32 x kUnroll vectors) for large gathers, a
   // warp per row for small ones (the warps then share the rows' units); a
   // thread per vector for narrow rows; capped at 8 resident 256-thread
-  // blocks on each of the 152 SMs. Sized by units, the small Q gather of a
+  // blocks on each SM of the device. Sized by units, the small Q gather of a
   // rank slice held more SMs for longer and the attention launch after it
   // started later; sized by rows, the large activation gathers left SMs
   // idle (82% vs 79% of the copy bandwidth on [131072, 8192] bf16).
@@ -189,7 +189,9 @@ static int launch_reorder(int n, const void* const* src, void* const* dst, const
     const long long w = (vpr >= 32) ? n_rows * upr * 32 : n_rows * vpr;
     work = w > work ? w : work;
   }
-  const int grid = grid_for(work, 256, 152 * 8);
+  const int sms = sm_count();
+  if (sms < 1) return CPTHD_ERR_CUDA;
+  const int grid = grid_for(work, 256, sms * 8);
   dim3 g(grid, n);
   CPTHD_TRY_CUDA(launch_pdl(reorder_kernel, g, dim3(256), 0, s, b, static_cast<long long>(src_rows), ig,
                             static_cast<long long>(n_rows), idx_out, err));

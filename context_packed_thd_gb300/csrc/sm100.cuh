@@ -16,7 +16,13 @@
 namespace cpthd {
 namespace sm100 {
 
+#ifdef CPTHD_WAIT_TEST
+// Test build only (never the shipped library): 5 ms, so that a wait that
+// cannot complete gives up quickly.
+constexpr unsigned long long kWaitLimitNs = 5000000ull;
+#else
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -273,8 +273,13 @@ CPTHD_API int thd_causal_attn_bwd(const int32_t* q_slice_idx_dev, int64_t t_loca
  * process exits; the call allocates nothing. That is enough for slices of at
  * least 250,000 query rows; a larger slice is rejected with
  * CPTHD_ERR_SCRATCH_LIMIT before anything is launched.
- * The first call on a device looks up the array's device address for that
- * device (with it current); make that first call before any stream capture.
+ * Every call whose stream is not capturing looks up the array's device
+ * address on the current device (so a device reset, or another context
+ * made current, is picked up by the next such call); a call made during a
+ * stream capture reuses the address the last uncaptured call on that device
+ * found, so make the first call on each device before any stream capture.
+ * Host checks run in the order of thd_causal_attn_fwd (shape, head dim,
+ * t_local == 0 returns CPTHD_OK), then the scratch limit.
  * All calls share the one array: calls that overlap on the GPU (different
  * streams without ordering between them) race and corrupt each other's
  * results. Nothing in the array needs clearing between calls.

@@ -154,6 +154,15 @@ def test_host_validation_restore_multi_reorder_backward(cp):
     assert bw(*args(4, 3, 2, 64, p)) == -3
     assert bw(*args(2048 * 128 + 1, 2, 2, 64, p)) == -3
     assert bw(*args(4, 2, 2, 64, None)) == -1
+    # every host check returns before dK/dV are zeroed: a misaligned pointer or
+    # a missing workspace is reported with nothing queued on the stream (the
+    # fake pointers here would fault if a memset were queued on them)
+    mis = lambda t_local, q, ws, nbytes: (p, t_local, q, p, p, p, p, p, 8, p, None, 1, 2, 2, 64, 0.0, p, p, p, ws,
+                                          nbytes, None, None)
+    assert bw(*mis(4, vp(264), p, 1 << 20)) == -3
+    assert bw(*mis(4, p, None, 0, )) == -4
+    assert bw(*mis(4, p, vp(260), 1 << 20)) == -4
+    assert bw(*mis(4, p, p, 16)) == -4
     size = ctypes.c_size_t(0)
     assert L.thd_causal_attn_bwd_workspace_size(-1, 2, 2, 64, ctypes.byref(size)) == -1
     assert L.thd_causal_attn_bwd_workspace_size(256, 2, 2, 64, ctypes.byref(size)) == 0 and size.value > 0

@@ -8,7 +8,10 @@ Tolerances: max |out - ref| <= 1e-2 + 1e-2 |ref| (bf16 output) and
 * T = 32768 lognormal GQA 32/8, 48 padded docs GQA 32/8 and the single
   131072-token document: every rank under the strategies the workload names,
   at full size, on sampled rows (first/last rows, rows at chunk and tile
-  boundaries, random rows) that the oracle computes one by one.
+  boundaries, random rows) that the oracle computes one by one; and every
+  row of one rank of the lognormal (both strategies) and padded packs.
+* DualChunkSwap as two launches per rank (one per owned chunk, the pages'
+  two attention steps): every row against the oracle and the one launch.
 * edge cases: ragged tails, empty and one-token documents, pad rows, GQA
   group sizes, custom scale, arbitrary row order of the query slice, and
   device-checked malformed offsets.
@@ -372,3 +375,70 @@ def test_malformed_offsets_recorded():
     cp.thd_causal_attn_fwd(idx, d.q, d.k, d.v, torch.tensor([0, 40, 60], dtype=torch.int32, device=dev), short,
                            err=err)
     assert err.cpu().tolist()[0] in (-6, -7)
+
+
+def _dcs_halves(lay, cpsize):
+    """Local rows of a DualChunkSwap rank's first owned chunk of every
+    document, and of its second: the two attention steps per rank of the
+    pages' design (one per owned chunk)."""
+    lcu = lay.cu_seqlens_padded.astype(np.int64) // cpsize
+    halves = [[], []]
+    for j in range(lay.num_docs):
+        c = (lcu[j + 1] - lcu[j]) // 2
+        halves[0].append(np.arange(lcu[j], lcu[j] + c))
+        halves[1].append(np.arange(lcu[j] + c, lcu[j + 1]))
+    return [np.concatenate(h).astype(np.int64) for h in halves]
+
+
+@pytest.mark.parametrize("name,ranks", [("t8192_mha16", [0, 1, 2, 3]), ("t32768_lognormal_gqa32x8", [6]),
+                                        ("padded48_gqa32x8", [1])])
+def test_dcs_two_launches_match_oracle(name, ranks):
+    """A DualChunkSwap rank run as two launches, one per owned chunk (each
+    launch gets that chunk's rows of every document and their slots): every
+    row of both launches against the oracle, and against the one-launch
+    result of the same rank, with the device checks clean."""
+    dev = cuda_or_skip(); cp = load_lib()
+    cfg = W.CONFIG_BY_NAME[name]
+    inp = W.make_attn_inputs(cfg, "dcs")
+    d = DevInputs(inp, dev)
+    lay = inp.layout
+    halves = _dcs_halves(lay, cfg.cp)
+    err = new_err(dev)
+    for r in ranks:
+        idx, out1, lse1 = _run_rank(cp, d, "dcs", cfg.cp, r, err)
+        ref_idx = np.asarray(P.partition_index("dcs", lay.cu_seqlens_padded.tolist(), cfg.cp, r), dtype=np.int64)
+        assert np.array_equal(np.sort(np.concatenate(halves)), np.arange(len(ref_idx)))
+        q_loc = cp.cp_reorder(d.q, idx, err=err)
+        for h, rows in enumerate(halves):
+            rows_t = torch.from_numpy(rows).to(dev)
+            idx_h = idx[rows_t].contiguous()
+            out_h, lse_h = cp.thd_causal_attn_fwd(idx_h, q_loc[rows_t].contiguous(), d.k, d.v, d.cu, d.cup, err=err)
+            ro, rl = A.attention_fwd(inp.q[torch.from_numpy(ref_idx[rows])], inp.k, inp.v, lay.cu_seqlens,
+                                     lay.cu_seqlens_padded, ref_idx[rows])
+            assert_attn_matches(out_h, lse_h, ro, rl, f"{name}/rank{r}/launch{h}")
+            assert_attn_matches(out_h, lse_h, out1[rows_t].float().cpu().numpy(),
+                                lse1[:, rows_t].cpu().numpy().astype(np.float64), f"{name}/rank{r}/launch{h} vs one")
+    torch.cuda.synchronize()
+    assert err.cpu().tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("name,strategy,rank", [
+    ("t32768_lognormal_gqa32x8", "dcs", 5), ("t32768_lognormal_gqa32x8", "nlb", 4),
+    ("padded48_gqa32x8", "dcs", 2),
+])
+def test_full_size_rank_every_row(name, strategy, rank):
+    """Every row of one full-size rank slice against the oracle (the other
+    ranks of these workloads are checked on sampled rows above)."""
+    dev = cuda_or_skip(); cp = load_lib()
+    cfg = W.CONFIG_BY_NAME[name]
+    inp = W.make_attn_inputs(cfg, strategy)
+    d = DevInputs(inp, dev)
+    lay = inp.layout
+    err = new_err(dev)
+    idx, out, lse = _run_rank(cp, d, strategy, cfg.cp, rank, err)
+    ref_idx = np.asarray(P.partition_index(strategy, lay.cu_seqlens_padded.tolist(), cfg.cp, rank), dtype=np.int64)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    ro, rl = A.attention_fwd(inp.q[torch.from_numpy(ref_idx)], inp.k, inp.v, lay.cu_seqlens, lay.cu_seqlens_padded,
+                             ref_idx)
+    assert_attn_matches(out, lse, ro, rl, f"{name}/{strategy}/rank{rank}")
+    assert err.cpu().tolist() == [0, 0]

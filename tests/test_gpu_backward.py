@@ -1,11 +1,19 @@
 """GPU attention backward (dQ, dK, dV) vs the float64 oracle.
 
-The GPU backward rounds P and dS to bf16 for the tensor cores and uses the
-forward's bf16 output for rowsum(dO * O); its results are compared per
-tensor with a norm-relative bound: max |x - ref| <= BWD_TOL * max |ref| (the
-bf16 rounding of P and dS is 2^-9 relative, and sums over many keys of mixed
-sign keep that order relative to the largest entries), plus pad / untouched
-entries exactly zero.
+Tolerance, element by element: |x - ref| <= BWD_C * M, where M is the
+per-element error scale of tests/gpu_common.bwd_term_magnitudes: the sum of
+the magnitudes of the terms that make up that gradient entry, weighted by the
+bf16 roundings the GPU applies (P, dS, and the forward's output inside
+D = rowsum(dO * O), each at most 2^-8 relative: bf16 keeps 8 significant
+bits). The worst case of those roundings is 2^-7 M; BWD_C = 2^-6 leaves a
+factor 2 for the fp32 accumulations and ex2.approx (orders of magnitude
+smaller). Pad query rows of dQ and keys no
+query of the slice reaches (dK, dV) must be exactly zero.
+
+Cases: every element of the tiny, T=8192 and lognormal slices listed below,
+edge cases, seeded random packs, and one query head (all its dQ rows and all
+its dK/dV keys) of the 131072-token DualChunkSwap rank 3 computed with all
+eight heads, the slice the backward is benchmarked on.
 """
 import numpy as np
 import pytest
@@ -14,10 +22,10 @@ import torch
 from oracle import attention as A
 from oracle import partition as P
 import workloads as W
-from gpu_common import cuda_or_skip, load_lib, new_err
+from gpu_common import bwd_term_magnitudes, cuda_or_skip, load_lib, new_err
 
 pytestmark = pytest.mark.gpu
-BWD_TOL = 2e-2
+BWD_C = 2.0 ** -6
 
 
 def _rank_bwd(cp, inp, strategy, cpsize, r, dev, dout_phys, err):
@@ -45,15 +53,36 @@ def _structural_zero(lay, idx):
     return ~valid, ~reached
 
 
-def _check(name, got, ref, zero_rows):
-    scale = np.abs(ref).max()
-    err = np.abs(got - ref).max()
-    rel = err / scale if scale > 0 else err
-    cos = float((got * ref).sum() / (np.linalg.norm(got) * np.linalg.norm(ref) + 1e-30))
+def _check(name, got, ref, mag, zero_rows):
+    """Element-wise |got - ref| <= BWD_C * mag; exact zeros where required.
+    Returns the largest |got - ref| / (BWD_C * mag) (1.0 = at the bound)."""
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
-    assert rel <= BWD_TOL, f"{name}: max|d| / max|ref| = {rel:.3e} (cos {cos:.6f})"
     assert np.all(got[zero_rows] == 0), f"{name}: nonzero in rows that must be zero"
-    return rel
+    err = np.abs(got - ref)
+    bound = BWD_C * mag
+    bad = err > bound
+    scale = np.abs(ref).max()
+    assert not bad.any(), (f"{name}: {int(bad.sum())} entries beyond the element bound; worst excess "
+                           f"{(err - bound).max():.3e}, max|d| / max|ref| = {err.max() / max(scale, 1e-30):.3e}")
+    nz = bound > 0
+    return float((err[nz] / bound[nz]).max()) if nz.any() else 0.0
+
+
+def _compare(label, cp_out, q_loc, k, v, lay, idx, dout, heads=None):
+    """Oracle gradients and error scales of the slice (optionally of some
+    heads only, MHA), checked against the GPU's."""
+    dq, dk, dv = cp_out
+    if heads is not None:
+        sel = list(heads)
+        q_loc, k, v, dout = q_loc[:, sel], k[:, sel], v[:, sel], dout[:, sel]
+        dq, dk, dv = dq[:, sel], dk[:, sel], dv[:, sel]
+    ref = A.attention_bwd(q_loc, k, v, lay.cu_seqlens, lay.cu_seqlens_padded, idx, dout)
+    mag = bwd_term_magnitudes(q_loc, k, v, lay.cu_seqlens, lay.cu_seqlens_padded, idx, dout)
+    zq, zk = _structural_zero(lay, idx)
+    ratios = [_check(f"{label}/{n}", g, e, m, z)
+              for n, g, e, m, z in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, mag, (zq, zk, zk))]
+    print(f"{label}: max |d| / bound  dq {ratios[0]:.3f} dk {ratios[1]:.3f} dv {ratios[2]:.3f}")
+    return ratios
 
 
 @pytest.mark.parametrize("name,strategy,ranks", [
@@ -70,12 +99,8 @@ def test_backward_matches_oracle(name, strategy, ranks):
     err = new_err(dev)
     for r in ranks:
         idx, dq, dk, dv, dout = _rank_bwd(cp, inp, strategy, cfg.cp, r, dev, dout_phys, err)
-        ref = A.attention_bwd(inp.q[torch.from_numpy(idx)], inp.k, inp.v, lay.cu_seqlens, lay.cu_seqlens_padded,
-                              idx, dout)
-        zq, zk = _structural_zero(lay, idx)
-        rels = [_check(f"{name}/{strategy}/r{r}/{n}", g, e, z)
-                for n, g, e, z in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, (zq, zk, zk))]
-        print(f"{name}/{strategy}/rank{r}: max|d|/max|ref| dq {rels[0]:.2e} dk {rels[1]:.2e} dv {rels[2]:.2e}")
+        _compare(f"{name}/{strategy}/rank{r}", (dq, dk, dv), inp.q[torch.from_numpy(idx)], inp.k, inp.v, lay, idx,
+                 dout)
     assert err.cpu().tolist() == [0, 0]
 
 
@@ -103,10 +128,7 @@ def test_backward_edge_cases(case):
             continue
         for r in range(case["cp"]):
             idx, dq, dk, dv, dout = _rank_bwd(cp, inp, s, case["cp"], r, dev, dout_phys, err)
-            ref = A.attention_bwd(q[torch.from_numpy(idx)], k, v, lay.cu_seqlens, lay.cu_seqlens_padded, idx, dout)
-            zq, zk = _structural_zero(lay, idx)
-            for n, g, e, z in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, (zq, zk, zk)):
-                _check(f"{case}/{s}/r{r}/{n}", g, e, z)
+            _compare(f"{case}/{s}/r{r}", (dq, dk, dv), q[torch.from_numpy(idx)], k, v, lay, idx, dout)
     assert err.cpu().tolist() == [0, 0]
 
 
@@ -136,8 +158,24 @@ def test_backward_random_packs(seed):
     for s in ("dcs", "nlb"):
         for r in range(cpsize):
             idx, dq, dk, dv, dout = _rank_bwd(cp, inp, s, cpsize, r, dev, dout_phys, err)
-            ref = A.attention_bwd(q[torch.from_numpy(idx)], k, v, lay.cu_seqlens, lay.cu_seqlens_padded, idx, dout)
-            zq, zk = _structural_zero(lay, idx)
-            for n, g, e, z in zip(("dq", "dk", "dv"), (dq, dk, dv), ref, (zq, zk, zk)):
-                _check(f"seed {seed}/{s}/r{r}/{n}", g, e, z)
+            _compare(f"seed {seed}/{s}/r{r}", (dq, dk, dv), q[torch.from_numpy(idx)], k, v, lay, idx, dout)
     assert err.cpu().tolist() == [0, 0]
+
+
+def test_backward_long_context_rank_one_head():
+    """The benchmarked slice: rank 3 of the 131072-token document under
+    DualChunkSwap (cp_size 16), run on the GPU with all eight heads. With
+    Hq = Hkv the heads are independent, so head 0's dQ (all 8192 rows) and
+    dK/dV (all 131072 keys) are checked against the oracle run on head 0's
+    inputs alone; the dK/dV pass's key tiles here collect up to 64 query
+    tiles each."""
+    dev = cuda_or_skip(); cp = load_lib()
+    cfg = W.CONFIG_BY_NAME["long131072_h8"]
+    inp = W.make_attn_inputs(cfg, "dcs")
+    lay = inp.layout
+    dout_phys = W.randn_bf16(cfg.seed, 6, (lay.T, cfg.hq, cfg.d))
+    err = new_err(dev)
+    idx, dq, dk, dv, dout = _rank_bwd(cp, inp, "dcs", cfg.cp, 3, dev, dout_phys, err)
+    assert err.cpu().tolist() == [0, 0]
+    _compare("long131072_h8/dcs/rank3/head0", (dq, dk, dv), inp.q[torch.from_numpy(idx)], inp.k, inp.v, lay, idx,
+             dout, heads=[0])

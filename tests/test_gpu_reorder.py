@@ -57,29 +57,25 @@ def test_ids_reorder_multi(cfg):
 
 @pytest.mark.parametrize("name", ["padded48_gqa32x8", "long131072_h8"])
 def test_activation_reorder_full_size(name):
-    """[T, 4096] / [T, 8192] bf16 activations at full size for every rank;
-    rows are checked on a sample drawn per rank (every row's bytes cannot be
-    shipped to the host cheaply), plus a device-side checksum of all rows."""
+    """[T, 4096] / [T, 8192] bf16 activations at full size for every rank:
+    every row of the library's gather equals, bit for bit (compared on the
+    device as int16 bit patterns), the source rows that the oracle's index
+    list names, gathered by torch's index_select."""
     dev = cuda_or_skip(); cp = load_lib()
     cfg = W.CONFIG_BY_NAME[name]
     s = cfg.strategies[0]
     lay = W.layout_for(cfg, s)
     act = W.make_activations(cfg.seed, lay.T, cfg.act_width, device="cuda:0")
+    bits = act.view(torch.int16)
     cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
-    rng = np.random.default_rng(cfg.seed)
     err = new_err(dev)
     out = None
     for r in range(cfg.cp):
         ref_idx = np.asarray(P.partition_index(s, lay.cu_seqlens_padded.tolist(), cfg.cp, r), dtype=np.int64)
         idx = cp.cp_partition_index(s, cup, lay.T, cfg.cp, r, err=err)
         out = cp.cp_reorder(act, idx, out=out, err=err)
-        rows = np.unique(np.concatenate([[0, len(ref_idx) - 1], rng.integers(0, len(ref_idx), 64)]))
-        got = out[torch.from_numpy(rows).to(dev)].view(torch.int16).cpu().numpy()
-        src_rows = act[torch.from_numpy(ref_idx[rows]).to(dev)].view(torch.int16).cpu().numpy()
-        assert got.tobytes() == src_rows.tobytes()
-        # every row: sum of int16 bit patterns per row must match
-        want = act.view(torch.int16)[torch.from_numpy(ref_idx).to(dev)].to(torch.int64).sum(dim=1)
-        assert torch.equal(out.view(torch.int16).to(torch.int64).sum(dim=1), want)
+        want = torch.index_select(bits, 0, torch.from_numpy(ref_idx).to(dev))
+        assert torch.equal(out.view(torch.int16), want), f"{name}: rank {r} differs"
     assert err.cpu().tolist() == [0, 0]
 
 

@@ -6,19 +6,18 @@ caller workspace.
 
 The GPU test calls it twice in a row through the C ABI, on two different
 slices (the second call finds the first call's leftovers in the shared
-array), and checks each result against the regular entry point's under the
-same tolerances as the other attention tests. This file sorts last so that a
+array), and checks that each result equals the regular entry point's bit for
+bit (both run the same kernels). This file sorts last so that a
 run stopping at the first failure has already run every other test; it also
 passes on its own in a fresh process.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 import workloads as W
-from gpu_common import LSE_ATOL, OUT_ATOL, OUT_RTOL, cuda_or_skip, load_lib, new_err
+from gpu_common import cuda_or_skip, load_lib, new_err
 
 SCRATCH_LIMIT = -10
 
@@ -52,6 +51,29 @@ def test_static_scratch_limit_rejected_on_host():
     assert "scratch" in cp.cpthd_status_string(rc)
 
 
+def test_static_scratch_host_checks_match_workspace_entry_point():
+    """The same host checks, in the same order, as thd_causal_attn_fwd: shape
+    arguments first (also for an empty slice), then the head dim, then the
+    scratch limit. Fake pointers: every call here returns before a launch."""
+    cp = load_lib()
+    f = cp.lib.thd_causal_attn_fwd_static_scratch
+    g = cp.lib.thd_causal_attn_fwd
+    p = ctypes.c_void_p(256)
+
+    def both(t_local, T, num_docs, hq, hkv, d):
+        a = f(p, t_local, p, p, p, T, p, None, num_docs, hq, hkv, d, 0.0, p, p, None, None)
+        b = g(p, t_local, p, p, p, T, p, None, num_docs, hq, hkv, d, 0.0, p, p, None, 0, None, None)
+        return a, b
+
+    assert both(0, -1, 1, 2, 2, 64) == (-1, -1)             # negative T, empty slice
+    assert both(0, 8, -1, 2, 2, 64) == (-1, -1)             # negative document count
+    assert both(0, 8, 1, 65536 * 2, 2, 64) == (-3, -3)     # too many query heads
+    assert both(4, 8, 1, 3, 2, 64) == (-3, -3)              # GQA mismatch
+    assert both(4, 8, 1, 2, 2, 96) == (-3, -3)              # head dim
+    assert both(2 ** 31, 2 ** 31 - 1, 1, 2, 2, 64) == (-1, -1)  # t_local beyond int32: invalid, not a scratch limit
+    assert both(0, 8, 1, 2, 2, 64) == (0, 0)                # empty slice: nothing to do
+
+
 @pytest.mark.gpu
 def test_static_scratch_matches_workspace_entry_point():
     dev = cuda_or_skip()
@@ -70,9 +92,7 @@ def test_static_scratch_matches_workspace_entry_point():
         assert rc == 0, cp.cpthd_status_string(rc)
         torch.cuda.synchronize()
         assert err.cpu().tolist() == [0, 0]
-        o, r = out.float().cpu().numpy(), ref_out.float().cpu().numpy()
-        assert np.all(np.abs(o - r) <= OUT_ATOL + OUT_RTOL * np.abs(r)), f"{cfg.name}: output differs"
-        l, rl = lse.cpu().numpy(), ref_lse.cpu().numpy()
-        assert np.array_equal(np.isneginf(l), np.isneginf(rl))
-        fin = np.isfinite(rl)
-        assert np.all(np.abs(l[fin] - rl[fin]) <= LSE_ATOL), f"{cfg.name}: LSE differs"
+        # both entry points run the same kernels on the same inputs: the
+        # results are identical, bit for bit
+        assert torch.equal(out, ref_out), f"{cfg.name}: output differs"
+        assert torch.equal(lse, ref_lse), f"{cfg.name}: LSE differs"
