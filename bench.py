@@ -125,28 +125,64 @@ def rank_pairs(idx: np.ndarray, lay: W.Layout) -> int:
     return int((pos[valid] + 1).sum())
 
 
-def kernel_pairs(idx: np.ndarray, lay: W.Layout, hq: int, hkv: int) -> int:
-    """(query row, key) products per head that the attention kernel's
-    schedule computes for one slice: consecutive local rows form row groups
-    (128 rows when the GQA group size is even, else 256), and a group walks,
-    for every document among its real rows, the 128-key blocks from the
-    document start to its largest row slot. Useful pairs / this = the
-    fraction of the tensor work that is unmasked."""
-    rows = 128 if (hq // hkv) % 2 == 0 else 256
+def attn_tiles(idx: np.ndarray, lay: W.Layout):
+    """Query tiles (first row, rows) the attention plan cuts one slice into:
+    at every change of document, a run's rows go into 128-row tiles aligned
+    to the run's end with the remainder first, and runs shorter than a tile
+    are packed together while they fit (the library's rule, restated here
+    for reporting)."""
     cup = lay.cu_seqlens_padded.astype(np.int64)
     j = np.searchsorted(cup, idx, side="right") - 1
-    pos = idx - cup[j]
-    valid = pos < lay.lengths[j]
-    grp = np.arange(len(idx)) // rows
+    n = len(idx)
+    starts = np.r_[0, np.nonzero(np.diff(j) != 0)[0] + 1]
+    ends = np.r_[starts[1:], n]
+    tiles, cur0, curh = [], 0, 0
+    for s, e in zip(starts.tolist(), ends.tolist()):
+        head, full = (e - s) % 128, (e - s) // 128
+        if head:
+            if curh and curh + head <= 128:
+                curh += head
+            else:
+                if curh:
+                    tiles.append((cur0, curh))
+                cur0, curh = s, head
+        if full:
+            if curh:
+                tiles.append((cur0, curh))
+                curh = 0
+            tiles += [(s + head + 128 * f, 128) for f in range(full)]
+    if curh:
+        tiles.append((cur0, curh))
+    return tiles
+
+
+def kernel_pairs(idx: np.ndarray, lay: W.Layout, hq: int, hkv: int) -> int:
+    """(query row, key) products per head that the attention kernel computes
+    for one slice: every 128-row tile (two tiles per CTA item, sharing their
+    key blocks, when the GQA group size is odd; one tile under two heads
+    otherwise) walks, for every document among its group's real rows, the
+    128-key blocks from the document start to the group's largest slot in it.
+    Useful pairs / this = the fraction of the tensor work that is unmasked."""
+    head_pairs = (hq // hkv) % 2 == 0
+    cup = lay.cu_seqlens_padded.astype(np.int64)
+    jj = np.searchsorted(cup, idx, side="right") - 1
+    pos = idx - cup[jj]
+    valid = pos < lay.lengths[jj]
+    tiles = attn_tiles(idx, lay)
+    if head_pairs:
+        groups = [(a, a + h) for a, h in tiles]
+    else:  # consecutive tiles in pairs: rows from the first tile's start to the second's end
+        groups = [(tiles[i][0], sum(tiles[min(i + 1, len(tiles) - 1)])) for i in range(0, len(tiles), 2)]
+    tiles_per_group = 1 if head_pairs else 2
     total = 0
-    gv, jv, pv = grp[valid], j[valid], pos[valid]
-    if gv.size:
-        key = gv * (lay.num_docs + 1) + jv
-        order = np.lexsort((pv, key))
-        k_sorted, p_sorted = key[order], pv[order]
-        last = np.r_[k_sorted[1:] != k_sorted[:-1], True]
-        total = int(((p_sorted[last] + 128) // 128).sum())
-    return total * 128 * rows
+    for a, b in groups:
+        m = valid[a:b]
+        if not m.any():
+            continue
+        dj, dp = jj[a:b][m], pos[a:b][m]
+        for d in np.unique(dj):
+            total += (int(dp[dj == d].max()) + 128) // 128
+    return total * 128 * 128 * tiles_per_group
 
 
 # ----------------------------------------------------------------------------
@@ -256,13 +292,15 @@ class Strategy:
         rb = hq * d * 2 + 3 * 8
         self.reorder_bytes = tl * (2 * rb + 4)
         # launches per rank: partition index 1, one gather of Q and the three
-        # id tensors 1, attention: row-group metadata 1, group order 1 (only
-        # when the attention grid needs more than one wave of CTAs, one per
-        # SM), attention 1
-        rows = 128 if (hq // cfg.hkv) % 2 == 0 else 256
-        items = -(-tl // rows) * (hq // 2 if rows == 128 else hq)
+        # id tensors 1, the attention plan 3 (rows, tiles, groups) + 1 (group
+        # order, when the plan can hold more work items than the GPU has SMs),
+        # the attention kernel 1
+        head_pairs = (hq // cfg.hkv) % 2 == 0
+        max_tiles = 2 * (-(-tl // 128)) + 1
+        max_groups = max_tiles if head_pairs else (max_tiles + 1) // 2
+        items = max_groups * (hq // 2 if head_pairs else hq)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        self.launches_per_rank = 4 + (1 if items > sms else 0)
+        self.launches_per_rank = 6 + (1 if items > sms else 0)
 
     def run_prep(self, cp, r):
         # The rank's index list, then one gather of Q and the three id

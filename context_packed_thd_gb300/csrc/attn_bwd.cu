@@ -710,7 +710,9 @@ static int launch_bwd(const void* q, const void* k, const void* v, const void* o
   // The dQ grid runs in decreasing-cost order (the forward's group order
   // over the query tiles) when it needs more than one wave of CTAs.
   const bool ordered = ntiles * Hq > sm_count();
-  if (ordered) attn_group_order_kernel<<<1, 1024, 0, s>>>(static_cast<int>(ntiles), ws);
+  if (ordered)
+    attn_group_order_kernel<<<1, 1024, 0, s>>>(static_cast<int>(ntiles), &ws.group_info[0].n_blocks,
+                                               static_cast<int>(sizeof(GroupInfo) / sizeof(int)), ws.order);
   BwdParams p;
   p.row_lo = ws.row_lo;
   p.row_hi = ws.row_hi;

@@ -54,6 +54,7 @@
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
+#include "attn_plan.cuh"
 
 namespace cpthd {
 
@@ -84,19 +85,24 @@ struct AttnSmem {
 struct AttnParams {
   const int32_t* row_lo;
   const int32_t* row_hi;
-  const GroupInfo* group_info;
+  const FwdGroup* groups;
   const int2* intervals;
-  const int32_t* order;
+  const int32_t* order;  // groups by decreasing cost; null: natural order
+  int32_t* ctrl;         // plan counters: [1] groups, [2] next work item, [3] CTAs finished
   float* lse;
+  uint8_t* out;          // bf16 [t_local, Hq, D]: tiles of fewer than 128 rows are stored through it
   long long t_local;
   int Hq;
   int Hkv;
-  int head_pairs;  // 1: tiles A/B = heads 2u, 2u+1 of one row tile; 0: row tiles 2g, 2g+1 of one head
-  int group_rows;  // 128 with head pairs, 256 with tile pairs
+  int head_pairs;  // 1: tiles A/B = heads 2u, 2u+1 of one row tile; 0: two consecutive row tiles of one head
+  int group_rows;  // interval slots per group: 128 with head pairs, 256 with tile pairs
+  int max_groups;  // groups the plan can hold (guards a malformed count)
   int max_blocks;  // upper bound on blocks per group, guards malformed metadata
   float scale_log2;
   int32_t* err;
 };
+
+constexpr int kItemConsumers = 4;  // MMA issuer, data relay, one warp of each softmax warpgroup
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -110,11 +116,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sK = smem + L::kKOff;
   uint8_t* sV = smem + L::kVOff;
 
-  __shared__ uint64_t q_full, k_full[kStages], v_full[kStages];
-  __shared__ uint64_t s_full[2], p_full[2], o_final[2], drain[1];
+  __shared__ uint64_t q_full[2], q_free[2], k_full[kStages], v_full[kStages];
+  __shared__ uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
+  __shared__ uint64_t item_full[2], item_empty[2], drain[1];
+  __shared__ int item_slot[2];
+  __shared__ int wg_item[2];
+  __shared__ int wg_abort[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ int epi_abort[2];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -122,16 +131,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // depends on: none of it touches global memory.
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    epi_abort[0] = epi_abort[1] = 0;
-    mbar_init(&q_full, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&q_full[x], 1);
+      mbar_init(&q_free[x], 1);   // the thread that stores tile x's output
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 5);   // four softmax warps and the data relay
+      mbar_init(&o_final[x], 1);
+      mbar_init(&o_free[x], 4);   // the four softmax warps of tile x
+      mbar_init(&item_full[x], 1);
+      mbar_init(&item_empty[x], kItemConsumers);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-    }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 5);  // four softmax warps and the data relay
-      mbar_init(&o_final[x], 1);
     }
     mbar_init(&drain[0], 1);
     fence_mbar_init();
@@ -149,78 +161,116 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   grid_dependency_wait();
   grid_dependents_launch();
   const int units = p.head_pairs ? (p.Hq >> 1) : p.Hq;
-  const int item = blockIdx.x;
-  // without an order (a grid of one wave) the groups run in index order
-  const int group = p.order ? __ldg(p.order + item / units) : item / units;
-  const int unit = item % units;
-  const int head0 = p.head_pairs ? 2 * unit : unit;
-  const int kvh = head0 / (p.Hq / p.Hkv);
-  const GroupInfo gi = p.group_info[group];
-  const int n_blocks = min(max(gi.n_blocks, 0), p.max_blocks);
-  const int2* group_iv = p.intervals + static_cast<long long>(group) * p.group_rows;
-  const int n_iv = min(max(gi.n_intervals, 0), p.group_rows);
-  const long long group_row0 = static_cast<long long>(group) * p.group_rows;
+  const int gqa = p.Hq / p.Hkv;
+  // Work item i: group order[i / units] (the plan's decreasing-cost order),
+  // head unit i % units.
+  auto item_group = [&](int item) {
+    const int pos = item / units;
+    return p.order ? __ldg(p.order + pos) : pos;
+  };
+  auto item_head0 = [&](int item) {
+    const int unit = item % units;
+    return p.head_pairs ? 2 * unit : unit;
+  };
+  // The k-th item of this CTA, as the producer published it (-1: none left,
+  // or the CTA aborted). Reading the slot and releasing it are one step.
+  auto take_item = [&](int k) -> int {
+    if (!mbar_wait(&item_full[k & 1], (k >> 1) & 1, &abort_flag)) return -1;
+    const int item = item_slot[k & 1];
+    mbar_arrive(&item_empty[k & 1]);
+    return item;
+  };
 
   if (warp < 4) {
    setmaxnreg_dec<kRegsControl>();
    if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_blocks > 0) {
+    // Takes work items (the first is blockIdx.x, then one from the plan's
+    // counter per item), publishes each in a two-slot ring, and loads the
+    // item's Q tiles and K/V blocks. Key blocks are numbered across items
+    // (b), so the stage ring and its release through tile B's score barrier
+    // run on without a break between items.
+    if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&q_full, 2 * L::kQ);
-      for (int x = 0; x < 2; ++x) {
-        const int qh = p.head_pairs ? head0 + x : head0;
-        const int qrow = static_cast<int>(group_row0) + (p.head_pairs ? 0 : x * kBlockM);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sQ + x * L::kQ + c * L::kChunk, &tm_q, &q_full, c * 64, qh, qrow);
-      }
-      BlockCursor cur;
-      cur.init(group_iv, n_iv);
-      int issued = 0;
-      for (int i = 0; i < n_blocks; ++i) {
-        const int st = i & 1;
-        // Stages are released through tile B's score barrier: its phase k
-        // completes when every MMA issued up to S_B(k) is done (one thread
-        // issues them all, tile B last), so phase i - 2 frees K_{i-2} and
-        // phase i - 1 frees V_{i-2}. Each phase is waited for once, in order
-        // (phase 0 before K_2, then phase i - 1 before V_i; K_i for i >= 3
-        // needs phase i - 2, already seen before V_{i-1}). A phase can only
-        // complete after loads this thread issues just before waiting for
-        // the phase ahead of it, so the barrier is never two phases ahead
-        // of a wait and the parity is unambiguous.
-        if (i == kStages && !mbar_wait(&s_full[1], 0, &abort_flag)) break;
-        mbar_arrive_expect_tx(&k_full[st], L::kKV);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sK + st * L::kKV + c * L::kChunk, &tm_k, &k_full[st], c * 64, kvh, cur.start);
-        issued = 2 * i + 1;
-        if (i >= kStages && !mbar_wait(&s_full[1], (i - 1) & 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&v_full[st], L::kKV);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sV + st * L::kKV + c * L::kChunk, &tm_v, &v_full[st], c * 64, kvh, cur.start);
-        issued = 2 * i + 2;
-        cur.next();
+      const int n_items = min(max(p.ctrl[1], 0), p.max_groups) * units;
+      int next = blockIdx.x;
+      int b = 0;       // key blocks of all items so far
+      int issued = 0;  // K/V loads issued, in block order: 2b + 1 after K_b, 2b + 2 after V_b
+      int nq[2] = {0, 0};
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        if (k >= 2 && !mbar_wait(&item_empty[k & 1], ((k >> 1) - 1) & 1, &abort_flag)) break;
+        const int item = (next < n_items) ? next : -1;
+        item_slot[k & 1] = item;
+        mbar_arrive(&item_full[k & 1]);
+        if (item < 0) break;
+        next = static_cast<int>(gridDim.x) + atomicAdd(p.ctrl + 2, 1);
+        const int group = item_group(item);
+        const int head0 = item_head0(item);
+        const int kvh = head0 / gqa;
+        const FwdGroup* gi = p.groups + group;
+        const int n_blocks = min(max(gi->n_blocks, 0), p.max_blocks);
+        if (n_blocks == 0) continue;
+        const int2* group_iv = p.intervals + static_cast<long long>(group) * p.group_rows;
+        const int n_iv = min(max(gi->n_intervals, 0), p.group_rows);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          // tile x's buffer holds the previous item's output until its store has read it
+          if (nq[x] > 0 && !mbar_wait(&q_free[x], (nq[x] - 1) & 1, &abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&q_full[x], L::kQ);
+          const int qh = p.head_pairs ? head0 + x : head0;
+          const int qrow = gi->row0[x];
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(sQ + x * L::kQ + c * L::kChunk, &tm_q, &q_full[x], c * 64, qh, qrow);
+          ++nq[x];
+        }
+        if (!ok) break;
+        BlockCursor cur;
+        cur.init(group_iv, n_iv);
+        for (int i = 0; i < n_blocks; ++i, ++b) {
+          const int st = b & 1;
+          // Stages are released through tile B's score barrier: its phase c
+          // completes when every MMA issued up to S_B(c) is done (one thread
+          // issues them all, tile B last), so phase b - 2 frees K_{b-2} and
+          // phase b - 1 frees V_{b-2}. Each phase is waited for once, in
+          // order (phase 0 before K_2, then phase b - 1 before V_b; K_b for
+          // b >= 3 needs phase b - 2, already seen before V_{b-1}).
+          if (b == kStages && !mbar_wait(&s_full[1], 0, &abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&k_full[st], L::kKV);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(sK + st * L::kKV + c * L::kChunk, &tm_k, &k_full[st], c * 64, kvh, cur.start);
+          issued = 2 * b + 1;
+          if (b >= kStages && !mbar_wait(&s_full[1], (b - 1) & 1, &abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&v_full[st], L::kKV);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(sV + st * L::kKV + c * L::kChunk, &tm_v, &v_full[st], c * 64, kvh, cur.start);
+          issued = 2 * b + 2;
+          cur.next();
+        }
       }
       if (abort_flag) {
         // let every copy still in flight land before the CTA exits
-        mbar_wait_drain(&q_full, 0);
-        for (int x = (issued > 4 ? issued - 4 : 0); x < issued; ++x) {
-          const int i = x >> 1, st = i & 1;
-          mbar_wait_drain((x & 1) ? &v_full[st] : &k_full[st], (i >> 1) & 1);
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+          if (nq[x] > 0) mbar_wait_drain(&q_full[x], (nq[x] - 1) & 1);
+        for (int y = (issued > 4 ? issued - 4 : 0); y < issued; ++y) {
+          const int i = y >> 1, st = i & 1;
+          mbar_wait_drain((y & 1) ? &v_full[st] : &k_full[st], (i >> 1) & 1);
         }
       }
     }
    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread issues both tiles' MMAs, tile A's batch before tile B's.
-    // Issued from one thread they run in that order, so tile B's scores
-    // arrive a batch after tile A's and the two tiles settle into a
-    // staggered schedule: one tile's softmax runs under the other tile's
-    // MMAs. (Two issuing threads started together interleave their MMAs on
-    // the tensor pipe, both tiles finish together, and their softmaxes then
-    // leave the tensor pipe idle: a lockstep that a single issuer avoids.)
-    if (lane == 0 && n_blocks > 0) {
+    // One thread issues both tiles' MMAs, tile A's batch before tile B's, so
+    // that tile B's scores arrive a batch after tile A's and one tile's
+    // softmax runs under the other tile's MMAs (two issuing threads started
+    // together interleave on the tensor pipe and fall into lockstep). An
+    // item's first scores are issued as soon as its Q and first K block are
+    // in, while the softmax warps may still be storing the previous item; its
+    // first P V waits until they have read that item's O.
+    if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kBlockM, D, 0, 1);
       // A descriptor's low word holds the start address (>> 4) and the
@@ -243,69 +293,98 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           umma_ss_w(t_s, qb + off, q_hi, kb + off, k_hi, kIdescS, kk > 0);
         }
       };
-      auto issue_pv = [&](int j, int x) {  // O_x += P_x V_j, P_x read from TMEM
+      auto issue_pv = [&](int j, int x, uint32_t acc0) {  // O_x (+)= P_x V_j, P_x read from TMEM
         const uint32_t t_s = tmem + x * kBlockN;
         const uint32_t t_o = tmem + 256 + x * D;
         const uint32_t vb = v_lo + (((j & 1) * L::kKV) >> 4);
-        const uint32_t acc0 = (j > 0) ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
           umma_ts_w(t_o, t_s + kk * 8, vb + ((kk * 16 * 128) >> 4), v_hi, kIdescO, kk > 0 ? 1u : acc0);
       };
-      int finals = 0;
-      bool ok = mbar_wait(&q_full, 0, &abort_flag) && mbar_wait(&k_full[0], 0, &abort_flag);
-      if (ok) {
-        tc_fence_after_sync();
-        issue_s(0, 0);
-        umma_commit(&s_full[0]);
-        issue_s(0, 1);
-        umma_commit(&s_full[1]);
-      }
-      for (int j = 0; ok && j < n_blocks; ++j) {
-        const bool more = (j + 1 < n_blocks);
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          // P_x(j) is ready, and (through the relay's arrival) V_j and K_{j+1}
-          // have landed
-          if (!mbar_wait(&p_full[x], j & 1, &abort_flag)) { ok = false; break; }
-          tc_fence_after_sync();
-          issue_pv(j, x);
-          if (more) {
-            issue_s(j + 1, x);
-            umma_commit(&s_full[x]);  // also reports O_x += P_x(j) V_j done
-          } else {
-            umma_commit(&o_final[x]);  // tile x's epilogue need not wait for the other tile
-            finals |= 1 << x;
+      int b = 0, nq = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int item = take_item(k);
+        if (item < 0) break;
+        const int n_blocks = min(max(p.groups[item_group(item)].n_blocks, 0), p.max_blocks);
+        int finals = 0;
+        if (n_blocks > 0) {
+          ok = mbar_wait(&q_full[0], nq & 1, &abort_flag) && mbar_wait(&q_full[1], nq & 1, &abort_flag) &&
+               mbar_wait(&k_full[b & 1], (b >> 1) & 1, &abort_flag);
+          ++nq;
+          if (ok) {
+            tc_fence_after_sync();
+            issue_s(b, 0);
+            umma_commit(&s_full[0]);
+            issue_s(b, 1);
+            umma_commit(&s_full[1]);
           }
+          for (int j = 0; ok && j < n_blocks; ++j) {
+            const int bb = b + j;
+            const bool more = (j + 1 < n_blocks);
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              // the previous item's O_x has been read by its epilogue
+              if (j == 0 && k > 0 && !mbar_wait(&o_free[x], (k - 1) & 1, &abort_flag)) { ok = false; break; }
+              // P_x(bb) is ready, and (through the relay's arrival) V_bb and K_{bb+1} have landed
+              if (!mbar_wait(&p_full[x], bb & 1, &abort_flag)) { ok = false; break; }
+              tc_fence_after_sync();
+              issue_pv(bb, x, j > 0 ? 1u : 0u);
+              if (more) {
+                issue_s(bb + 1, x);
+                umma_commit(&s_full[x]);  // also reports O_x += P_x(bb) V_bb done
+              } else {
+                umma_commit(&o_final[x]);  // tile x's epilogue need not wait for the other tile
+                finals |= 1 << x;
+              }
+            }
+          }
+          b += n_blocks;
+        } else if (k > 0) {
+          // an item without keys (only pad rows): no MMA, but its epilogue
+          // must not be signalled before the previous one has read O
+          ok = mbar_wait(&o_free[0], (k - 1) & 1, &abort_flag) && mbar_wait(&o_free[1], (k - 1) & 1, &abort_flag);
         }
+        // a tile whose final commit did not happen (no key block, or an abort)
+        if (!(finals & 1)) umma_commit(&o_final[0]);
+        if (!(finals & 2)) umma_commit(&o_final[1]);
       }
-      // a tile whose final commit did not happen (no block, or an abort)
-      if (!(finals & 1)) umma_commit(&o_final[0]);
-      if (!(finals & 2)) umma_commit(&o_final[1]);
       umma_commit(&drain[0]);
       mbar_wait_drain(&drain[0], 0);
     }
    } else if (warp == 2) {
     // ------------------------------------------------------------ data relay
-    // Waits, per block j, until V_j and K_{j+1} have landed and then arrives
-    // on both tiles' p_full, so that the MMA issuer (the busiest thread of
-    // the CTA) needs a single wait per tile and block. Before arriving for
-    // block j it waits for both p_full phases of block j - 1 to complete, so
-    // that an early arrival never counts toward the previous phase.
+    // Waits, per key block, until V_b and (when the item has a next block)
+    // K_{b+1} have landed and then arrives on both tiles' p_full, so that the
+    // MMA issuer (the busiest thread of the CTA) needs a single wait per tile
+    // and block. Before arriving for block b it waits for both p_full phases
+    // of block b - 1 to complete, so that an early arrival never counts
+    // toward the previous phase.
     if (lane == 0) {
-      for (int j = 0; j < n_blocks; ++j) {
-        if (j > 0 && !(mbar_wait(&p_full[0], (j - 1) & 1, &abort_flag) &&
-                       mbar_wait(&p_full[1], (j - 1) & 1, &abort_flag)))
-          break;
-        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, &abort_flag)) break;
-        if (j + 1 < n_blocks && !mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, &abort_flag)) break;
+      int b = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int item = take_item(k);
+        if (item < 0) break;
+        const int n_blocks = min(max(p.groups[item_group(item)].n_blocks, 0), p.max_blocks);
+        for (int j = 0; j < n_blocks; ++j) {
+          const int bb = b + j;
+          if (bb > 0 && !(mbar_wait(&p_full[0], (bb - 1) & 1, &abort_flag) &&
+                          mbar_wait(&p_full[1], (bb - 1) & 1, &abort_flag))) { ok = false; break; }
+          if (!mbar_wait(&v_full[bb & 1], (bb >> 1) & 1, &abort_flag)) { ok = false; break; }
+          if (j + 1 < n_blocks && !mbar_wait(&k_full[(bb + 1) & 1], ((bb + 1) >> 1) & 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
 #ifdef CPTHD_WAIT_TEST
-        // Test build only: block 1's arrivals are withheld, so the waits for
-        // P(1) can never complete and must run out into the abort path.
-        if (j == 1) continue;
+          // Test build only: key block 1's arrivals are withheld, so the waits
+          // for P(1) can never complete and must run out into the abort path.
+          if (bb == 1) continue;
 #endif
-        mbar_arrive(&p_full[0]);
-        mbar_arrive(&p_full[1]);
+          mbar_arrive(&p_full[0]);
+          mbar_arrive(&p_full[1]);
+        }
+        b += n_blocks;
       }
     }
    }
@@ -315,204 +394,272 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int x = (warp - 4) >> 2;  // tile of this warpgroup
     const int quarter = warp & 3;   // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;
-    const long long grow = group_row0 + (p.head_pairs ? 0 : x * kBlockM) + r;
-    const int qh = p.head_pairs ? head0 + x : head0;
-    const int lo = p.row_lo[grow];
-    const int hi = p.row_hi[grow];
-    const bool valid = (grow < p.t_local) && (lo <= hi);
-    const int tmax_lo = gi.max_lo[x], tmin_hi = gi.min_hi[x];
+    const int bar_id = 1 + x;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off + x * kBlockN;
     const uint32_t t_o = tmem + lane_off + 256 + x * D;
     const float sl2 = p.scale_log2;
-    float m = -INFINITY;  // running max of scale*log2(e)*s
-    float l = 0.f;
-    BlockCursor cur;
-    cur.init(group_iv, n_iv);
-    bool ok = true;
-    for (int j = 0; j < n_blocks; ++j) {
-      // a block never reaches past its interval's end: the next interval may
-      // start inside it, and its keys must be counted there only
-      const int kstart = cur.start;
-      const int kend = cur.end;
-      cur.next();
-      if (!warp_wait(&s_full[x], j & 1, &abort_flag)) { ok = false; break; }
-      tc_fence_after_sync();
-      uint32_t sr[kBlockN];
-      tmem_ld128(t_s, sr);
-      tmem_ld_wait128(sr);
-      const bool full = (kstart >= tmax_lo) && (kstart + kBlockN - 1 <= min(tmin_hi, kend));
-      // 16-column groups of this block that no row of the warp may use
-      uint32_t dead_groups = 0;
-      bool row_dead = false;  // this row has no key in this block
-      if (!full) {
-        // allowed columns of this row: [c_lo, c_hi] (empty when c_lo > c_hi)
-        const int c_lo = min(max(lo - kstart, 0), kBlockN);
-        int c_hi = max(min(min(hi, kend) - kstart, kBlockN - 1), -1);
-        // Blocks start at document starts, so with monotone offsets a row
-        // either starts at or before the block (c_lo = 0) or has no key in
-        // it (c_lo > c_hi). Anything else can only come from offsets the
-        // metadata kernel has already reported; such a row uses no key of
-        // the block, so it never reaches a key before its own start.
-        if (c_lo > 0 && c_lo <= c_hi) record_error(p.err, CPTHD_ERR_BAD_OFFSETS, grow);
-        row_dead = (c_lo > 0) || (c_hi < 0);
-        if (row_dead) c_hi = -1;
-        // bounds over the warp's live rows (a warp whose rows straddle a
-        // document boundary still skips the mask where its live rows may use
-        // every column); dead rows are zeroed below whatever their scores
-        const int w_min = __reduce_min_sync(0xffffffffu, row_dead ? kBlockN - 1 : c_hi);
-        const int w_max = __reduce_max_sync(0xffffffffu, c_hi);
-        dead_groups = (w_max < 0) ? 0xffu : ((0xffu << ((w_max >> 4) + 1)) & 0xffu);
-        if (w_max >= 0) {
-          // The mask runs on the FMA pipe: u = saturate(c - c_hi) is 1
-          // exactly for columns past the row's last key (c is an integer),
-          // and s - u * 2^100 pushes them far below any real score. A row
-          // left with no key in this block is caught after the max (below),
-          // so no two huge values are ever subtracted from each other.
-          // Groups every live row may use are left alone.
-          const float f_hi = static_cast<float>(c_hi);
+    uint8_t* stile = sQ + x * L::kQ;
+    int b = 0;
+    for (int k = 0;; ++k) {
+      // One warp takes the item for the warpgroup, so that its four warps
+      // always agree on the item and on stopping.
+      if (quarter == 0) {
+        int item = -1;
+        if (lane == 0) item = take_item(k);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (lane == 0) {
+          wg_item[x] = item;
+          wg_abort[x] = 0;
+        }
+      }
+      named_bar_sync(bar_id, 128);
+      const int item = wg_item[x];
+      if (item < 0) break;
+      const int group = item_group(item);
+      const int head0 = item_head0(item);
+      const int qh = p.head_pairs ? head0 + x : head0;
+      const FwdGroup* gi = p.groups + group;
+      const int n_blocks = min(max(gi->n_blocks, 0), p.max_blocks);
+      const int2* group_iv = p.intervals + static_cast<long long>(group) * p.group_rows;
+      const int n_iv = min(max(gi->n_intervals, 0), p.group_rows);
+      const int row0 = gi->row0[x];
+      const int h = min(max(gi->h[x], 0), kBlockM);
+      const int tmax_lo = gi->max_lo[x], tmin_hi = gi->min_hi[x];
+      const bool in_tile = r < h;
+      const long long grow = static_cast<long long>(row0) + r;
+      int lo = 1, hi = 0;
+      if (in_tile) {
+        lo = p.row_lo[grow];
+        hi = p.row_hi[grow];
+      }
+      const bool valid = in_tile && (lo <= hi);
+      float m = -INFINITY;  // running max of scale*log2(e)*s
+      float l = 0.f;
+      BlockCursor cur;
+      cur.init(group_iv, n_iv);
+      bool ok = true;
+      for (int j = 0; j < n_blocks; ++j) {
+        const int bb = b + j;
+        // a block never reaches past its interval's end: the next interval may
+        // start inside it, and its keys must be counted there only
+        const int kstart = cur.start;
+        const int kend = cur.end;
+        cur.next();
+        if (!warp_wait(&s_full[x], bb & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after_sync();
+        uint32_t sr[kBlockN];
+        tmem_ld128(t_s, sr);
+        tmem_ld_wait128(sr);
+        const bool full = (kstart >= tmax_lo) && (kstart + kBlockN - 1 <= min(tmin_hi, kend));
+        // 16-column groups of this block that no row of the warp may use
+        uint32_t dead_groups = 0;
+        bool row_dead = false;  // this row has no key in this block
+        if (!full) {
+          // allowed columns of this row: [c_lo, c_hi] (empty when c_lo > c_hi)
+          const int c_lo = min(max(lo - kstart, 0), kBlockN);
+          int c_hi = max(min(min(hi, kend) - kstart, kBlockN - 1), -1);
+          // Blocks start at document starts, so with monotone offsets a row
+          // either starts at or before the block (c_lo = 0) or has no key in
+          // it (c_lo > c_hi). Anything else can only come from offsets the
+          // plan has already reported; such a row uses no key of the block,
+          // so it never reaches a key before its own start.
+          if (c_lo > 0 && c_lo <= c_hi) record_error(p.err, CPTHD_ERR_BAD_OFFSETS, grow);
+          row_dead = (c_lo > 0) || (c_hi < 0);
+          if (row_dead) c_hi = -1;
+          // bounds over the warp's live rows (a warp whose rows straddle a
+          // document boundary still skips the mask where its live rows may use
+          // every column); dead rows are zeroed below whatever their scores
+          const int w_min = __reduce_min_sync(0xffffffffu, row_dead ? kBlockN - 1 : c_hi);
+          const int w_max = __reduce_max_sync(0xffffffffu, c_hi);
+          dead_groups = (w_max < 0) ? 0xffu : ((0xffu << ((w_max >> 4) + 1)) & 0xffu);
+          if (w_max >= 0) {
+            // The mask runs on the FMA pipe: u = saturate(c - c_hi) is 1
+            // exactly for columns past the row's last key (c is an integer),
+            // and s - u * 2^100 pushes them far below any real score. A row
+            // left with no key in this block is caught after the max (below),
+            // so no two huge values are ever subtracted from each other.
+            // Groups every live row may use are left alone.
+            const float f_hi = static_cast<float>(c_hi);
 #pragma unroll
-          for (int g = 0; g < kBlockN / 16; ++g) {
-            if (16 * g + 15 > w_min) {
+            for (int g = 0; g < kBlockN / 16; ++g) {
+              if (16 * g + 15 > w_min) {
 #pragma unroll
-              for (int c = 16 * g; c < 16 * g + 16; c += 2) {
-                float s0, s1;
-                fma2(s0, s1, __saturatef(static_cast<float>(c) - f_hi),
-                     __saturatef(static_cast<float>(c + 1) - f_hi), -kMaskShift, __uint_as_float(sr[c]),
-                     __uint_as_float(sr[c + 1]));
-                sr[c] = __float_as_uint(s0);
-                sr[c + 1] = __float_as_uint(s1);
+                for (int c = 16 * g; c < 16 * g + 16; c += 2) {
+                  float s0, s1;
+                  fma2(s0, s1, __saturatef(static_cast<float>(c) - f_hi),
+                       __saturatef(static_cast<float>(c + 1) - f_hi), -kMaskShift, __uint_as_float(sr[c]),
+                       __uint_as_float(sr[c + 1]));
+                  sr[c] = __float_as_uint(s0);
+                  sr[c + 1] = __float_as_uint(s1);
+                }
               }
             }
           }
         }
-      }
-      // row max of the raw scores: four chains of three-input max
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // row max of the raw scores: four chains of three-input max
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < kBlockN; c += 8) {
+        for (int c = 0; c < kBlockN; c += 8) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          mx[u] = max3f(mx[u], __uint_as_float(sr[c + 2 * u]), __uint_as_float(sr[c + 2 * u + 1]));
-      }
-      float mx_row = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]));
-      // no key of this row in this block
-      if (row_dead || mx_row < -0.5f * kMaskShift) mx_row = -INFINITY;
-      const float m_new = fmaxf(m, mx_row * sl2);
-      const bool grow_o = (m != -INFINITY) && (m_new > m + kRescaleThreshold);
-      float alpha = 1.f;
-      if (m == -INFINITY) {
-        m = m_new;  // nothing accumulated yet: O and l are exactly zero
-      } else if (grow_o) {
-        alpha = ex2(m - m_new);
-        l *= alpha;
-        m = m_new;
-      }
-      // a dead row subtracts 2^100 from every exponent, so all its p are 0
-      const float mref = row_dead ? kMaskShift : ((m == -INFINITY) ? 0.f : m);
-      // p = 2^(scale*log2(e)*s - m): one packed FMA per pair, ex2 per element,
-      // row sum in two packed accumulators. A 64-column half no row may use
-      // stores zeros without exponentials; elsewhere masked columns give 0.
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int u = 0; u < 4; ++u)
+            mx[u] = max3f(mx[u], __uint_as_float(sr[c + 2 * u]), __uint_as_float(sr[c + 2 * u + 1]));
+        }
+        float mx_row = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+        // no key of this row in this block
+        if (row_dead || mx_row < -0.5f * kMaskShift) mx_row = -INFINITY;
+        const float m_new = fmaxf(m, mx_row * sl2);
+        const bool grow_o = (m != -INFINITY) && (m_new > m + kRescaleThreshold);
+        float alpha = 1.f;
+        if (m == -INFINITY) {
+          m = m_new;  // nothing accumulated yet: O and l are exactly zero
+        } else if (grow_o) {
+          alpha = ex2(m - m_new);
+          l *= alpha;
+          m = m_new;
+        }
+        // a dead row subtracts 2^100 from every exponent, so all its p are 0
+        const float mref = row_dead ? kMaskShift : ((m == -INFINITY) ? 0.f : m);
+        // p = 2^(scale*log2(e)*s - m): one packed FMA per pair, ex2 per element,
+        // row sum in two packed accumulators. A 64-column half no row may use
+        // stores zeros without exponentials; elsewhere masked columns give 0.
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t pk[32];
-        if (((dead_groups >> (4 * h2)) & 0xfu) == 0xfu) {
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[32];
+          if (((dead_groups >> (4 * h2)) & 0xfu) == 0xfu) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = 0u;
-        } else {
+            for (int c = 0; c < 32; ++c) pk[c] = 0u;
+          } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            float a0, a1;
-            fma2(a0, a1, __uint_as_float(sr[64 * h2 + 2 * c]), __uint_as_float(sr[64 * h2 + 2 * c + 1]), sl2, -mref);
-            const float e0 = ex2(a0);
-            const float e1 = ex2(a1);
-            add2(rs[2 * (c & 1)], rs[2 * (c & 1) + 1], e0, e1);
-            pk[c] = pack_bf16x2(e0, e1);
+            for (int c = 0; c < 32; ++c) {
+              float a0, a1;
+              fma2(a0, a1, __uint_as_float(sr[64 * h2 + 2 * c]), __uint_as_float(sr[64 * h2 + 2 * c + 1]), sl2,
+                   -mref);
+              const float e0 = ex2(a0);
+              const float e1 = ex2(a1);
+              add2(rs[2 * (c & 1)], rs[2 * (c & 1) + 1], e0, e1);
+              pk[c] = pack_bf16x2(e0, e1);
+            }
+          }
+          tmem_st32(t_s + 32 * h2, pk);
+        }
+        l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+        if (__any_sync(0xffffffffu, grow_o)) {
+          // O_x holds P_x V up to the previous block (complete before S_x(bb)
+          // was reported) and nothing newer: rescale it before the next P V
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(t_o + c * 32, orr);
+            tmem_ld_wait(orr);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) orr[q] = __float_as_uint(__uint_as_float(orr[q]) * alpha);
+            tmem_st32(t_o + c * 32, orr);
           }
         }
-        tmem_st32(t_s + 32 * h2, pk);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[x]);
       }
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-      if (__any_sync(0xffffffffu, grow_o)) {
-        // O_x holds P_x(j-1) V_{j-1} (complete before S_x(j) was reported) and
-        // nothing newer: rescale it before O_x += P_x(j) V_j is issued
+      b += n_blocks;
+      // ---------------------------------------------------------- epilogue
+      // O / l in bf16 goes into this tile's Q buffer (free once o_final[x] is
+      // reported: the last MMA reading it is done) in the 128-byte swizzle of
+      // the output's tensor map. A full tile is stored by one thread with
+      // TMA; a shorter one by the warpgroup's threads, 16 bytes each, from
+      // the same staging (a TMA box would write the next tile's rows). Then
+      // the buffer is released for the next item's Q. Every warp reaches the
+      // barriers of every item it took; an aborted one only marks the tile.
+      if (ok) ok = warp_wait(&o_final[x], k & 1, &abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after_sync();
+      if (ok && n_blocks > 0) {
+        const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t orr[32];
-          tmem_ld32(t_o + c * 32, orr);
-          tmem_ld_wait(orr);
-#pragma unroll
-          for (int q = 0; q < 32; ++q) orr[q] = __float_as_uint(__uint_as_float(orr[q]) * alpha);
-          tmem_st32(t_o + c * 32, orr);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[x]);
-    }
-    // ---------------------------------------------------------- epilogue
-    // O / l in bf16 goes into this tile's Q buffer (free once o_final[x] is
-    // reported: the last MMA reading it is done), in the 128-byte swizzle of
-    // the output's tensor map, and one thread of the warpgroup stores the
-    // tile with TMA (rows past the slice are not written). Every warp of the
-    // warpgroup reaches the barrier; an aborted one only marks the tile.
-    if (ok && n_blocks > 0) ok = warp_wait(&o_final[x], 0, &abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after_sync();
-    uint8_t* stile = sQ + x * L::kQ;
-    if (ok) {
-      const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        if (n_blocks > 0) {
+          uint32_t rr[32];
           tmem_ld32(t_o + c * 32, rr);
           tmem_ld_wait(rr);
-        }
-        uint32_t ob[16];
+          uint32_t ob[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          ob[q] = (valid && n_blocks > 0)
-                      ? pack_bf16x2(__uint_as_float(rr[2 * q]) * inv, __uint_as_float(rr[2 * q + 1]) * inv)
-                      : 0u;
+          for (int q = 0; q < 16; ++q)
+            ob[q] = valid ? pack_bf16x2(__uint_as_float(rr[2 * q]) * inv, __uint_as_float(rr[2 * q + 1]) * inv) : 0u;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int u = 4 * c + q4;  // 16-byte unit of the row; 8 units per 64-column panel
-          uint8_t* dst = stile + (u >> 3) * L::kChunk + r * 128 + (((u & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(ob[4 * q4], ob[4 * q4 + 1], ob[4 * q4 + 2], ob[4 * q4 + 3]);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int u = 4 * c + q4;  // 16-byte unit of the row; 8 units per 64-column panel
+            uint8_t* dst = stile + (u >> 3) * L::kChunk + r * 128 + (((u & 7) ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(ob[4 * q4], ob[4 * q4 + 1], ob[4 * q4 + 2], ob[4 * q4 + 3]);
+          }
         }
       }
-      if (grow < p.t_local)
+      // O_x is read: the next item's first P V may overwrite it
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[x]);
+      if (ok && in_tile) {
         p.lse[static_cast<long long>(qh) * p.t_local + grow] =
             (valid && l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-      fence_proxy_async_smem();
-    } else {
-      epi_abort[x] = 1;
-    }
-    named_bar_sync(1 + x, 128);
-    const long long tile_row0 = group_row0 + (p.head_pairs ? 0 : x * kBlockM);
-    if (r == 0 && !epi_abort[x] && tile_row0 < p.t_local) {
+        if (n_blocks == 0) {
+          // no key in the whole group (only pad rows): zeros, stored directly
+          uint4* dst = reinterpret_cast<uint4*>(p.out + (grow * p.Hq + qh) * static_cast<long long>(D) * 2);
 #pragma unroll
-      for (int c = 0; c < L::kChunks; ++c)
-        tma_store_3d(&tm_o, stile + c * L::kChunk, c * 64, qh, static_cast<int>(tile_row0));
-      bulk_commit_group();
-      bulk_wait_group_read_all();
+          for (int u = 0; u < D / 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if (!ok) wg_abort[x] = 1;
+      fence_proxy_async_smem();
+      named_bar_sync(bar_id, 128);
+      // read once, between the two barriers: the warpgroup's first warp
+      // clears the flag for the next item only after the second one
+      const bool stop = (wg_abort[x] != 0);
+      if (!stop && n_blocks > 0 && h > 0) {
+        if (h == kBlockM) {
+          if (r == 0) {
+#pragma unroll
+            for (int c = 0; c < L::kChunks; ++c) tma_store_3d(&tm_o, stile + c * L::kChunk, c * 64, qh, row0);
+            bulk_commit_group();
+            bulk_wait_group_read_all();
+          }
+        } else {
+          constexpr int kUnitsPerRow = D / 8;  // 16-byte units of one output row
+          for (int u = r; u < h * kUnitsPerRow; u += kBlockM) {
+            const int rr = u / kUnitsPerRow;
+            const int cu = u - rr * kUnitsPerRow;
+            const uint8_t* src = stile + (cu >> 3) * L::kChunk + rr * 128 + (((cu & 7) ^ (rr & 7)) << 4);
+            uint8_t* dst = p.out + ((static_cast<long long>(row0) + rr) * p.Hq + qh) * static_cast<long long>(D) * 2 +
+                           cu * 16;
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+          }
+        }
+      }
+      named_bar_sync(bar_id, 128);
+      if (n_blocks > 0 && r == 0) mbar_arrive(&q_free[x]);
+      if (stop) break;
     }
+    if (r == 0) bulk_wait_group_all();  // this tile's last output store has landed
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if (abort_flag && threadIdx.x == 0) record_error(p.err, CPTHD_ERR_TIMEOUT, item);
+  if (threadIdx.x == 0) {
+    if (abort_flag) record_error(p.err, CPTHD_ERR_TIMEOUT, blockIdx.x);
+    // The last CTA to finish returns the work counters to zero for the next
+    // launch on this plan.
+    __threadfence();
+    if (atomicAdd(p.ctrl + 3, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(p.ctrl + 2, 0);
+      atomicExch(p.ctrl + 3, 0);
+    }
+  }
   tc_fence_after_sync();
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 template <int D>
 static int launch_attn(const void* q, const void* k, const void* v, long long t_local, long long T, int Hq, int Hkv,
-                       float scale_log2, const AttnWorkspace& ws, long long ngroups, int group_rows, bool ordered,
-                       void* out,
+                       float scale_log2, const FwdPlan& plan, const FwdShape& shape, bool ordered, void* out,
                        float* lse, int32_t* err, cudaStream_t s) {
   EncodeTiledFn enc = get_encode_tiled();
   if (enc == nullptr) return CPTHD_ERR_CUDA;
@@ -521,27 +668,42 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
       !make_rows_heads_map(enc, &mv, v, T, Hkv, D) || !make_rows_heads_map(enc, &mo, out, t_local, Hq, D))
     return CPTHD_ERR_UNSUPPORTED;
   AttnParams p;
-  p.row_lo = ws.row_lo;
-  p.row_hi = ws.row_hi;
-  p.group_info = ws.group_info;
-  p.intervals = ws.intervals;
-  p.order = ordered ? ws.order : nullptr;
+  p.row_lo = plan.row_lo;
+  p.row_hi = plan.row_hi;
+  p.groups = plan.groups;
+  p.intervals = plan.intervals;
+  p.order = ordered ? plan.order : nullptr;
+  p.ctrl = plan.ctrl;
   p.lse = lse;
+  p.out = static_cast<uint8_t*>(out);
   p.t_local = t_local;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.head_pairs = (group_rows == kBlockM) ? 1 : 0;
-  p.group_rows = group_rows;
-  p.max_blocks = static_cast<int>((T + kBlockN - 1) / kBlockN + group_rows);
+  p.head_pairs = shape.head_pairs;
+  p.group_rows = shape.group_rows;
+  p.max_groups = static_cast<int>(shape.max_groups);
+  p.max_blocks = static_cast<int>((T + kBlockN - 1) / kBlockN + shape.group_rows);
   p.scale_log2 = scale_log2;
   p.err = err;
   const int smem = AttnSmem<D>::kLaunchBytes;
   CPTHD_TRY_CUDA(cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-  const long long items = ngroups * (p.head_pairs ? Hq / 2 : Hq);
+  const long long items = shape.max_groups * (shape.head_pairs ? Hq / 2 : Hq);
   if (items > INT32_MAX) return CPTHD_ERR_UNSUPPORTED;
-  CPTHD_TRY_CUDA(launch_pdl(attn_fwd_tc_kernel<D>, dim3(static_cast<unsigned>(items)), dim3(kAttnThreads), smem, s,
+  const int sms = sm_count();
+  if (sms < 1) return CPTHD_ERR_CUDA;
+  // one CTA per SM (one fits: shared memory and TMEM are taken whole), each
+  // taking work items until none is left
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  CPTHD_TRY_CUDA(launch_pdl(attn_fwd_tc_kernel<D>, dim3(static_cast<unsigned>(grid)), dim3(kAttnThreads), smem, s,
                             mq, mk, mv, mo, p));
   return CPTHD_OK;
+}
+
+// Whether the plan orders the groups: when there are more work items than
+// SMs (the attention grid's CTAs take items in that order).
+static bool plan_ordered(const FwdShape& shape, int Hq) {
+  const long long items = shape.max_groups * (shape.head_pairs ? Hq / 2 : Hq);
+  return items > sm_count();
 }
 
 }  // namespace cpthd
@@ -550,48 +712,45 @@ extern "C" int thd_causal_attn_workspace_size(int64_t t_local, int Hq, int Hkv, 
   if (bytes_host == nullptr || t_local < 0 || Hq < 1 || Hkv < 1) return CPTHD_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return CPTHD_ERR_UNSUPPORTED;
   (void)d;
-  const int rows = cpthd::group_rows_for(Hq, Hkv);
-  const long long ngroups = (t_local + rows - 1) / rows;
-  *bytes_host = cpthd::attn_workspace_bytes(ngroups, rows);
+  *bytes_host = cpthd::fwd_plan_bytes(cpthd::fwd_shape(t_local, Hq, Hkv));
   return CPTHD_OK;
 }
 
 namespace cpthd {
 
 static int check_workspace(int64_t t_local, int Hq, int Hkv, const void* workspace_dev, size_t workspace_bytes) {
-  const int rows = group_rows_for(Hq, Hkv);
-  const long long ngroups = (t_local + rows - 1) / rows;
-  if (workspace_dev == nullptr || workspace_bytes < attn_workspace_bytes(ngroups, rows) ||
+  if (workspace_dev == nullptr || workspace_bytes < fwd_plan_bytes(fwd_shape(t_local, Hq, Hkv)) ||
       (reinterpret_cast<uintptr_t>(workspace_dev) & 255))
     return CPTHD_ERR_WORKSPACE;
   return CPTHD_OK;
 }
 
-}  // namespace cpthd
-
-namespace cpthd {
-
-// Metadata of the slice's row groups (and, past one wave, their order) into
-// the workspace; shape and workspace already checked.
+// The plan of the slice's rows (rows, tiles, groups and, past one wave,
+// their order) into the workspace; shape and workspace already checked.
 static int launch_plan(const IndexGen& slots, long long t_local, long long T, const int32_t* cu,
                        const int32_t* cup, int num_docs, int Hq, int Hkv, void* workspace, int32_t* err,
                        cudaStream_t s) {
-  const int rows = group_rows_for(Hq, Hkv);
-  const long long ngroups = (t_local + rows - 1) / rows;
-  AttnWorkspace ws = carve_workspace(workspace, ngroups, rows);
-  if (rows == kBlockM) {
-    CPTHD_TRY_CUDA(launch_pdl(attn_group_meta_kernel<kBlockM>, dim3(static_cast<unsigned>(ngroups)), dim3(kBlockM), 0,
-                              s, slots, t_local, cu, cup, num_docs, T, ws, err));
+  const FwdShape shape = fwd_shape(t_local, Hq, Hkv);
+  FwdPlan plan = carve_fwd_plan(workspace, shape);
+  const int sms = sm_count();
+  if (sms < 1) return CPTHD_ERR_CUDA;
+  if (shape.max_groups > INT32_MAX / 2) return CPTHD_ERR_UNSUPPORTED;
+  CPTHD_TRY_CUDA(launch_pdl(attn_rows_kernel, dim3(static_cast<unsigned>((t_local + 255) / 256)), dim3(256), 0, s,
+                            slots, t_local, cu, cup, num_docs, T, plan, err));
+  CPTHD_TRY_CUDA(launch_pdl(attn_tiles_kernel, dim3(1), dim3(1024), 0, s, t_local, shape.max_tiles,
+                            shape.head_pairs, plan, err));
+  if (shape.head_pairs) {
+    CPTHD_TRY_CUDA(launch_pdl(attn_fwd_group_kernel<kBlockM>, dim3(static_cast<unsigned>(shape.max_groups)),
+                              dim3(kBlockM), 0, s, 1, cup, plan));
   } else {
-    CPTHD_TRY_CUDA(launch_pdl(attn_group_meta_kernel<2 * kBlockM>, dim3(static_cast<unsigned>(ngroups)),
-                              dim3(2 * kBlockM), 0, s, slots, t_local, cu, cup, num_docs, T, ws, err));
+    CPTHD_TRY_CUDA(launch_pdl(attn_fwd_group_kernel<2 * kBlockM>, dim3(static_cast<unsigned>(shape.max_groups)),
+                              dim3(2 * kBlockM), 0, s, 0, cup, plan));
   }
-  // The longest groups go first when the grid needs more than one wave (one
-  // CTA per SM); within a single wave the order makes no difference and the
-  // ordering launch is skipped.
-  const long long items = ngroups * ((rows == kBlockM) ? Hq / 2 : Hq);
-  if (items > sm_count())
-    CPTHD_TRY_CUDA(launch_pdl(attn_group_order_kernel, dim3(1), dim3(1024), 0, s, static_cast<int>(ngroups), ws));
+  // The costliest groups go first when there are more work items than SMs.
+  if (plan_ordered(shape, Hq))
+    CPTHD_TRY_CUDA(launch_pdl(attn_group_order_kernel, dim3(1), dim3(1024), 0, s,
+                              static_cast<int>(shape.max_groups), &plan.groups[0].n_blocks,
+                              static_cast<int>(sizeof(FwdGroup) / sizeof(int)), plan.order));
   return CPTHD_OK;
 }
 
@@ -649,19 +808,17 @@ extern "C" int thd_causal_attn_fwd_planned(int64_t t_local, const void* q_dev, c
   if (align & 15) return CPTHD_ERR_UNSUPPORTED;
   st = check_workspace(t_local, Hq, Hkv, workspace_dev, workspace_bytes);
   if (st != CPTHD_OK) return st;
-  const int rows = group_rows_for(Hq, Hkv);
-  const long long ngroups = (t_local + rows - 1) / rows;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
   const float scale_log2 = scale * 1.4426950408889634f;
-  AttnWorkspace ws = carve_workspace(const_cast<void*>(workspace_dev), ngroups, rows);
-  // the plan launched the group order exactly when the grid exceeds a wave
-  const long long items = ngroups * ((rows == kBlockM) ? Hq / 2 : Hq);
-  const bool ordered = items > sm_count();
+  const FwdShape shape = fwd_shape(t_local, Hq, Hkv);
+  const FwdPlan plan = carve_fwd_plan(const_cast<void*>(workspace_dev), shape);
+  // the plan ordered its groups exactly when there are more items than SMs
+  const bool ordered = plan_ordered(shape, Hq);
   if (d == 128)
-    return launch_attn<128>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ngroups, rows, ordered, out_dev,
+    return launch_attn<128>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, plan, shape, ordered, out_dev,
                             lse_dev, err_dev, s);
-  return launch_attn<64>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, ws, ngroups, rows, ordered, out_dev,
+  return launch_attn<64>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, plan, shape, ordered, out_dev,
                          lse_dev, err_dev, s);
 }
 

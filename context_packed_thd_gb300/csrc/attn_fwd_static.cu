@@ -5,7 +5,8 @@
 // plugins that must not call cudaMalloc (it synchronises the device and can
 // fail or fragment memory mid-step), or hot paths that must never enter the
 // allocator at all. For them this file keeps the attention's scratch
-// (per-row key bounds, per-group key intervals, the group schedule) in a
+// (per-row key bounds, the query tiles, per-group key intervals, the group
+// schedule) in a
 // fixed-size array that lives in device memory for as long as the library is
 // loaded, so the call itself allocates nothing.
 //
@@ -24,10 +25,11 @@
 
 namespace cpthd {
 
-// 4 MiB: the scratch of a slice of up to about 250,000 query rows (16 bytes
-// per row plus 28 bytes per row group). Every GPU that loads the library
-// holds this array until the process exits.
-constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+// 8 MiB: the scratch of a slice of up to about 255,000 query rows (the plan
+// takes about 33 bytes per row: per-row bounds and document, the document
+// runs, and per tile and group its key intervals). Every GPU that loads the
+// library holds this array until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kStaticScratchBytes];
 

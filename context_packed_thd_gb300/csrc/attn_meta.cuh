@@ -194,22 +194,25 @@ static __global__ void __launch_bounds__(ROWS) attn_group_meta_kernel(
 }
 
 // One block of 1024 threads: order[] = groups by decreasing block count
-// (ties by group index). Larger group counts keep the natural order.
-static __global__ void __launch_bounds__(1024) attn_group_order_kernel(int ngroups, AttnWorkspace ws) {
+// (ties by group index, so equal-cost groups keep their natural order).
+// cost[i * cost_stride] is group i's block count. Larger group counts keep
+// the natural order.
+static __global__ void __launch_bounds__(1024) attn_group_order_kernel(int ngroups, const int* __restrict__ cost,
+                                                                       int cost_stride, int32_t* __restrict__ order) {
   __shared__ unsigned keys[kMaxSortGroups];
   grid_dependency_wait();
   grid_dependents_launch();
   const int t = threadIdx.x;
   if (ngroups > kMaxSortGroups) {
-    for (int i = t; i < ngroups; i += blockDim.x) ws.order[i] = i;
+    for (int i = t; i < ngroups; i += blockDim.x) order[i] = i;
     return;
   }
   int n2 = 1;
   while (n2 < ngroups) n2 <<= 1;
   for (int i = t; i < n2; i += blockDim.x) {
     if (i < ngroups) {
-      const unsigned cost = static_cast<unsigned>(min(max(ws.group_info[i].n_blocks, 0), (1 << 18) - 1));
-      keys[i] = ((cost ^ 0x3ffffu) << 13) | static_cast<unsigned>(i);
+      const unsigned c = static_cast<unsigned>(min(max(cost[static_cast<long long>(i) * cost_stride], 0), (1 << 18) - 1));
+      keys[i] = ((c ^ 0x3ffffu) << 13) | static_cast<unsigned>(i);
     } else {
       keys[i] = 0xffffffffu;
     }
@@ -228,7 +231,7 @@ static __global__ void __launch_bounds__(1024) attn_group_order_kernel(int ngrou
       __syncthreads();
     }
   }
-  for (int i = t; i < ngroups; i += blockDim.x) ws.order[i] = static_cast<int>(keys[i] & 0x1fffu);
+  for (int i = t; i < ngroups; i += blockDim.x) order[i] = static_cast<int>(keys[i] & 0x1fffu);
 }
 
 }  // namespace cpthd

@@ -1,0 +1,362 @@
+// The forward attention's plan: variable-height query tiles cut at document
+// boundaries, their key intervals, and the order the attention kernel takes
+// them in.
+//
+// A query row with physical slot p in document j may attend exactly the key
+// slots [cu_seqlens_padded[j], p] (TransformerEngine PR #3221, "Scope and
+// constraints": causal, window_size = (-1, 0); "What changed": document
+// boundaries kept through THD metadata). The tensor cores work on 128-row
+// query tiles, and a tile pays for the union of its rows' key intervals, so
+// the plan cuts the slice's rows where the document changes: every run of
+// consecutive rows of one document (a DualChunkSwap rank holds each document
+// as one run, chunk r then chunk 2*cp_size-1-r; a NO_LOAD_BALANCE rank as a
+// contiguous piece) is cut into 128-row tiles aligned to the run's end, with
+// the remainder as the run's first tile, which holds its earliest positions
+// and therefore its cheapest rows. Runs shorter than a tile are packed
+// together, in order, while they fit in 128 rows (a packed tile pays each
+// document's keys once, as separate tiles would). Any two consecutive tiles
+// then hold more than 128 rows together, so a slice of n rows has at most
+// 2 * ceil(n / 128) + 1 tiles; buffers and grids are sized by that bound.
+//
+// Kernels, in stream order (all launched by thd_causal_attn_plan):
+//  1. attn_rows_kernel: per local row, its document and key interval; also
+//     checks the offset table.
+//  2. attn_tiles_kernel (one block): the runs and the greedy cut into tiles.
+//  3. attn_fwd_group_kernel: per group (one tile under two query heads when
+//     the GQA group size is even, else two consecutive tiles under one head)
+//     the union of its rows' intervals, one per document, sorted; its cost
+//     in 128-key blocks; and per tile the bounds inside which a key block
+//     needs no mask.
+//  4. attn_group_order_kernel (when the grid has more items than SMs): the
+//     groups by decreasing cost.
+#pragma once
+
+#include "attn_meta.cuh"
+
+namespace cpthd {
+
+struct FwdGroup {
+  int n_intervals;
+  int n_blocks;   // cost: 128-key blocks over the group's intervals
+  int max_lo[2];  // per tile, over real rows; INT_MIN when the tile has none
+  int min_hi[2];  // per tile, over real rows; INT_MAX when the tile has none
+  int row0[2];    // first local row of each tile
+  int h[2];       // rows of each tile (0: no tile)
+};
+
+// Device arrays of a plan, carved from the caller's workspace.
+struct FwdPlan {
+  int32_t* row_lo;     // [n] first allowed key slot of each local row (empty: lo > hi)
+  int32_t* row_hi;     // [n] last allowed key slot
+  int32_t* row_doc;    // [n] document of the row's slot, -1 when the slot is out of range
+  int32_t* seg;        // [n] first rows of the document runs (scratch of the tile kernel)
+  int2* tiles;         // [max_tiles] (first row, rows)
+  int32_t* ctrl;       // [0] tiles, [1] groups, [2] next work item, [3] attention CTAs finished
+  FwdGroup* groups;    // [max_groups]
+  int2* intervals;     // [max_groups * group_rows] (start, end) inclusive, per group
+  int32_t* order;      // [max_groups]
+};
+
+struct FwdShape {
+  long long n;           // query rows of the slice
+  long long max_tiles;   // 2 * ceil(n / 128) + 1
+  long long max_groups;  // tiles (head pairs) or ceil(tiles / 2) (tile pairs)
+  int group_rows;        // 128 (head pairs) or 256 (tile pairs): interval slots per group
+  int head_pairs;        // 1: a group is one tile under two query heads of one KV head
+};
+
+inline FwdShape fwd_shape(long long n, int Hq, int Hkv) {
+  FwdShape s;
+  s.n = n;
+  s.head_pairs = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
+  s.max_tiles = 2 * ((n + kBlockM - 1) / kBlockM) + 1;
+  s.max_groups = s.head_pairs ? s.max_tiles : (s.max_tiles + 1) / 2;
+  s.group_rows = s.head_pairs ? kBlockM : 2 * kBlockM;
+  return s;
+}
+
+inline size_t fwd_plan_bytes(const FwdShape& s) {
+  size_t b = 0;
+  b += 4 * align256(sizeof(int32_t) * s.n);
+  b += align256(sizeof(int2) * s.max_tiles);
+  b += align256(sizeof(int32_t) * 8);
+  b += align256(sizeof(FwdGroup) * s.max_groups);
+  b += align256(sizeof(int2) * s.max_groups * s.group_rows);
+  b += align256(sizeof(int32_t) * s.max_groups);
+  return b;
+}
+
+inline FwdPlan carve_fwd_plan(void* base, const FwdShape& s) {
+  char* p = static_cast<char*>(base);
+  FwdPlan w;
+  w.row_lo = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * s.n);
+  w.row_hi = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * s.n);
+  w.row_doc = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * s.n);
+  w.seg = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * s.n);
+  w.tiles = reinterpret_cast<int2*>(p); p += align256(sizeof(int2) * s.max_tiles);
+  w.ctrl = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * 8);
+  w.groups = reinterpret_cast<FwdGroup*>(p); p += align256(sizeof(FwdGroup) * s.max_groups);
+  w.intervals = reinterpret_cast<int2*>(p); p += align256(sizeof(int2) * s.max_groups * s.group_rows);
+  w.order = reinterpret_cast<int32_t*>(p);
+  return w;
+}
+
+// 1. One thread per local row: the row's physical slot (from the slice's
+// index list or the partition formulas), its document and its key interval.
+// The blocks also check the document table (offsets start at 0 and never
+// decrease, padded offsets end at T, L_j <= P_j, and under a computed
+// DualChunkSwap slice every padded length is a multiple of 2*cp_size) in a
+// grid-stride loop over documents.
+static __global__ void __launch_bounds__(256) attn_rows_kernel(IndexGen slots, long long n,
+                                                               const int32_t* __restrict__ cu,
+                                                               const int32_t* __restrict__ cup, int num_docs,
+                                                               long long T, FwdPlan plan, int32_t* err) {
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const long long i = blockIdx.x * 256LL + threadIdx.x;
+  const int p = (i < n) ? slots.at(i) : 0;  // issued before the checks below
+  for (long long j = i; j <= num_docs; j += static_cast<long long>(gridDim.x) * 256) {
+    if (j == 0 && (cu[0] != 0 || cup[0] != 0)) record_error(err, CPTHD_ERR_BAD_OFFSETS, 0);
+    if (j == num_docs && cup[j] != T) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
+    if (j < num_docs) {
+      const int L = cu[j + 1] - cu[j];
+      const int P = cup[j + 1] - cup[j];
+      if (L < 0 || P < 0) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
+      else if (L > P) record_error(err, CPTHD_ERR_PAD_LENGTH, j);
+      else if (slots.idx == nullptr && slots.strategy == CPTHD_DUAL_CHUNK_SWAP && P % (2 * slots.cp) != 0)
+        record_error(err, CPTHD_ERR_NOT_DIVISIBLE, j);
+    }
+  }
+  if (i >= n) return;
+  int lo = 1, hi = 0, doc = -1;  // empty interval
+  if (p < 0 || p >= T) {
+    record_error(err, CPTHD_ERR_INDEX_RANGE, i);
+  } else {
+    doc = upper_bound_doc(cup, num_docs, p);
+    const int start = cup[doc];
+    const int L = cu[doc + 1] - cu[doc];
+    const int pos = p - start;
+    // start >= 0 is re-checked so that malformed offsets can never widen an
+    // interval beyond [0, T)
+    if (pos >= 0 && pos < L && start >= 0) { lo = start; hi = p; }
+  }
+  plan.row_lo[i] = lo;
+  plan.row_hi[i] = hi;
+  plan.row_doc[i] = doc;
+}
+
+// 2. One block of 1024 threads: the runs of equal documents (each thread
+// scans a contiguous share of the rows; a block-wide scan places the run
+// starts in order), then one thread cuts the runs into tiles greedily as
+// described at the top of this file and writes the tile and group counts.
+// It also clears the attention kernel's work counters.
+static __global__ void __launch_bounds__(1024) attn_tiles_kernel(long long n, long long max_tiles, int head_pairs,
+                                                                 FwdPlan plan, int32_t* err) {
+  __shared__ int warp_total[32];
+  __shared__ int block_total;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int t = threadIdx.x;
+  const int lane = t & 31, wid = t >> 5;
+  const long long per = (n + 1023) / 1024;
+  const long long a = min(n, t * per);
+  const long long b = min(n, a + per);
+  int count = 0;
+  int prev = (a > 0 && a < n) ? plan.row_doc[a - 1] : 0;
+  for (long long i = a; i < b; ++i) {
+    const int d = plan.row_doc[i];
+    if (i == 0 || d != prev) ++count;
+    prev = d;
+  }
+  // exclusive scan of the per-thread counts in thread order
+  int incl = count;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_total[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int w = warp_total[lane];
+    int wi = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_total[lane] = wi - w;  // exclusive prefix of the warps
+    if (lane == 31) block_total = wi;
+  }
+  __syncthreads();
+  int pos = warp_total[wid] + incl - count;
+  prev = (a > 0 && a < n) ? plan.row_doc[a - 1] : 0;
+  for (long long i = a; i < b; ++i) {
+    const int d = plan.row_doc[i];
+    if (i == 0 || d != prev) plan.seg[pos++] = static_cast<int32_t>(i);
+    prev = d;
+  }
+  __syncthreads();  // the run starts written above are visible to thread 0
+  if (t != 0) return;
+  const int runs = block_total;
+  long long nt = 0;
+  long long cur0 = 0;
+  int curh = 0;
+  auto emit = [&](long long r0, int h) {
+    if (nt < max_tiles) plan.tiles[nt] = make_int2(static_cast<int>(r0), h);
+    ++nt;
+  };
+  for (int k = 0; k < runs; ++k) {
+    const long long s = plan.seg[k];
+    const long long e = (k + 1 < runs) ? static_cast<long long>(plan.seg[k + 1]) : n;
+    const long long len = e - s;
+    const int head = static_cast<int>(len % kBlockM);
+    const long long full = len / kBlockM;
+    if (head > 0) {
+      if (curh > 0 && curh + head <= kBlockM) {
+        curh += head;  // packed with the short runs before it (rows are contiguous)
+      } else {
+        if (curh > 0) emit(cur0, curh);
+        cur0 = s;
+        curh = head;
+      }
+    }
+    if (full > 0) {
+      if (curh > 0) { emit(cur0, curh); curh = 0; }
+      for (long long f = 0; f < full; ++f) emit(s + head + kBlockM * f, kBlockM);
+    }
+  }
+  if (curh > 0) emit(cur0, curh);
+  // The bound holds for every input (any two consecutive tiles hold more
+  // than 128 rows); were it ever exceeded, the missing rows are reported.
+  if (nt > max_tiles) {
+    record_error(err, CPTHD_ERR_INDEX_RANGE, nt);
+    nt = max_tiles;
+  }
+  plan.ctrl[0] = static_cast<int>(nt);
+  plan.ctrl[1] = static_cast<int>(head_pairs ? nt : (nt + 1) / 2);
+  plan.ctrl[2] = 0;
+  plan.ctrl[3] = 0;
+}
+
+// 3. One block of ROWS threads per group (grid: max_groups): thread t owns
+// row t of tile A (t < 128) or row t - 128 of tile B. Groups past the
+// count get an empty record. The rows' intervals are sorted by (document,
+// end) with a bitonic sort (partners closer than 32 rows exchange through
+// warp shuffles, the rest through shared memory), and the last row of each
+// document gives that document's interval [cup[j], its largest slot].
+template <int ROWS>
+static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(int head_pairs, const int32_t* __restrict__ cup,
+                                                                     FwdPlan plan) {
+  constexpr int kWarps = ROWS / 32;
+  __shared__ unsigned long long xbuf[2][ROWS];
+  __shared__ int warp_sum[kWarps];
+  __shared__ int red_blocks[kWarps];
+  __shared__ int red_lo[kWarps];
+  __shared__ int red_hi[kWarps];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int t = threadIdx.x;
+  const int lane = t & 31, wid = t >> 5;
+  const int g = blockIdx.x;
+  const int ntiles = plan.ctrl[0];
+  const int ngroups = plan.ctrl[1];
+  if (g >= ngroups) {
+    if (t == 0) {
+      FwdGroup e;
+      e.n_intervals = 0;
+      e.n_blocks = 0;
+      for (int x = 0; x < 2; ++x) { e.max_lo[x] = INT_MIN; e.min_hi[x] = INT_MAX; e.row0[x] = 0; e.h[x] = 0; }
+      plan.groups[g] = e;
+    }
+    return;
+  }
+  const int ta = head_pairs ? g : 2 * g;
+  const int tb = head_pairs ? g : 2 * g + 1;
+  const int2 A = plan.tiles[ta];
+  const int2 B = (tb < ntiles) ? plan.tiles[tb] : make_int2(A.x + A.y, 0);
+  const int x = (ROWS == 2 * kBlockM) ? (t >> 7) : 0;
+  const int r = t & (kBlockM - 1);
+  const int2 tile = x ? B : A;
+  const bool in_tile = r < tile.y;
+  const long long row = static_cast<long long>(tile.x) + r;
+  int lo = 1, hi = 0, doc = 0;
+  if (in_tile) {
+    lo = plan.row_lo[row];
+    hi = plan.row_hi[row];
+    doc = plan.row_doc[row];
+  }
+  const bool valid = in_tile && lo <= hi && doc >= 0;
+  unsigned long long key = valid ? ((static_cast<unsigned long long>(doc) << 32) | static_cast<unsigned>(hi)) : ~0ull;
+  int buf = 0;
+  for (int k = 2; k <= ROWS; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      unsigned long long other;
+      if (j >= 32) {
+        xbuf[buf][t] = key;
+        __syncthreads();
+        other = xbuf[buf][t ^ j];
+        buf ^= 1;
+      } else {
+        other = __shfl_xor_sync(0xffffffffu, key, j);
+      }
+      const bool up = ((t & k) == 0);
+      const bool lower = ((t & j) == 0);
+      key = (lower == up) ? (key < other ? key : other) : (key > other ? key : other);
+    }
+  }
+  xbuf[buf][t] = key;
+  __syncthreads();
+  const unsigned long long nxt = (t + 1 < ROWS) ? xbuf[buf][t + 1] : ~0ull;
+  const bool last = (key != ~0ull) && ((nxt >> 32) != (key >> 32));
+  int my_lo = 0, my_hi = -1, my_blocks = 0;
+  if (last) {
+    const int d = static_cast<int>(key >> 32);
+    my_lo = max(cup[d], 0);
+    my_hi = static_cast<int>(key & 0xffffffffu);
+    my_blocks = (my_hi - my_lo + kBlockN) / kBlockN;
+  }
+  const unsigned ballot = __ballot_sync(0xffffffffu, last);
+  if (lane == 0) warp_sum[wid] = __popc(ballot);
+  int blocks = my_blocks;
+  int vlo = valid ? lo : INT_MIN;
+  int vhi = valid ? hi : INT_MAX;
+  for (int o = 16; o > 0; o >>= 1) {
+    blocks += __shfl_xor_sync(0xffffffffu, blocks, o);
+    vlo = max(vlo, __shfl_xor_sync(0xffffffffu, vlo, o));
+    vhi = min(vhi, __shfl_xor_sync(0xffffffffu, vhi, o));
+  }
+  if (lane == 0) { red_blocks[wid] = blocks; red_lo[wid] = vlo; red_hi[wid] = vhi; }
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < wid; ++w) base += warp_sum[w];
+  if (last) {
+    const int slot = base + __popc(ballot & ((1u << lane) - 1u));
+    plan.intervals[static_cast<long long>(g) * ROWS + slot] = make_int2(my_lo, my_hi);
+  }
+  if (t == 0) {
+    FwdGroup gi;
+    gi.n_intervals = 0;
+    gi.n_blocks = 0;
+    for (int y = 0; y < 2; ++y) { gi.max_lo[y] = INT_MIN; gi.min_hi[y] = INT_MAX; }
+    for (int w = 0; w < kWarps; ++w) {
+      gi.n_intervals += warp_sum[w];
+      gi.n_blocks += red_blocks[w];
+      const int y = (w * 32) / kBlockM;  // tile of this warp's rows
+      gi.max_lo[y] = max(gi.max_lo[y], red_lo[w]);
+      gi.min_hi[y] = min(gi.min_hi[y], red_hi[w]);
+    }
+    gi.row0[0] = A.x;
+    gi.h[0] = A.y;
+    if (ROWS == kBlockM) {
+      gi.max_lo[1] = gi.max_lo[0];
+      gi.min_hi[1] = gi.min_hi[0];
+      gi.row0[1] = A.x;
+      gi.h[1] = A.y;
+    } else {
+      gi.row0[1] = B.x;
+      gi.h[1] = B.y;
+    }
+    plan.groups[g] = gi;
+  }
+}
+
+}  // namespace cpthd

@@ -268,7 +268,7 @@ CPTHD_API int thd_causal_attn_bwd(const int32_t* q_slice_idx_dev, int64_t t_loca
  * device memory (a host framework that owns all allocations, a plugin that
  * must not call cudaMalloc mid-step, a path that may never enter an
  * allocator). The pages have no counterpart: this is a deployment variant.
- * Instead of a caller workspace it uses a fixed 4 MiB device array built into
+ * Instead of a caller workspace it uses a fixed 8 MiB device array built into
  * the library, which every GPU that loads the library holds until the
  * process exits; the call allocates nothing. That is enough for slices of at
  * least 250,000 query rows; a larger slice is rejected with
