@@ -292,15 +292,9 @@ class Strategy:
         rb = hq * d * 2 + 3 * 8
         self.reorder_bytes = tl * (2 * rb + 4)
         # launches per rank: partition index 1, one gather of Q and the three
-        # id tensors 1, the attention plan 3 (rows, tiles, groups) + 1 (group
-        # order, when the plan can hold more work items than the GPU has SMs),
-        # the attention kernel 1
-        head_pairs = (hq // cfg.hkv) % 2 == 0
-        max_tiles = 2 * (-(-tl // 128)) + 1
-        max_groups = max_tiles if head_pairs else (max_tiles + 1) // 2
-        items = max_groups * (hq // 2 if head_pairs else hq)
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        self.launches_per_rank = 6 + (1 if items > sms else 0)
+        # id tensors 1, the attention plan 3 (rows, tiles, groups with their
+        # order), the attention kernel 1
+        self.launches_per_rank = 6
 
     def run_prep(self, cp, r):
         # The rank's index list, then one gather of Q and the three id

@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sV = smem + L::kVOff;
 
   __shared__ uint64_t q_full[2], q_free[2], k_full[kStages], v_full[kStages];
-  __shared__ uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
+  __shared__ uint64_t s_full[2][kStages], p_full[2], o_final[2], o_free[2];
   __shared__ uint64_t item_full[2], item_empty[2], drain[1];
   __shared__ int item_slot[2];
   __shared__ int wg_item[2];
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&q_full[x], 1);
       mbar_init(&q_free[x], 1);   // the thread that stores tile x's output
-      mbar_init(&s_full[x], 1);
+      for (int s = 0; s < kStages; ++s) mbar_init(&s_full[x][s], 1);  // scores of tile x, key blocks of stage s
       mbar_init(&p_full[x], 5);   // four softmax warps and the data relay
       mbar_init(&o_final[x], 1);
       mbar_init(&o_free[x], 4);   // the four softmax warps of tile x
@@ -206,13 +206,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         item_slot[k & 1] = item;
         mbar_arrive(&item_full[k & 1]);
         if (item < 0) break;
-        next = static_cast<int>(gridDim.x) + atomicAdd(p.ctrl + 2, 1);
         const int group = item_group(item);
         const int head0 = item_head0(item);
         const int kvh = head0 / gqa;
         const FwdGroup* gi = p.groups + group;
         const int n_blocks = min(max(gi->n_blocks, 0), p.max_blocks);
-        if (n_blocks == 0) continue;
+        if (n_blocks == 0) {
+          next = static_cast<int>(gridDim.x) + atomicAdd(p.ctrl + 2, 1);
+          continue;
+        }
         const int2* group_iv = p.intervals + static_cast<long long>(group) * p.group_rows;
         const int n_iv = min(max(gi->n_intervals, 0), p.group_rows);
 #pragma unroll
@@ -231,24 +233,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         cur.init(group_iv, n_iv);
         for (int i = 0; i < n_blocks; ++i, ++b) {
           const int st = b & 1;
-          // Stages are released through tile B's score barrier: its phase c
-          // completes when every MMA issued up to S_B(c) is done (one thread
-          // issues them all, tile B last), so phase b - 2 frees K_{b-2} and
-          // phase b - 1 frees V_{b-2}. Each phase is waited for once, in
-          // order (phase 0 before K_2, then phase b - 1 before V_b; K_b for
-          // b >= 3 needs phase b - 2, already seen before V_{b-1}).
-          if (b == kStages && !mbar_wait(&s_full[1], 0, &abort_flag)) { ok = false; break; }
+          // Stages are released through tile B's score barriers, one per
+          // stage: the commit after S_B(c) goes to s_full[1][c & 1] and
+          // reports every MMA issued up to it (one thread issues them all,
+          // tile B last). So S_B(b - 2) done frees K_{b-2} (same stage) and
+          // S_B(b - 1) done frees V_{b-2} (P V of block b - 2 is issued before
+          // S(b - 1)). The phase after the one waited for is S_B(b) for K and
+          // S_B(b + 1) for V, which need K_b and K_{b+1}: loads this thread
+          // has not issued yet. So no barrier is ever two phases past a wait,
+          // however long the producer stalls between items, and the parity
+          // is unambiguous.
+          if (b >= kStages && !mbar_wait(&s_full[1][st], ((b - 2) >> 1) & 1, &abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&k_full[st], L::kKV);
           for (int c = 0; c < L::kChunks; ++c)
             tma_load_3d(sK + st * L::kKV + c * L::kChunk, &tm_k, &k_full[st], c * 64, kvh, cur.start);
           issued = 2 * b + 1;
-          if (b >= kStages && !mbar_wait(&s_full[1], (b - 1) & 1, &abort_flag)) { ok = false; break; }
+          if (b >= kStages && !mbar_wait(&s_full[1][st ^ 1], ((b - 1) >> 1) & 1, &abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&v_full[st], L::kKV);
           for (int c = 0; c < L::kChunks; ++c)
             tma_load_3d(sV + st * L::kKV + c * L::kChunk, &tm_v, &v_full[st], c * 64, kvh, cur.start);
           issued = 2 * b + 2;
           cur.next();
         }
+        // The next item is claimed only now, two key blocks before this one
+        // ends (the ring holds two), so that items go to the CTAs that are
+        // about to be free: the costliest-first order then balances the SMs
+        // as a greedy schedule does. Claiming at the item's start would hand
+        // out items round-robin, whatever their cost.
+        next = static_cast<int>(gridDim.x) + atomicAdd(p.ctrl + 2, 1);
       }
       if (abort_flag) {
         // let every copy still in flight land before the CTA exits
@@ -315,9 +327,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (ok) {
             tc_fence_after_sync();
             issue_s(b, 0);
-            umma_commit(&s_full[0]);
+            umma_commit(&s_full[0][b & 1]);
             issue_s(b, 1);
-            umma_commit(&s_full[1]);
+            umma_commit(&s_full[1][b & 1]);
           }
           for (int j = 0; ok && j < n_blocks; ++j) {
             const int bb = b + j;
@@ -332,7 +344,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               issue_pv(bb, x, j > 0 ? 1u : 0u);
               if (more) {
                 issue_s(bb + 1, x);
-                umma_commit(&s_full[x]);  // also reports O_x += P_x(bb) V_bb done
+                umma_commit(&s_full[x][(bb + 1) & 1]);  // also reports O_x += P_x(bb) V_bb done
               } else {
                 umma_commit(&o_final[x]);  // tile x's epilogue need not wait for the other tile
                 finals |= 1 << x;
@@ -414,30 +426,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
       named_bar_sync(bar_id, 128);
-      const int item = wg_item[x];
-      if (item < 0) break;
-      const int group = item_group(item);
-      const int head0 = item_head0(item);
-      const int qh = p.head_pairs ? head0 + x : head0;
-      const FwdGroup* gi = p.groups + group;
-      const int n_blocks = min(max(gi->n_blocks, 0), p.max_blocks);
-      const int2* group_iv = p.intervals + static_cast<long long>(group) * p.group_rows;
-      const int n_iv = min(max(gi->n_intervals, 0), p.group_rows);
-      const int row0 = gi->row0[x];
-      const int h = min(max(gi->h[x], 0), kBlockM);
-      const int tmax_lo = gi->max_lo[x], tmin_hi = gi->min_hi[x];
-      const bool in_tile = r < h;
-      const long long grow = static_cast<long long>(row0) + r;
-      int lo = 1, hi = 0;
-      if (in_tile) {
-        lo = p.row_lo[grow];
-        hi = p.row_hi[grow];
+      int n_blocks, lo = 1, hi = 0, tmax_lo, tmin_hi;
+      BlockCursor cur;
+      {
+        const int item = wg_item[x];
+        if (item < 0) break;
+        const int group = item_group(item);
+        const FwdGroup* gi = p.groups + group;
+        n_blocks = min(max(gi->n_blocks, 0), p.max_blocks);
+        cur.init(p.intervals + static_cast<long long>(group) * p.group_rows,
+                 min(max(gi->n_intervals, 0), p.group_rows));
+        tmax_lo = gi->max_lo[x];
+        tmin_hi = gi->min_hi[x];
+        if (r < min(max(gi->h[x], 0), kBlockM)) {
+          lo = p.row_lo[static_cast<long long>(gi->row0[x]) + r];
+          hi = p.row_hi[static_cast<long long>(gi->row0[x]) + r];
+        }
       }
-      const bool valid = in_tile && (lo <= hi);
       float m = -INFINITY;  // running max of scale*log2(e)*s
       float l = 0.f;
-      BlockCursor cur;
-      cur.init(group_iv, n_iv);
       bool ok = true;
       for (int j = 0; j < n_blocks; ++j) {
         const int bb = b + j;
@@ -446,7 +453,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int kstart = cur.start;
         const int kend = cur.end;
         cur.next();
-        if (!warp_wait(&s_full[x], bb & 1, &abort_flag)) { ok = false; break; }
+        if (!warp_wait(&s_full[x][bb & 1], (bb >> 1) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after_sync();
         uint32_t sr[kBlockN];
         tmem_ld128(t_s, sr);
@@ -464,7 +471,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // it (c_lo > c_hi). Anything else can only come from offsets the
           // plan has already reported; such a row uses no key of the block,
           // so it never reaches a key before its own start.
-          if (c_lo > 0 && c_lo <= c_hi) record_error(p.err, CPTHD_ERR_BAD_OFFSETS, grow);
+          if (c_lo > 0 && c_lo <= c_hi) record_error(p.err, CPTHD_ERR_BAD_OFFSETS, kstart);
           row_dead = (c_lo > 0) || (c_hi < 0);
           if (row_dead) c_hi = -1;
           // bounds over the warp's live rows (a warp whose rows straddle a
@@ -564,6 +571,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (lane == 0) mbar_arrive(&p_full[x]);
       }
       b += n_blocks;
+      // The tile's rows and head are read again here rather than kept
+      // through the block loop, whose registers the scores fill.
+      const int item = wg_item[x];
+      const FwdGroup* gi = p.groups + item_group(item);
+      const int qh = p.head_pairs ? item_head0(item) + x : item_head0(item);
+      const int row0 = gi->row0[x];
+      const int h = min(max(gi->h[x], 0), kBlockM);
+      const bool in_tile = r < h;
+      const long long grow = static_cast<long long>(row0) + r;
+      const bool valid = in_tile && (lo <= hi);
       // ---------------------------------------------------------- epilogue
       // O / l in bf16 goes into this tile's Q buffer (free once o_final[x] is
       // reported: the last MMA reading it is done) in the 128-byte swizzle of
@@ -700,10 +717,11 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
 }
 
 // Whether the plan orders the groups: when there are more work items than
-// SMs (the attention grid's CTAs take items in that order).
+// SMs (the attention grid's CTAs take items in that order) and the groups
+// fit the sort.
 static bool plan_ordered(const FwdShape& shape, int Hq) {
   const long long items = shape.max_groups * (shape.head_pairs ? Hq / 2 : Hq);
-  return items > sm_count();
+  return items > sm_count() && shape.max_groups <= kMaxSortGroups;
 }
 
 }  // namespace cpthd
@@ -739,18 +757,22 @@ static int launch_plan(const IndexGen& slots, long long t_local, long long T, co
                             slots, t_local, cu, cup, num_docs, T, plan, err));
   CPTHD_TRY_CUDA(launch_pdl(attn_tiles_kernel, dim3(1), dim3(1024), 0, s, t_local, shape.max_tiles,
                             shape.head_pairs, plan, err));
+  // The costliest groups go first when there are more work items than SMs:
+  // the group kernel's last block sorts them (a power-of-two key buffer in
+  // dynamic shared memory); plans too large for the sort keep index order.
+  int sort_n = 0;
+  if (plan_ordered(shape, Hq) && shape.max_groups <= kMaxSortGroups) {
+    sort_n = 1;
+    while (sort_n < shape.max_groups) sort_n <<= 1;
+  }
+  const size_t sort_bytes = sizeof(unsigned) * static_cast<size_t>(sort_n);
   if (shape.head_pairs) {
     CPTHD_TRY_CUDA(launch_pdl(attn_fwd_group_kernel<kBlockM>, dim3(static_cast<unsigned>(shape.max_groups)),
-                              dim3(kBlockM), 0, s, 1, cup, plan));
+                              dim3(kBlockM), sort_bytes, s, 1, cup, plan, sort_n));
   } else {
     CPTHD_TRY_CUDA(launch_pdl(attn_fwd_group_kernel<2 * kBlockM>, dim3(static_cast<unsigned>(shape.max_groups)),
-                              dim3(2 * kBlockM), 0, s, 0, cup, plan));
+                              dim3(2 * kBlockM), sort_bytes, s, 0, cup, plan, sort_n));
   }
-  // The costliest groups go first when there are more work items than SMs.
-  if (plan_ordered(shape, Hq))
-    CPTHD_TRY_CUDA(launch_pdl(attn_group_order_kernel, dim3(1), dim3(1024), 0, s,
-                              static_cast<int>(shape.max_groups), &plan.groups[0].n_blocks,
-                              static_cast<int>(sizeof(FwdGroup) / sizeof(int)), plan.order));
   return CPTHD_OK;
 }
 

@@ -19,16 +19,17 @@
 // 2 * ceil(n / 128) + 1 tiles; buffers and grids are sized by that bound.
 //
 // Kernels, in stream order (all launched by thd_causal_attn_plan):
-//  1. attn_rows_kernel: per local row, its document and key interval; also
-//     checks the offset table.
-//  2. attn_tiles_kernel (one block): the runs and the greedy cut into tiles.
+//  1. attn_rows_kernel: per local row, its document and key interval, and
+//     whether it starts a run; also checks the offset table.
+//  2. attn_tiles_kernel (one block): the run starts in order and the greedy
+//     cut into tiles.
 //  3. attn_fwd_group_kernel: per group (one tile under two query heads when
 //     the GQA group size is even, else two consecutive tiles under one head)
 //     the union of its rows' intervals, one per document, sorted; its cost
 //     in 128-key blocks; and per tile the bounds inside which a key block
-//     needs no mask.
-//  4. attn_group_order_kernel (when the grid has more items than SMs): the
-//     groups by decreasing cost.
+//     needs no mask. When the attention grid has more work items than SMs,
+//     the block that finishes last also writes the groups' order by
+//     decreasing cost (a greedy schedule of the costliest first).
 #pragma once
 
 #include "attn_meta.cuh"
@@ -50,8 +51,10 @@ struct FwdPlan {
   int32_t* row_hi;     // [n] last allowed key slot
   int32_t* row_doc;    // [n] document of the row's slot, -1 when the slot is out of range
   int32_t* seg;        // [n] first rows of the document runs (scratch of the tile kernel)
+  uint32_t* run_bits;  // [ceil(n / 32)] bit r of word w: row 32 w + r starts a run
   int2* tiles;         // [max_tiles] (first row, rows)
-  int32_t* ctrl;       // [0] tiles, [1] groups, [2] next work item, [3] attention CTAs finished
+  int32_t* ctrl;       // [0] tiles, [1] groups, [2] next work item, [3] attention CTAs finished,
+                       // [4] group blocks finished
   FwdGroup* groups;    // [max_groups]
   int2* intervals;     // [max_groups * group_rows] (start, end) inclusive, per group
   int32_t* order;      // [max_groups]
@@ -78,6 +81,7 @@ inline FwdShape fwd_shape(long long n, int Hq, int Hkv) {
 inline size_t fwd_plan_bytes(const FwdShape& s) {
   size_t b = 0;
   b += 4 * align256(sizeof(int32_t) * s.n);
+  b += align256(sizeof(uint32_t) * ((s.n + 31) / 32));
   b += align256(sizeof(int2) * s.max_tiles);
   b += align256(sizeof(int32_t) * 8);
   b += align256(sizeof(FwdGroup) * s.max_groups);
@@ -93,6 +97,7 @@ inline FwdPlan carve_fwd_plan(void* base, const FwdShape& s) {
   w.row_hi = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * s.n);
   w.row_doc = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * s.n);
   w.seg = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * s.n);
+  w.run_bits = reinterpret_cast<uint32_t*>(p); p += align256(sizeof(uint32_t) * ((s.n + 31) / 32));
   w.tiles = reinterpret_cast<int2*>(p); p += align256(sizeof(int2) * s.max_tiles);
   w.ctrl = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * 8);
   w.groups = reinterpret_cast<FwdGroup*>(p); p += align256(sizeof(FwdGroup) * s.max_groups);
@@ -102,19 +107,34 @@ inline FwdPlan carve_fwd_plan(void* base, const FwdShape& s) {
 }
 
 // 1. One thread per local row: the row's physical slot (from the slice's
-// index list or the partition formulas), its document and its key interval.
-// The blocks also check the document table (offsets start at 0 and never
+// index list or the partition formulas), its document and its key interval,
+// and whether the row starts a run of equal documents (its document differs
+// from the row before it); each warp writes those 32 flags as one word. The
+// blocks also check the document table (offsets start at 0 and never
 // decrease, padded offsets end at T, L_j <= P_j, and under a computed
 // DualChunkSwap slice every padded length is a multiple of 2*cp_size) in a
 // grid-stride loop over documents.
+static __device__ __forceinline__ int row_document(const IndexGen& slots, long long row, const int32_t* cup,
+                                                   int num_docs, long long T) {
+  const int p = slots.at(row);
+  return (p < 0 || p >= T) ? -1 : upper_bound_doc(cup, num_docs, p);
+}
+
 static __global__ void __launch_bounds__(256) attn_rows_kernel(IndexGen slots, long long n,
                                                                const int32_t* __restrict__ cu,
                                                                const int32_t* __restrict__ cup, int num_docs,
                                                                long long T, FwdPlan plan, int32_t* err) {
+  __shared__ int warp_last_doc[8];
   grid_dependency_wait();
   grid_dependents_launch();
   const long long i = blockIdx.x * 256LL + threadIdx.x;
-  const int p = (i < n) ? slots.at(i) : 0;  // issued before the checks below
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const bool in = i < n;
+  const int p = in ? slots.at(i) : 0;  // issued before the checks below
+  // the document of the row before this block's first row (a run may go on
+  // across the block boundary)
+  int doc_before_block = -2;
+  if (threadIdx.x == 0 && i > 0 && in) doc_before_block = row_document(slots, i - 1, cup, num_docs, T);
   for (long long j = i; j <= num_docs; j += static_cast<long long>(gridDim.x) * 256) {
     if (j == 0 && (cu[0] != 0 || cup[0] != 0)) record_error(err, CPTHD_ERR_BAD_OFFSETS, 0);
     if (j == num_docs && cup[j] != T) record_error(err, CPTHD_ERR_BAD_OFFSETS, j);
@@ -127,48 +147,59 @@ static __global__ void __launch_bounds__(256) attn_rows_kernel(IndexGen slots, l
         record_error(err, CPTHD_ERR_NOT_DIVISIBLE, j);
     }
   }
-  if (i >= n) return;
   int lo = 1, hi = 0, doc = -1;  // empty interval
-  if (p < 0 || p >= T) {
-    record_error(err, CPTHD_ERR_INDEX_RANGE, i);
-  } else {
-    doc = upper_bound_doc(cup, num_docs, p);
-    const int start = cup[doc];
-    const int L = cu[doc + 1] - cu[doc];
-    const int pos = p - start;
-    // start >= 0 is re-checked so that malformed offsets can never widen an
-    // interval beyond [0, T)
-    if (pos >= 0 && pos < L && start >= 0) { lo = start; hi = p; }
+  if (in) {
+    if (p < 0 || p >= T) {
+      record_error(err, CPTHD_ERR_INDEX_RANGE, i);
+    } else {
+      doc = upper_bound_doc(cup, num_docs, p);
+      const int start = cup[doc];
+      const int L = cu[doc + 1] - cu[doc];
+      const int pos = p - start;
+      // start >= 0 is re-checked so that malformed offsets can never widen
+      // an interval beyond [0, T)
+      if (pos >= 0 && pos < L && start >= 0) { lo = start; hi = p; }
+    }
+    plan.row_lo[i] = lo;
+    plan.row_hi[i] = hi;
+    plan.row_doc[i] = doc;
   }
-  plan.row_lo[i] = lo;
-  plan.row_hi[i] = hi;
-  plan.row_doc[i] = doc;
+  // run starts: compare with the row before (same warp: a shuffle; the
+  // previous warp's last row: shared memory; the previous block: the
+  // document computed above)
+  int before = __shfl_up_sync(0xffffffffu, doc, 1);
+  if (lane == 31) warp_last_doc[wid] = doc;
+  __syncthreads();
+  if (lane == 0) before = (wid > 0) ? warp_last_doc[wid - 1] : doc_before_block;
+  const bool starts = in && (i == 0 || doc != before);
+  const unsigned bits = __ballot_sync(0xffffffffu, starts);
+  if (lane == 0 && i < n) plan.run_bits[i >> 5] = bits;
 }
 
-// 2. One block of 1024 threads: the runs of equal documents (each thread
-// scans a contiguous share of the rows; a block-wide scan places the run
-// starts in order), then one thread cuts the runs into tiles greedily as
-// described at the top of this file and writes the tile and group counts.
-// It also clears the attention kernel's work counters.
+// 2. One block of 1024 threads: the run starts (the set bits of the flag
+// words, each thread taking a contiguous share of the words; a block-wide
+// scan places them in row order), then one thread cuts the runs into tiles
+// greedily as described at the top of this file and writes the tile and
+// group counts. It also clears the attention kernel's work counters and the
+// group kernel's completion count.
+constexpr int kRunsInShared = 4096;  // run starts the tile kernel keeps in shared memory for its greedy walk
+
 static __global__ void __launch_bounds__(1024) attn_tiles_kernel(long long n, long long max_tiles, int head_pairs,
                                                                  FwdPlan plan, int32_t* err) {
   __shared__ int warp_total[32];
   __shared__ int block_total;
+  __shared__ int run_start[kRunsInShared];
   grid_dependency_wait();
   grid_dependents_launch();
   const int t = threadIdx.x;
   const int lane = t & 31, wid = t >> 5;
-  const long long per = (n + 1023) / 1024;
-  const long long a = min(n, t * per);
-  const long long b = min(n, a + per);
+  const long long words = (n + 31) / 32;
+  const long long per = (words + 1023) / 1024;
+  const long long a = min(words, t * per);
+  const long long b = min(words, a + per);
   int count = 0;
-  int prev = (a > 0 && a < n) ? plan.row_doc[a - 1] : 0;
-  for (long long i = a; i < b; ++i) {
-    const int d = plan.row_doc[i];
-    if (i == 0 || d != prev) ++count;
-    prev = d;
-  }
-  // exclusive scan of the per-thread counts in thread order
+  for (long long w = a; w < b; ++w) count += __popc(plan.run_bits[w]);
+  // exclusive scan of the per-thread counts in thread (= row) order
   int incl = count;
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
@@ -177,7 +208,7 @@ static __global__ void __launch_bounds__(1024) attn_tiles_kernel(long long n, lo
   if (lane == 31) warp_total[wid] = incl;
   __syncthreads();
   if (wid == 0) {
-    int w = warp_total[lane];
+    const int w = warp_total[lane];
     int wi = w;
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, wi, o);
@@ -188,15 +219,20 @@ static __global__ void __launch_bounds__(1024) attn_tiles_kernel(long long n, lo
   }
   __syncthreads();
   int pos = warp_total[wid] + incl - count;
-  prev = (a > 0 && a < n) ? plan.row_doc[a - 1] : 0;
-  for (long long i = a; i < b; ++i) {
-    const int d = plan.row_doc[i];
-    if (i == 0 || d != prev) plan.seg[pos++] = static_cast<int32_t>(i);
-    prev = d;
+  for (long long w = a; w < b; ++w) {
+    unsigned bits = plan.run_bits[w];
+    while (bits) {
+      const int row = static_cast<int>(w * 32) + __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (pos < kRunsInShared) run_start[pos] = row;
+      plan.seg[pos++] = row;
+    }
   }
   __syncthreads();  // the run starts written above are visible to thread 0
   if (t != 0) return;
   const int runs = block_total;
+  // the walk reads the run starts from shared memory when they fit
+  auto seg_at = [&](int k) -> long long { return k < kRunsInShared ? run_start[k] : plan.seg[k]; };
   long long nt = 0;
   long long cur0 = 0;
   int curh = 0;
@@ -205,8 +241,8 @@ static __global__ void __launch_bounds__(1024) attn_tiles_kernel(long long n, lo
     ++nt;
   };
   for (int k = 0; k < runs; ++k) {
-    const long long s = plan.seg[k];
-    const long long e = (k + 1 < runs) ? static_cast<long long>(plan.seg[k + 1]) : n;
+    const long long s = seg_at(k);
+    const long long e = (k + 1 < runs) ? seg_at(k + 1) : n;
     const long long len = e - s;
     const int head = static_cast<int>(len % kBlockM);
     const long long full = len / kBlockM;
@@ -235,6 +271,7 @@ static __global__ void __launch_bounds__(1024) attn_tiles_kernel(long long n, lo
   plan.ctrl[1] = static_cast<int>(head_pairs ? nt : (nt + 1) / 2);
   plan.ctrl[2] = 0;
   plan.ctrl[3] = 0;
+  plan.ctrl[4] = 0;
 }
 
 // 3. One block of ROWS threads per group (grid: max_groups): thread t owns
@@ -243,32 +280,16 @@ static __global__ void __launch_bounds__(1024) attn_tiles_kernel(long long n, lo
 // end) with a bitonic sort (partners closer than 32 rows exchange through
 // warp shuffles, the rest through shared memory), and the last row of each
 // document gives that document's interval [cup[j], its largest slot].
+// The intervals and record of real group g (the body of attn_fwd_group_kernel).
 template <int ROWS>
-static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(int head_pairs, const int32_t* __restrict__ cup,
-                                                                     FwdPlan plan) {
+static __device__ __forceinline__ void group_intervals(int head_pairs, const int32_t* __restrict__ cup,
+                                                       const FwdPlan& plan, int g,
+                                                       unsigned long long (&xbuf)[2][ROWS], int* warp_sum,
+                                                       int* red_blocks, int* red_lo, int* red_hi) {
   constexpr int kWarps = ROWS / 32;
-  __shared__ unsigned long long xbuf[2][ROWS];
-  __shared__ int warp_sum[kWarps];
-  __shared__ int red_blocks[kWarps];
-  __shared__ int red_lo[kWarps];
-  __shared__ int red_hi[kWarps];
-  grid_dependency_wait();
-  grid_dependents_launch();
   const int t = threadIdx.x;
   const int lane = t & 31, wid = t >> 5;
-  const int g = blockIdx.x;
   const int ntiles = plan.ctrl[0];
-  const int ngroups = plan.ctrl[1];
-  if (g >= ngroups) {
-    if (t == 0) {
-      FwdGroup e;
-      e.n_intervals = 0;
-      e.n_blocks = 0;
-      for (int x = 0; x < 2; ++x) { e.max_lo[x] = INT_MIN; e.min_hi[x] = INT_MAX; e.row0[x] = 0; e.h[x] = 0; }
-      plan.groups[g] = e;
-    }
-    return;
-  }
   const int ta = head_pairs ? g : 2 * g;
   const int tb = head_pairs ? g : 2 * g + 1;
   const int2 A = plan.tiles[ta];
@@ -357,6 +378,80 @@ static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(int head_pa
     }
     plan.groups[g] = gi;
   }
+}
+
+
+// The block that finishes last then writes the LPT order of the groups
+// (decreasing cost, ties by index, so unused groups come last) when
+// sort_n > 0: a bitonic sort of sort_n (a power of two >= the grid) keys in
+// dynamic shared memory.
+template <int ROWS>
+static __device__ void order_groups_last_block(const FwdPlan& plan, int ngroups_total, int sort_n) {
+  extern __shared__ unsigned sort_keys[];
+  const int t = threadIdx.x;
+  for (int i = t; i < sort_n; i += ROWS) {
+    if (i < ngroups_total) {
+      const int c = __ldcg(&plan.groups[i].n_blocks);  // written by other blocks: read past L1
+      const unsigned cost = static_cast<unsigned>(min(max(c, 0), (1 << 18) - 1));
+      sort_keys[i] = ((cost ^ 0x3ffffu) << 13) | static_cast<unsigned>(i);
+    } else {
+      sort_keys[i] = 0xffffffffu;
+    }
+  }
+  __syncthreads();
+  for (int k = 2; k <= sort_n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = t; i < sort_n; i += ROWS) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned a = sort_keys[i], b = sort_keys[ixj];
+          const bool up = ((i & k) == 0);
+          if ((a > b) == up) { sort_keys[i] = b; sort_keys[ixj] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = t; i < ngroups_total; i += ROWS) plan.order[i] = static_cast<int>(sort_keys[i] & 0x1fffu);
+}
+
+template <int ROWS>
+static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(int head_pairs, const int32_t* __restrict__ cup,
+                                                                     FwdPlan plan, int sort_n) {
+  constexpr int kWarps = ROWS / 32;
+  __shared__ unsigned long long xbuf[2][ROWS];
+  __shared__ int warp_sum[kWarps];
+  __shared__ int red_blocks[kWarps];
+  __shared__ int red_lo[kWarps];
+  __shared__ int red_hi[kWarps];
+  __shared__ int is_last;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int t = threadIdx.x;
+  const int g = blockIdx.x;
+  const int ngroups = plan.ctrl[1];
+  if (g >= ngroups) {
+    if (t == 0) {
+      FwdGroup e;
+      e.n_intervals = 0;
+      e.n_blocks = 0;
+      for (int x = 0; x < 2; ++x) { e.max_lo[x] = INT_MIN; e.min_hi[x] = INT_MAX; e.row0[x] = 0; e.h[x] = 0; }
+      plan.groups[g] = e;
+    }
+  } else {
+    group_intervals<ROWS>(head_pairs, cup, plan, g, xbuf, warp_sum, red_blocks, red_lo, red_hi);
+  }
+  if (sort_n == 0) return;
+  // every block counts itself done; the last one orders the groups
+  __syncthreads();
+  if (t == 0) {
+    __threadfence();
+    is_last = (atomicAdd(plan.ctrl + 4, 1) == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  order_groups_last_block<ROWS>(plan, static_cast<int>(gridDim.x), sort_n);
 }
 
 }  // namespace cpthd
