@@ -292,9 +292,9 @@ class Strategy:
         rb = hq * d * 2 + 3 * 8
         self.reorder_bytes = tl * (2 * rb + 4)
         # launches per rank: partition index 1, one gather of Q and the three
-        # id tensors 1, the attention plan 3 (rows, tiles, groups with their
-        # order), the attention kernel 1
-        self.launches_per_rank = 6
+        # id tensors 1, the attention plan 2 (rows; groups with their tiles
+        # and order), the attention kernel 1
+        self.launches_per_rank = 5
 
     def run_prep(self, cp, r):
         # The rank's index list, then one gather of Q and the three id

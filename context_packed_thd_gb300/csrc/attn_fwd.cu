@@ -743,8 +743,9 @@ static int check_workspace(int64_t t_local, int Hq, int Hkv, const void* workspa
   return CPTHD_OK;
 }
 
-// The plan of the slice's rows (rows, tiles, groups and, past one wave,
-// their order) into the workspace; shape and workspace already checked.
+// The plan of the slice (rows, then the groups: their tiles, intervals and,
+// past one wave of work items, their order) into the workspace; shape and
+// workspace already checked.
 static int launch_plan(const IndexGen& slots, long long t_local, long long T, const int32_t* cu,
                        const int32_t* cup, int num_docs, int Hq, int Hkv, void* workspace, int32_t* err,
                        cudaStream_t s) {
@@ -755,8 +756,6 @@ static int launch_plan(const IndexGen& slots, long long t_local, long long T, co
   if (shape.max_groups > INT32_MAX / 2) return CPTHD_ERR_UNSUPPORTED;
   CPTHD_TRY_CUDA(launch_pdl(attn_rows_kernel, dim3(static_cast<unsigned>((t_local + 255) / 256)), dim3(256), 0, s,
                             slots, t_local, cu, cup, num_docs, T, plan, err));
-  CPTHD_TRY_CUDA(launch_pdl(attn_tiles_kernel, dim3(1), dim3(1024), 0, s, t_local, shape.max_tiles,
-                            shape.head_pairs, plan, err));
   // The costliest groups go first when there are more work items than SMs:
   // the group kernel's last block sorts them (a power-of-two key buffer in
   // dynamic shared memory); plans too large for the sort keep index order.
@@ -768,10 +767,11 @@ static int launch_plan(const IndexGen& slots, long long t_local, long long T, co
   const size_t sort_bytes = sizeof(unsigned) * static_cast<size_t>(sort_n);
   if (shape.head_pairs) {
     CPTHD_TRY_CUDA(launch_pdl(attn_fwd_group_kernel<kBlockM>, dim3(static_cast<unsigned>(shape.max_groups)),
-                              dim3(kBlockM), sort_bytes, s, 1, cup, plan, sort_n));
+                              dim3(kBlockM), sort_bytes, s, t_local, shape.max_tiles, 1, cup, plan, sort_n, err));
   } else {
     CPTHD_TRY_CUDA(launch_pdl(attn_fwd_group_kernel<2 * kBlockM>, dim3(static_cast<unsigned>(shape.max_groups)),
-                              dim3(2 * kBlockM), sort_bytes, s, 0, cup, plan, sort_n));
+                              dim3(2 * kBlockM), sort_bytes, s, t_local, shape.max_tiles, 0, cup, plan, sort_n,
+                              err));
   }
   return CPTHD_OK;
 }

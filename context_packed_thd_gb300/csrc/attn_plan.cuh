@@ -18,12 +18,13 @@
 // then hold more than 128 rows together, so a slice of n rows has at most
 // 2 * ceil(n / 128) + 1 tiles; buffers and grids are sized by that bound.
 //
-// Kernels, in stream order (all launched by thd_causal_attn_plan):
+// Kernels, in stream order (both launched by thd_causal_attn_plan):
 //  1. attn_rows_kernel: per local row, its document and key interval, and
 //     whether it starts a run; also checks the offset table.
-//  2. attn_tiles_kernel (one block): the run starts in order and the greedy
-//     cut into tiles.
-//  3. attn_fwd_group_kernel: per group (one tile under two query heads when
+//  2. attn_fwd_group_kernel: each block finds its own group's tiles (the run
+//     starts in order, then the greedy cut, walked until they are known;
+//     block 0 walks to the end and publishes the counts), then, per group
+//     (one tile under two query heads when
 //     the GQA group size is even, else two consecutive tiles under one head)
 //     the union of its rows' intervals, one per document, sorted; its cost
 //     in 128-key blocks; and per tile the bounds inside which a key block
@@ -50,11 +51,10 @@ struct FwdPlan {
   int32_t* row_lo;     // [n] first allowed key slot of each local row (empty: lo > hi)
   int32_t* row_hi;     // [n] last allowed key slot
   int32_t* row_doc;    // [n] document of the row's slot, -1 when the slot is out of range
-  int32_t* seg;        // [n] first rows of the document runs (scratch of the tile kernel)
+  int32_t* seg;        // [n] run starts past the group blocks' shared copy (scratch)
   uint32_t* run_bits;  // [ceil(n / 32)] bit r of word w: row 32 w + r starts a run
-  int2* tiles;         // [max_tiles] (first row, rows)
   int32_t* ctrl;       // [0] tiles, [1] groups, [2] next work item, [3] attention CTAs finished,
-                       // [4] group blocks finished
+                       // [4] group blocks finished (cleared by the rows kernel)
   FwdGroup* groups;    // [max_groups]
   int2* intervals;     // [max_groups * group_rows] (start, end) inclusive, per group
   int32_t* order;      // [max_groups]
@@ -82,7 +82,6 @@ inline size_t fwd_plan_bytes(const FwdShape& s) {
   size_t b = 0;
   b += 4 * align256(sizeof(int32_t) * s.n);
   b += align256(sizeof(uint32_t) * ((s.n + 31) / 32));
-  b += align256(sizeof(int2) * s.max_tiles);
   b += align256(sizeof(int32_t) * 8);
   b += align256(sizeof(FwdGroup) * s.max_groups);
   b += align256(sizeof(int2) * s.max_groups * s.group_rows);
@@ -98,7 +97,6 @@ inline FwdPlan carve_fwd_plan(void* base, const FwdShape& s) {
   w.row_doc = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * s.n);
   w.seg = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * s.n);
   w.run_bits = reinterpret_cast<uint32_t*>(p); p += align256(sizeof(uint32_t) * ((s.n + 31) / 32));
-  w.tiles = reinterpret_cast<int2*>(p); p += align256(sizeof(int2) * s.max_tiles);
   w.ctrl = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * 8);
   w.groups = reinterpret_cast<FwdGroup*>(p); p += align256(sizeof(FwdGroup) * s.max_groups);
   w.intervals = reinterpret_cast<int2*>(p); p += align256(sizeof(int2) * s.max_groups * s.group_rows);
@@ -147,6 +145,9 @@ static __global__ void __launch_bounds__(256) attn_rows_kernel(IndexGen slots, l
         record_error(err, CPTHD_ERR_NOT_DIVISIBLE, j);
     }
   }
+  // the group kernel's completion count starts at zero (it counts blocks
+  // only after this kernel has finished)
+  if (i == 0) plan.ctrl[4] = 0;
   int lo = 1, hi = 0, doc = -1;  // empty interval
   if (in) {
     if (p < 0 || p >= T) {
@@ -176,104 +177,6 @@ static __global__ void __launch_bounds__(256) attn_rows_kernel(IndexGen slots, l
   if (lane == 0 && i < n) plan.run_bits[i >> 5] = bits;
 }
 
-// 2. One block of 1024 threads: the run starts (the set bits of the flag
-// words, each thread taking a contiguous share of the words; a block-wide
-// scan places them in row order), then one thread cuts the runs into tiles
-// greedily as described at the top of this file and writes the tile and
-// group counts. It also clears the attention kernel's work counters and the
-// group kernel's completion count.
-constexpr int kRunsInShared = 4096;  // run starts the tile kernel keeps in shared memory for its greedy walk
-
-static __global__ void __launch_bounds__(1024) attn_tiles_kernel(long long n, long long max_tiles, int head_pairs,
-                                                                 FwdPlan plan, int32_t* err) {
-  __shared__ int warp_total[32];
-  __shared__ int block_total;
-  __shared__ int run_start[kRunsInShared];
-  grid_dependency_wait();
-  grid_dependents_launch();
-  const int t = threadIdx.x;
-  const int lane = t & 31, wid = t >> 5;
-  const long long words = (n + 31) / 32;
-  const long long per = (words + 1023) / 1024;
-  const long long a = min(words, t * per);
-  const long long b = min(words, a + per);
-  int count = 0;
-  for (long long w = a; w < b; ++w) count += __popc(plan.run_bits[w]);
-  // exclusive scan of the per-thread counts in thread (= row) order
-  int incl = count;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_total[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    const int w = warp_total[lane];
-    int wi = w;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += v;
-    }
-    warp_total[lane] = wi - w;  // exclusive prefix of the warps
-    if (lane == 31) block_total = wi;
-  }
-  __syncthreads();
-  int pos = warp_total[wid] + incl - count;
-  for (long long w = a; w < b; ++w) {
-    unsigned bits = plan.run_bits[w];
-    while (bits) {
-      const int row = static_cast<int>(w * 32) + __ffs(bits) - 1;
-      bits &= bits - 1;
-      if (pos < kRunsInShared) run_start[pos] = row;
-      plan.seg[pos++] = row;
-    }
-  }
-  __syncthreads();  // the run starts written above are visible to thread 0
-  if (t != 0) return;
-  const int runs = block_total;
-  // the walk reads the run starts from shared memory when they fit
-  auto seg_at = [&](int k) -> long long { return k < kRunsInShared ? run_start[k] : plan.seg[k]; };
-  long long nt = 0;
-  long long cur0 = 0;
-  int curh = 0;
-  auto emit = [&](long long r0, int h) {
-    if (nt < max_tiles) plan.tiles[nt] = make_int2(static_cast<int>(r0), h);
-    ++nt;
-  };
-  for (int k = 0; k < runs; ++k) {
-    const long long s = seg_at(k);
-    const long long e = (k + 1 < runs) ? seg_at(k + 1) : n;
-    const long long len = e - s;
-    const int head = static_cast<int>(len % kBlockM);
-    const long long full = len / kBlockM;
-    if (head > 0) {
-      if (curh > 0 && curh + head <= kBlockM) {
-        curh += head;  // packed with the short runs before it (rows are contiguous)
-      } else {
-        if (curh > 0) emit(cur0, curh);
-        cur0 = s;
-        curh = head;
-      }
-    }
-    if (full > 0) {
-      if (curh > 0) { emit(cur0, curh); curh = 0; }
-      for (long long f = 0; f < full; ++f) emit(s + head + kBlockM * f, kBlockM);
-    }
-  }
-  if (curh > 0) emit(cur0, curh);
-  // The bound holds for every input (any two consecutive tiles hold more
-  // than 128 rows); were it ever exceeded, the missing rows are reported.
-  if (nt > max_tiles) {
-    record_error(err, CPTHD_ERR_INDEX_RANGE, nt);
-    nt = max_tiles;
-  }
-  plan.ctrl[0] = static_cast<int>(nt);
-  plan.ctrl[1] = static_cast<int>(head_pairs ? nt : (nt + 1) / 2);
-  plan.ctrl[2] = 0;
-  plan.ctrl[3] = 0;
-  plan.ctrl[4] = 0;
-}
-
 // 3. One block of ROWS threads per group (grid: max_groups): thread t owns
 // row t of tile A (t < 128) or row t - 128 of tile B. Groups past the
 // count get an empty record. The rows' intervals are sorted by (document,
@@ -282,18 +185,12 @@ static __global__ void __launch_bounds__(1024) attn_tiles_kernel(long long n, lo
 // document gives that document's interval [cup[j], its largest slot].
 // The intervals and record of real group g (the body of attn_fwd_group_kernel).
 template <int ROWS>
-static __device__ __forceinline__ void group_intervals(int head_pairs, const int32_t* __restrict__ cup,
-                                                       const FwdPlan& plan, int g,
-                                                       unsigned long long (&xbuf)[2][ROWS], int* warp_sum,
-                                                       int* red_blocks, int* red_lo, int* red_hi) {
+static __device__ __forceinline__ void group_intervals(const int32_t* __restrict__ cup, const FwdPlan& plan, int g,
+                                                       int2 A, int2 B, unsigned long long (&xbuf)[2][ROWS],
+                                                       int* warp_sum, int* red_blocks, int* red_lo, int* red_hi) {
   constexpr int kWarps = ROWS / 32;
   const int t = threadIdx.x;
   const int lane = t & 31, wid = t >> 5;
-  const int ntiles = plan.ctrl[0];
-  const int ta = head_pairs ? g : 2 * g;
-  const int tb = head_pairs ? g : 2 * g + 1;
-  const int2 A = plan.tiles[ta];
-  const int2 B = (tb < ntiles) ? plan.tiles[tb] : make_int2(A.x + A.y, 0);
   const int x = (ROWS == 2 * kBlockM) ? (t >> 7) : 0;
   const int r = t & (kBlockM - 1);
   const int2 tile = x ? B : A;
@@ -415,22 +312,145 @@ static __device__ void order_groups_last_block(const FwdPlan& plan, int ngroups_
   for (int i = t; i < ngroups_total; i += ROWS) plan.order[i] = static_cast<int>(sort_keys[i] & 0x1fffu);
 }
 
+constexpr int kRunsInShared = 4096;  // run starts a group block keeps in shared memory for the greedy walk
+
+// The tiles of group g (tile indices ta and tb), found by the group's own
+// block: the run starts (the set bits of the rows kernel's flag words) in
+// row order, each thread taking a contiguous share of the words and a
+// block-wide scan placing them, then the greedy cut described at the top of
+// this file, walked by thread 0 only until the group's tiles are known
+// (block 0 walks to the end and publishes the tile and group counts). Runs
+// past kRunsInShared also go to the global run list; every block writes the
+// same values there.
 template <int ROWS>
-static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(int head_pairs, const int32_t* __restrict__ cup,
-                                                                     FwdPlan plan, int sort_n) {
+static __device__ void find_group_tiles(long long n, long long max_tiles, int head_pairs, const FwdPlan& plan,
+                                        int g, int* run_start, int* warp_total, int* sh, int2* tiles_out,
+                                        int32_t* err) {
   constexpr int kWarps = ROWS / 32;
+  const int t = threadIdx.x;
+  const int lane = t & 31, wid = t >> 5;
+  const long long words = (n + 31) / 32;
+  const long long per = (words + ROWS - 1) / ROWS;
+  const long long a = min(words, t * per);
+  const long long b = min(words, a + per);
+  int count = 0;
+  for (long long w = a; w < b; ++w) count += __popc(plan.run_bits[w]);
+  int incl = count;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_total[wid] = incl;
+  __syncthreads();
+  if (t == 0) {
+    int acc = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int x = warp_total[w];
+      warp_total[w] = acc;
+      acc += x;
+    }
+    sh[0] = acc;  // runs
+  }
+  __syncthreads();
+  const int runs = sh[0];
+  int pos = warp_total[wid] + incl - count;
+  for (long long w = a; w < b; ++w) {
+    unsigned bits = plan.run_bits[w];
+    while (bits) {
+      const int row = static_cast<int>(w * 32) + __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (pos < kRunsInShared) run_start[pos] = row;
+      else plan.seg[pos] = row;
+      ++pos;
+    }
+  }
+  __syncthreads();  // the run starts above are visible to thread 0
+  if (t == 0) {
+    auto run_at = [&](int k) -> long long { return k < kRunsInShared ? run_start[k] : plan.seg[k]; };
+    const long long ta = head_pairs ? g : 2LL * g;
+    const long long tb = head_pairs ? g : 2LL * g + 1;
+    int2 A = make_int2(0, 0), B = make_int2(0, 0);
+    long long nt = 0;
+    auto emit = [&](long long r0, int h) {
+      if (nt == ta) A = make_int2(static_cast<int>(r0), h);
+      if (nt == tb) B = make_int2(static_cast<int>(r0), h);
+      ++nt;
+    };
+    long long cur0 = 0;
+    int curh = 0;
+    for (int k = 0; k < runs; ++k) {
+      const long long st = run_at(k);
+      const long long e = (k + 1 < runs) ? run_at(k + 1) : n;
+      const long long len = e - st;
+      const int head = static_cast<int>(len % kBlockM);
+      const long long full = len / kBlockM;
+      if (head > 0) {
+        if (curh > 0 && curh + head <= kBlockM) {
+          curh += head;  // packed with the short runs before it (rows are contiguous)
+        } else {
+          if (curh > 0) emit(cur0, curh);
+          cur0 = st;
+          curh = head;
+        }
+      }
+      if (full > 0) {
+        if (curh > 0) {
+          emit(cur0, curh);
+          curh = 0;
+        }
+        // the run's full tiles are nt .. nt + full - 1; only this group's
+        // (ta, tb) are written
+        for (long long x = (ta > nt ? ta : nt); x <= tb && x < nt + full; ++x) {
+          const int2 tile = make_int2(static_cast<int>(st + head + kBlockM * (x - nt)), kBlockM);
+          if (x == ta) A = tile;
+          if (x == tb) B = tile;
+        }
+        nt += full;
+      }
+      if (g != 0 && nt > tb) break;  // this group's tiles are known
+    }
+    if (curh > 0 && (g == 0 || nt <= tb)) emit(cur0, curh);
+    if (g == 0) {
+      // The bound holds for every input (any two consecutive tiles hold more
+      // than 128 rows); were it ever exceeded, the groups past it are lost
+      // and that is reported.
+      if (nt > max_tiles) {
+        record_error(err, CPTHD_ERR_INDEX_RANGE, nt);
+        nt = max_tiles;
+      }
+      plan.ctrl[0] = static_cast<int>(nt);
+      plan.ctrl[1] = static_cast<int>(head_pairs ? nt : (nt + 1) / 2);
+      plan.ctrl[2] = 0;
+      plan.ctrl[3] = 0;
+    }
+    const bool real = ta < nt;
+    if (tb >= nt) B = make_int2(A.x + A.y, 0);  // no second tile
+    tiles_out[0] = A;
+    tiles_out[1] = B;
+    sh[1] = real ? 1 : 0;
+  }
+  __syncthreads();
+}
+
+template <int ROWS>
+static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(long long n, long long max_tiles, int head_pairs,
+                                                                     const int32_t* __restrict__ cup, FwdPlan plan,
+                                                                     int sort_n, int32_t* err) {
   __shared__ unsigned long long xbuf[2][ROWS];
-  __shared__ int warp_sum[kWarps];
-  __shared__ int red_blocks[kWarps];
-  __shared__ int red_lo[kWarps];
-  __shared__ int red_hi[kWarps];
+  __shared__ int warp_sum[ROWS / 32];
+  __shared__ int red_blocks[ROWS / 32];
+  __shared__ int red_lo[ROWS / 32];
+  __shared__ int red_hi[ROWS / 32];
+  __shared__ int run_start[kRunsInShared];
+  __shared__ int2 tiles[2];
+  __shared__ int sh[2];
   __shared__ int is_last;
   grid_dependency_wait();
   grid_dependents_launch();
   const int t = threadIdx.x;
   const int g = blockIdx.x;
-  const int ngroups = plan.ctrl[1];
-  if (g >= ngroups) {
+  find_group_tiles<ROWS>(n, max_tiles, head_pairs, plan, g, run_start, warp_sum, sh, tiles, err);
+  if (sh[1] == 0) {
     if (t == 0) {
       FwdGroup e;
       e.n_intervals = 0;
@@ -439,7 +459,7 @@ static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(int head_pa
       plan.groups[g] = e;
     }
   } else {
-    group_intervals<ROWS>(head_pairs, cup, plan, g, xbuf, warp_sum, red_blocks, red_lo, red_hi);
+    group_intervals<ROWS>(cup, plan, g, tiles[0], tiles[1], xbuf, warp_sum, red_blocks, red_lo, red_hi);
   }
   if (sort_n == 0) return;
   // every block counts itself done; the last one orders the groups
