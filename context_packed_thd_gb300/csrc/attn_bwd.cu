@@ -19,7 +19,8 @@
 //    buffers let S(j+1) and dQ(j) run while the elementwise warps work.
 //  * dK/dV pass, one CTA per (128-key tile, KV head), over every query tile
 //    whose key intervals reach the key tile and every query head of the
-//    group: S^T = K Q^T and dP^T = V dO^T into TMEM, the elementwise warps
+//    group (a key tile no query reaches gets zeros, so dK/dV need no
+//    clearing pass): S^T = K Q^T and dP^T = V dO^T into TMEM, the elementwise warps
 //    write P^T and then dS^T (bf16) back over them in two phases, and
 //    dV += P^T dO and dK += dS^T Q, both accumulated in TMEM and written
 //    once, run during the other phase.
@@ -656,6 +657,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok && n_items > 0) ok = warp_wait(&kv_final, 0, &abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after_sync();
+    if (ok && n_items == 0 && key < p.T) {
+      // no query of the slice reaches these keys: their contribution is zero
+      // (written here, so the call needs no separate clearing pass)
+      float4* dv4 = reinterpret_cast<float4*>(p.dv + (static_cast<long long>(key) * p.Hkv + g) * D);
+      float4* dk4 = reinterpret_cast<float4*>(p.dk + (static_cast<long long>(key) * p.Hkv + g) * D);
+#pragma unroll 8
+      for (int q = 0; q < D / 4; ++q) {
+        dv4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dk4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
     if (ok && n_items > 0) {
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -788,10 +800,13 @@ extern "C" int thd_causal_attn_bwd(const int32_t* q_slice_idx_dev, int64_t t_loc
       return CPTHD_ERR_WORKSPACE;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // this rank's dK/dV contribution: keys its queries do not reach stay zero
-  CPTHD_TRY_CUDA(cudaMemsetAsync(dk_dev, 0, sizeof(float) * static_cast<size_t>(T) * Hkv * d, s));
-  CPTHD_TRY_CUDA(cudaMemsetAsync(dv_dev, 0, sizeof(float) * static_cast<size_t>(T) * Hkv * d, s));
-  if (t_local == 0) return CPTHD_OK;
+  // An empty slice contributes nothing: dK/dV are zero. Otherwise the dK/dV
+  // pass writes every key tile, zeros where no query of the slice reaches.
+  if (t_local == 0) {
+    CPTHD_TRY_CUDA(cudaMemsetAsync(dk_dev, 0, sizeof(float) * static_cast<size_t>(T) * Hkv * d, s));
+    CPTHD_TRY_CUDA(cudaMemsetAsync(dv_dev, 0, sizeof(float) * static_cast<size_t>(T) * Hkv * d, s));
+    return CPTHD_OK;
+  }
   const int32_t* cup = cu_seqlens_padded_dev ? cu_seqlens_padded_dev : cu_seqlens_dev;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
   AttnWorkspace ws = carve_workspace(workspace_dev, ntiles, kBlockM);

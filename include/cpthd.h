@@ -251,7 +251,7 @@ CPTHD_API int thd_causal_attn_bwd_workspace_size(int64_t t_local, int Hq, int Hk
  *   dq_dev: fp32 [t_local, Hq, d].
  *   dk_dev, dv_dev: fp32 [T, Hkv, d] for the whole K/V buffer, holding this
  *     rank's contribution (the part a reduce-scatter over CP ranks would sum);
- *     the call zeroes them first, so keys no query of the slice reaches get 0.
+ *     every key is written, so keys no query of the slice reaches get 0.
  *   workspace_dev: thd_causal_attn_bwd_workspace_size() bytes, 256-byte aligned.
  * Supported: d in {64, 128}; Hq % Hkv == 0; t_local <= 262,144 (2048 query
  * tiles). Host errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. Device
