@@ -44,8 +44,8 @@ struct BwdSmem {
   static constexpr int kCol = 4 * kBlockM * 4;    // row_lo, row_hi, lse2, D of 128 query rows
   // dQ pass: Q, dO, K[3], V[2]
   static constexpr int kDqBytes = 7 * kTile;
-  // dK/dV pass: K, V, Q[2], dO[2], column info[2], tile list
-  static constexpr int kDkvBytes = 6 * kTile + 2 * kCol + kBwdMaxTiles * 4;
+  // dK/dV pass: K, V, Q[2], dO[2], column info[2], two tile lists
+  static constexpr int kDkvBytes = 6 * kTile + 2 * kCol + 2 * kBwdMaxTiles * 4;
   static constexpr int launch(int b) { return (b + 1024 > 120 * 1024) ? b + 1024 : 120 * 1024; }
 };
 
@@ -60,11 +60,13 @@ struct BwdParams {
   float* dq;
   float* dk;
   float* dv;
+  int32_t* work;  // dK/dV pass: [0] next work item (cleared by the pre-pass)
   long long t_local;
   long long T;
   int Hq;
   int Hkv;
   int ntiles;
+  int n_key_tiles;
   int rows_pad;
   int max_blocks;
   float scale;
@@ -79,7 +81,9 @@ template <int D>
 static __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
                                                                   const __nv_bfloat16* __restrict__ dout,
                                                                   const float* __restrict__ lse, long long t_local,
-                                                                  int Hq, int rows_pad, float* lse2, float* dvec) {
+                                                                  int Hq, int rows_pad, float* lse2, float* dvec,
+                                                                  int32_t* work) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) work[0] = 0;  // the dK/dV pass's work counter
   const long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= (long long)rows_pad * Hq) return;
@@ -369,6 +373,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // --------------------------------------------------------------- dK/dV pass
+// Persistent: one CTA per SM takes work items (128-key tile kt, KV head g):
+// the first is its block index, the rest come from a counter (cleared by
+// the pre-pass), claimed after the item's last Q/dO load. Work items run in
+// key-tile order, the costliest first for causal slices (early keys are
+// reached by the most query tiles).
+// Roles: warp 0 builds each item's list of query tiles whose key intervals
+// reach [kt*128, kt*128+127] (32 lanes with ballots, in tile order) into one
+// of two list buffers and publishes the item; its lane 0 then loads K and V
+// (once the previous item's last scores are issued: kv_empty) and the Q / dO
+// tiles with their row data through a two-stage ring (numbered over all of
+// the CTA's items). Warp 1 issues the MMAs; an item's first dV / dK MMA waits
+// until the elementwise warps have read the previous item's dV / dK from TMEM
+// (acc_free). Warps 2-5 run the elementwise phases and the epilogue; an item
+// that no query reaches gets zeros.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -382,52 +400,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sQ = smem + 2 * L::kTile;   // two stages
   uint8_t* sDO = smem + 4 * L::kTile;  // two stages
   uint8_t* sCol = smem + 6 * L::kTile; // two stages of {row_lo, row_hi, lse2, D} x 128
-  int* sList = reinterpret_cast<int*>(sCol + 2 * L::kCol);
-  __shared__ uint8_t sFull[kBwdMaxTiles];  // every real row of the listed tile sees all 128 keys
+  int* sList = reinterpret_cast<int*>(sCol + 2 * L::kCol);  // two lists of kBwdMaxTiles
+  __shared__ uint8_t sFull[2][kBwdMaxTiles];  // every real row of the listed tile sees all 128 keys
 
-  __shared__ uint64_t kv_full, qdo_full[2], qdo_empty[2], sdp_full[2], pds_full[2], kv_final, drain;
+  __shared__ uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2], sdp_full[2], pds_full[2], kv_final, acc_free;
+  __shared__ uint64_t item_full[2], item_empty[2], drain;
+  __shared__ int item_slot[2], list_n[2];
   __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_flag, list_n;
+  __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kt = blockIdx.x / p.Hkv;
-  const int g = blockIdx.x % p.Hkv;
   const int group = p.Hq / p.Hkv;
-  const int K0 = kt * kBlockN;
-
-  // query tiles whose key intervals reach [K0, K0 + 127]
-  if (threadIdx.x == 0) list_n = 0;
-  __syncthreads();
-  for (int t = threadIdx.x; t < p.ntiles; t += blockDim.x) {
-    const GroupInfo ti = p.tile_info[t];
-    const int n_iv = min(max(ti.n_intervals, 0), kBlockM);
-    const int2* iv = p.intervals + static_cast<long long>(t) * kBlockM;
-    bool rel = false;
-    for (int k = 0; k < n_iv && !rel; ++k) {
-      const int2 a = iv[k];
-      rel = (a.x <= K0 + kBlockN - 1) && (a.y >= K0);
-    }
-    if (rel) {
-      const int slot = atomicAdd(&list_n, 1);
-      if (slot < kBwdMaxTiles) {
-        sList[slot] = t;
-        sFull[slot] = (ti.max_lo[0] <= K0 && ti.min_hi[0] >= K0 + kBlockN - 1) ? 1 : 0;
-      }
-    }
-  }
-  __syncthreads();
-  const int n_items = min(list_n, kBwdMaxTiles) * group;
+  const int n_work = p.n_key_tiles * p.Hkv;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&kv_full, 1);
+    mbar_init(&kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&qdo_full[s], 1);
       mbar_init(&qdo_empty[s], 1);
       mbar_init(&sdp_full[s], 1);
       mbar_init(&pds_full[s], 4);
+      mbar_init(&item_full[s], 1);
+      mbar_init(&item_empty[s], 5);  // the MMA issuer and the four elementwise warps
     }
     mbar_init(&kv_final, 1);
+    mbar_init(&acc_free, 4);
     mbar_init(&drain, 1);
     fence_mbar_init();
   }
@@ -438,48 +437,110 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  // S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D). An item
-  // (query tile, head) is processed as two halves of 64 queries: half x uses
-  // columns [64x, 64x+64) of S^T and dP^T, its P^T / dS^T (bf16) go to the
-  // first 32 of them. Once a half's dV / dK MMAs are issued, the next item's
-  // scores for that half can be computed while the elementwise warps work on
-  // the other half.
+  // S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
   const uint32_t tmem = tmem_base_sh;
+  // the item's list length, from the published slot (items past the end: -1)
+  auto items_of = [&](int slot) { return min(list_n[slot], kBwdMaxTiles) * group; };
 
   if (warp == 0) {
-    if (lane == 0 && n_items > 0) {
-      mbar_arrive_expect_tx(&kv_full, 2 * L::kTile);
-      for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_3d(sK + c * L::kChunk, &tm_k, &kv_full, c * 64, g, K0);
-        tma_load_3d(sV + c * L::kChunk, &tm_v, &kv_full, c * 64, g, K0);
+    // ------------------------------------------------------------ producer
+    int next = blockIdx.x;
+    int ig = 0;   // Q/dO items loaded so far, over all work items
+    int nkv = 0;  // K/V loads so far
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      if (k >= 2) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&item_empty[slot], ((k >> 1) - 1) & 1, &abort_flag);
+        if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) break;
       }
-      int issued = 0;
-      for (int i = 0; i < n_items; ++i) {
-        const int st = i & 1;
-        const int t = sList[i / group];
-        const int h = g * group + i % group;
-        if (i >= 2 && !mbar_wait(&qdo_empty[st], ((i >> 1) + 1) & 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&qdo_full[st], 2 * L::kTile + L::kCol);
-        for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_3d(sQ + st * L::kTile + c * L::kChunk, &tm_q, &qdo_full[st], c * 64, h, t * kBlockM);
-          tma_load_3d(sDO + st * L::kTile + c * L::kChunk, &tm_do, &qdo_full[st], c * 64, h, t * kBlockM);
+      const int item = (next < n_work) ? next : -1;
+      int count = 0;
+      if (item >= 0) {
+        // query tiles whose key intervals reach this key tile, in tile order
+        const int K0 = (item / p.Hkv) * kBlockN;
+        for (int base = 0; base < p.ntiles; base += 32) {
+          const int t = base + lane;
+          bool rel = false, full = false;
+          if (t < p.ntiles) {
+            const GroupInfo ti = p.tile_info[t];
+            const int n_iv = min(max(ti.n_intervals, 0), kBlockM);
+            const int2* iv = p.intervals + static_cast<long long>(t) * kBlockM;
+            for (int q = 0; q < n_iv && !rel; ++q) {
+              const int2 a = iv[q];
+              rel = (a.x <= K0 + kBlockN - 1) && (a.y >= K0);
+            }
+            full = (ti.max_lo[0] <= K0 && ti.min_hi[0] >= K0 + kBlockN - 1);
+          }
+          const unsigned ballot = __ballot_sync(0xffffffffu, rel);
+          const int pos = count + __popc(ballot & ((1u << lane) - 1u));
+          if (rel && pos < kBwdMaxTiles) {
+            sList[slot * kBwdMaxTiles + pos] = t;
+            sFull[slot][pos] = full ? 1 : 0;
+          }
+          count += __popc(ballot);
         }
-        uint8_t* col = sCol + st * L::kCol;
-        const long long r0 = static_cast<long long>(t) * kBlockM;
-        const long long hr = static_cast<long long>(h) * p.rows_pad + r0;
-        bulk_load(col, p.row_lo + r0, kBlockM * 4, &qdo_full[st]);
-        bulk_load(col + kBlockM * 4, p.row_hi + r0, kBlockM * 4, &qdo_full[st]);
-        bulk_load(col + 2 * kBlockM * 4, p.lse2 + hr, kBlockM * 4, &qdo_full[st]);
-        bulk_load(col + 3 * kBlockM * 4, p.dvec + hr, kBlockM * 4, &qdo_full[st]);
-        issued = i + 1;
       }
-      if (abort_flag) {
-        mbar_wait_drain(&kv_full, 0);
-        for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) mbar_wait_drain(&qdo_full[i & 1], (i >> 1) & 1);
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) {
+        item_slot[slot] = item;
+        list_n[slot] = count;
+        mbar_arrive(&item_full[slot]);
       }
+      if (item < 0) break;
+      const int n_items = min(count, kBwdMaxTiles) * group;
+      if (lane == 0 && n_items > 0) {
+        const int kt = item / p.Hkv, g = item % p.Hkv;
+        const int K0 = kt * kBlockN;
+        // K and V of the previous item are read by its last S^T / dP^T
+        if (nkv > 0 && !mbar_wait(&kv_empty, (nkv - 1) & 1, &abort_flag)) ok = false;
+        if (ok) {
+          mbar_arrive_expect_tx(&kv_full, 2 * L::kTile);
+          for (int c = 0; c < L::kChunks; ++c) {
+            tma_load_3d(sK + c * L::kChunk, &tm_k, &kv_full, c * 64, g, K0);
+            tma_load_3d(sV + c * L::kChunk, &tm_v, &kv_full, c * 64, g, K0);
+          }
+          ++nkv;
+        }
+        for (int i = 0; ok && i < n_items; ++i, ++ig) {
+          const int st = ig & 1;
+          const int t = sList[slot * kBwdMaxTiles + i / group];
+          const int h = g * group + i % group;
+          // Q / dO stage st is free once dK of the item two before is done;
+          // that barrier's next phase needs this load, so the parity is
+          // unambiguous however far behind this thread runs
+          if (ig >= 2 && !mbar_wait(&qdo_empty[st], ((ig >> 1) - 1) & 1, &abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&qdo_full[st], 2 * L::kTile + L::kCol);
+          for (int c = 0; c < L::kChunks; ++c) {
+            tma_load_3d(sQ + st * L::kTile + c * L::kChunk, &tm_q, &qdo_full[st], c * 64, h, t * kBlockM);
+            tma_load_3d(sDO + st * L::kTile + c * L::kChunk, &tm_do, &qdo_full[st], c * 64, h, t * kBlockM);
+          }
+          uint8_t* col = sCol + st * L::kCol;
+          const long long r0 = static_cast<long long>(t) * kBlockM;
+          const long long hr = static_cast<long long>(h) * p.rows_pad + r0;
+          bulk_load(col, p.row_lo + r0, kBlockM * 4, &qdo_full[st]);
+          bulk_load(col + kBlockM * 4, p.row_hi + r0, kBlockM * 4, &qdo_full[st]);
+          bulk_load(col + 2 * kBlockM * 4, p.lse2 + hr, kBlockM * 4, &qdo_full[st]);
+          bulk_load(col + 3 * kBlockM * 4, p.dvec + hr, kBlockM * 4, &qdo_full[st]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      ig = __shfl_sync(0xffffffffu, ig, 0);
+      nkv = __shfl_sync(0xffffffffu, nkv, 0);
+      // the next item is claimed once this one's loads are issued
+      if (lane == 0) next = static_cast<int>(gridDim.x) + atomicAdd(p.work + 0, 1);
+      next = __shfl_sync(0xffffffffu, next, 0);
+    }
+    if (lane == 0 && abort_flag) {
+      // let every copy still in flight land before the CTA exits
+      if (nkv > 0) mbar_wait_drain(&kv_full, (nkv - 1) & 1);
+      for (int i = (ig > 2 ? ig - 2 : 0); i < ig; ++i) mbar_wait_drain(&qdo_full[i & 1], (i >> 1) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0 && n_items > 0) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t kIdO = idesc_bf16_f32(kBlockM, D, 0, 1);
       uint32_t k_lo, k_hi, v_lo, v_hi, q_lo, q_hi, do_lo, do_hi, qmn_lo, qmn_hi, domn_lo, domn_hi;
@@ -505,189 +566,244 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           umma_ss_w(tmem + 128, v_lo + off, v_hi, do_lo + so + off, do_hi, kIdS, kk > 0);
         }
       };
-      auto issue_dv = [&](int i) {  // dV += P^T dO, P^T (bf16) in [0, 64)
+      auto issue_dv = [&](int i, uint32_t acc0) {  // dV (+)= P^T dO, P^T (bf16) in [0, 64)
         const uint32_t so = ((i & 1) * L::kTile) >> 4;
 #pragma unroll
         for (int kk = 0; kk < kBlockM / 16; ++kk)
           umma_ts_w(tmem + 256, tmem + kk * 8, domn_lo + so + ((kk * 16 * 128) >> 4), domn_hi, kIdO,
-                    (i > 0 || kk > 0) ? 1u : 0u);
+                    kk > 0 ? 1u : acc0);
       };
-      auto issue_dk = [&](int i) {  // dK += dS^T Q, dS^T (bf16) in [128, 192)
+      auto issue_dk = [&](int i, uint32_t acc0) {  // dK (+)= dS^T Q, dS^T (bf16) in [128, 192)
         const uint32_t so = ((i & 1) * L::kTile) >> 4;
 #pragma unroll
         for (int kk = 0; kk < kBlockM / 16; ++kk)
           umma_ts_w(tmem + 256 + D, tmem + 128 + kk * 8, qmn_lo + so + ((kk * 16 * 128) >> 4), qmn_hi, kIdO,
-                    (i > 0 || kk > 0) ? 1u : 0u);
+                    kk > 0 ? 1u : acc0);
       };
-      bool ok = mbar_wait(&kv_full, 0, &abort_flag) && mbar_wait(&qdo_full[0], 0, &abort_flag);
-      if (ok) {
-        tc_fence_after_sync();
-        issue_s(0);
-        umma_commit(&sdp_full[0]);
-        issue_dp(0);
-        umma_commit(&sdp_full[1]);
-      }
-      for (int i = 0; ok && i < n_items; ++i) {
-        const bool more = (i + 1 < n_items);
-        // phase 1 of item i done: P^T(i) in [0, 64)
-        if (!mbar_wait(&pds_full[0], i & 1, &abort_flag)) break;
-        tc_fence_after_sync();
-        issue_dv(i);
-        if (more) {  // S^T(i+1) overwrites [0, 128) only after dV(i) (issue order)
-          if (!mbar_wait(&qdo_full[(i + 1) & 1], ((i + 1) >> 1) & 1, &abort_flag)) break;
-          tc_fence_after_sync();
-          issue_s(i + 1);
-          umma_commit(&sdp_full[0]);
+      int ig = 0, nkv = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!mbar_wait(&item_full[slot], (k >> 1) & 1, &abort_flag)) break;
+        const int item = item_slot[slot];
+        const int n_items = items_of(slot);
+        mbar_arrive(&item_empty[slot]);  // the issuer needs only the count
+        if (item < 0) break;
+        if (n_items == 0 && k > 0) {
+          // no MMA, but this item's kv_final must not come before the
+          // previous item's dV / dK have been read out of TMEM
+          if (!mbar_wait(&acc_free, (k - 1) & 1, &abort_flag)) ok = false;
         }
-        // phase 2 of item i done: dS^T(i) in [128, 192)
-        if (!mbar_wait(&pds_full[1], i & 1, &abort_flag)) break;
-        tc_fence_after_sync();
-        issue_dk(i);
-        umma_commit(&qdo_empty[i & 1]);  // Q(i), dO(i) and their column data are free
-        if (more) {  // dP^T(i+1) overwrites [128, 256) only after dK(i)
-          issue_dp(i + 1);
-          umma_commit(&sdp_full[1]);
+        if (ok && n_items > 0) {
+          ok = mbar_wait(&kv_full, nkv & 1, &abort_flag) && mbar_wait(&qdo_full[ig & 1], (ig >> 1) & 1, &abort_flag);
+          ++nkv;
+          if (ok) {
+            tc_fence_after_sync();
+            issue_s(ig);
+            umma_commit(&sdp_full[0]);
+            issue_dp(ig);
+            umma_commit(&sdp_full[1]);
+            if (n_items == 1) umma_commit(&kv_empty);  // the item's last reads of K and V are issued
+          }
+          for (int i = 0; ok && i < n_items; ++i) {
+            const int gi = ig + i;
+            const bool more = (i + 1 < n_items);
+            // the previous item's dV / dK have been read out of TMEM before
+            // this item's first dV / dK overwrite them
+            if (i == 0 && k > 0 && !mbar_wait(&acc_free, (k - 1) & 1, &abort_flag)) { ok = false; break; }
+            // phase 1 of item gi done: P^T(gi) in [0, 64)
+            if (!mbar_wait(&pds_full[0], gi & 1, &abort_flag)) { ok = false; break; }
+            tc_fence_after_sync();
+            issue_dv(gi, i > 0 ? 1u : 0u);
+            if (more) {  // S^T(gi+1) overwrites [0, 128) only after dV(gi) (issue order)
+              if (!mbar_wait(&qdo_full[(gi + 1) & 1], ((gi + 1) >> 1) & 1, &abort_flag)) { ok = false; break; }
+              tc_fence_after_sync();
+              issue_s(gi + 1);
+              umma_commit(&sdp_full[0]);
+            }
+            // phase 2 of item gi done: dS^T(gi) in [128, 192)
+            if (!mbar_wait(&pds_full[1], gi & 1, &abort_flag)) { ok = false; break; }
+            tc_fence_after_sync();
+            issue_dk(gi, i > 0 ? 1u : 0u);
+            umma_commit(&qdo_empty[gi & 1]);  // Q(gi), dO(gi) and their column data are free
+            if (more) {  // dP^T(gi+1) overwrites [128, 256) only after dK(gi)
+              issue_dp(gi + 1);
+              umma_commit(&sdp_full[1]);
+              if (i + 2 == n_items) umma_commit(&kv_empty);
+            }
+          }
+          ig += n_items;
         }
+        umma_commit(&kv_final);  // this item's dV / dK are complete (or it had none)
       }
-      umma_commit(&kv_final);
       umma_commit(&drain);
       mbar_wait_drain(&drain, 0);
     }
   } else {
-    // Elementwise, one thread per key (TMEM lane), in two phases per item:
-    // phase 1 turns S^T into P^T (bf16, over the first 64 columns of S^T) and
-    // keeps P as bf16 pairs in registers; phase 2 turns dP^T into
+    // ------------------------------------------------------------ elementwise
+    // One thread per key (TMEM lane), in two phases per query item: phase 1
+    // turns S^T into P^T (bf16, over the first 64 columns of S^T) and keeps
+    // P as bf16 pairs in registers; phase 2 turns dP^T into
     // dS^T = P (dP^T - D) (bf16, over the first 64 columns of dP^T). The
     // issuer runs dV(i) and S^T(i+1) during phase 2, and dK(i) and
     // dP^T(i+1) during the next phase 1.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const int key = K0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
     const uint32_t t_v = tmem + lane_off + 256, t_k = tmem + lane_off + 256 + D;
     const float sl2 = p.scale_log2;
+    int ig = 0;
     bool ok = true;
-    for (int i = 0; ok && i < n_items; ++i) {
-      const int st = i & 1;
-      // the column data arrived with Q/dO through the TMA barrier
-      if (!warp_wait(&qdo_full[st], (i >> 1) & 1, &abort_flag)) { ok = false; break; }
-      const int* c_lo = reinterpret_cast<const int*>(sCol + st * L::kCol);
-      const int* c_hi = c_lo + kBlockM;
-      const float* c_l2 = reinterpret_cast<const float*>(c_lo + 2 * kBlockM);
-      const float* c_d = c_l2 + kBlockM;
-      const bool item_full = sFull[i / group] != 0;
-      uint32_t pp[64];  // P of the 128 queries, bf16 pairs
-      // ---- phase 1: P = 2^(S scale log2(e) - lse2), masked
-      if (!warp_wait(&sdp_full[0], i & 1, &abort_flag)) { ok = false; break; }
-      tc_fence_after_sync();
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t sv[64];
-        tmem_ld64(t_s + 64 * c2, sv);
-        tmem_ld_wait64(sv);
-#pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4) {
-          const int col = 64 * c2 + 4 * q4;
-          const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
-          const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
-          float pv[4];
-#pragma unroll
-          for (int u = 0; u < 4; u += 2) {
-            float a0, a1;
-            fma2(a0, a1, __uint_as_float(sv[4 * q4 + u]), __uint_as_float(sv[4 * q4 + u + 1]), sl2, -l2s[u],
-                 -l2s[u + 1]);
-            pv[u] = ex2(a0);
-            pv[u + 1] = ex2(a1);
-          }
-          if (!item_full) {
-            const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
-            const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
-            const int los[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
-            const int his[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) pv[u] = (key >= los[u] && key <= his[u]) ? pv[u] : 0.f;
-          }
-          pp[32 * c2 + 2 * q4] = pack_bf16x2(pv[0], pv[1]);
-          pp[32 * c2 + 2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
-        }
-        // P^T of these 64 queries over columns 32 c2 .. 32 c2 + 31, already read
-        uint32_t (&half)[32] = *reinterpret_cast<uint32_t(*)[32]>(pp + 32 * c2);
-        tmem_st32(t_s + 32 * c2, half);
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      if (!warp_wait(&item_full[slot], (k >> 1) & 1, &abort_flag)) break;
+      const int item = item_slot[slot];
+      if (item < 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&item_empty[slot]);
+        break;
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pds_full[0]);
-      // ---- phase 2: dS = P (dP - D)
-      if (!warp_wait(&sdp_full[1], i & 1, &abort_flag)) { ok = false; break; }
-      tc_fence_after_sync();
+      const int n_items = items_of(slot);
+      const int kt = item / p.Hkv, g = item % p.Hkv;
+      const int key = kt * kBlockN + r;
+      for (int i = 0; ok && i < n_items; ++i) {
+        const int gi = ig + i;
+        const int st = gi & 1;
+        // the column data arrived with Q/dO through the TMA barrier
+        if (!warp_wait(&qdo_full[st], (gi >> 1) & 1, &abort_flag)) { ok = false; break; }
+        const int* c_lo = reinterpret_cast<const int*>(sCol + st * L::kCol);
+        const int* c_hi = c_lo + kBlockM;
+        const float* c_l2 = reinterpret_cast<const float*>(c_lo + 2 * kBlockM);
+        const float* c_d = c_l2 + kBlockM;
+        const bool item_full_keys = sFull[slot][i / group] != 0;
+        uint32_t pp[64];  // P of the 128 queries, bf16 pairs
+        // ---- phase 1: P = 2^(S scale log2(e) - lse2), masked
+        if (!warp_wait(&sdp_full[0], gi & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after_sync();
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t dp[64];
-        tmem_ld64(t_dp + 64 * c2, dp);
-        tmem_ld_wait64(dp);
-        uint32_t pd[32];
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t sv[64];
+          tmem_ld64(t_s + 64 * c2, sv);
+          tmem_ld_wait64(sv);
 #pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4) {
-          const int col = 64 * c2 + 4 * q4;
-          const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
-          const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
-          const uint32_t w0 = pp[32 * c2 + 2 * q4], w1 = pp[32 * c2 + 2 * q4 + 1];
-          const float pv[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u),
-                               __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u)};
-          float dsv[4];
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const int col = 64 * c2 + 4 * q4;
+            const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
+            const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
+            float pv[4];
 #pragma unroll
-          for (int u = 0; u < 4; u += 2) {
-            float t0, t1;
-            fma2(t0, t1, __uint_as_float(dp[4 * q4 + u]), __uint_as_float(dp[4 * q4 + u + 1]), 1.f, -ds[u],
-                 -ds[u + 1]);
-            mul2(dsv[u], dsv[u + 1], pv[u], pv[u + 1], t0, t1);
+            for (int u = 0; u < 4; u += 2) {
+              float a0, a1;
+              fma2(a0, a1, __uint_as_float(sv[4 * q4 + u]), __uint_as_float(sv[4 * q4 + u + 1]), sl2, -l2s[u],
+                   -l2s[u + 1]);
+              pv[u] = ex2(a0);
+              pv[u + 1] = ex2(a1);
+            }
+            if (!item_full_keys) {
+              const int4 lo4 = *reinterpret_cast<const int4*>(c_lo + col);
+              const int4 hi4 = *reinterpret_cast<const int4*>(c_hi + col);
+              const int los[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
+              const int his[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) pv[u] = (key >= los[u] && key <= his[u]) ? pv[u] : 0.f;
+            }
+            pp[32 * c2 + 2 * q4] = pack_bf16x2(pv[0], pv[1]);
+            pp[32 * c2 + 2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
           }
-          pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-          pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          // P^T of these 64 queries over columns 32 c2 .. 32 c2 + 31, already read
+          uint32_t (&half)[32] = *reinterpret_cast<uint32_t(*)[32]>(pp + 32 * c2);
+          tmem_st32(t_s + 32 * c2, half);
         }
-        tmem_st32(t_dp + 32 * c2, pd);  // dS^T over columns already read
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pds_full[0]);
+        // ---- phase 2: dS = P (dP - D)
+        if (!warp_wait(&sdp_full[1], gi & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t dp[64];
+          tmem_ld64(t_dp + 64 * c2, dp);
+          tmem_ld_wait64(dp);
+          uint32_t pd[32];
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const int col = 64 * c2 + 4 * q4;
+            const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
+            const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
+            const uint32_t w0 = pp[32 * c2 + 2 * q4], w1 = pp[32 * c2 + 2 * q4 + 1];
+            const float pv[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u),
+                                 __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u)};
+            float dsv[4];
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              float t0, t1;
+              fma2(t0, t1, __uint_as_float(dp[4 * q4 + u]), __uint_as_float(dp[4 * q4 + u + 1]), 1.f, -ds[u],
+                   -ds[u + 1]);
+              mul2(dsv[u], dsv[u + 1], pv[u], pv[u + 1], t0, t1);
+            }
+            pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+            pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          }
+          tmem_st32(t_dp + 32 * c2, pd);  // dS^T over columns already read
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pds_full[1]);
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pds_full[1]);
-    }
-    if (ok && n_items > 0) ok = warp_wait(&kv_final, 0, &abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after_sync();
-    if (ok && n_items == 0 && key < p.T) {
-      // no query of the slice reaches these keys: their contribution is zero
-      // (written here, so the call needs no separate clearing pass)
-      float4* dv4 = reinterpret_cast<float4*>(p.dv + (static_cast<long long>(key) * p.Hkv + g) * D);
-      float4* dk4 = reinterpret_cast<float4*>(p.dk + (static_cast<long long>(key) * p.Hkv + g) * D);
+      ig += n_items;
+      // ---- epilogue: this key tile's dV and dK (zeros when no query reaches it)
+      if (ok) ok = warp_wait(&kv_final, k & 1, &abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after_sync();
+      float* dv_row = p.dv + (static_cast<long long>(key) * p.Hkv + g) * D;
+      float* dk_row = p.dk + (static_cast<long long>(key) * p.Hkv + g) * D;
+      if (ok && n_items > 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rv[32], rk[32];
+          tmem_ld32(t_v + 32 * c, rv);
+          tmem_ld32(t_k + 32 * c, rk);
+          tmem_ld_wait(rv);
+          tmem_ld_wait(rk);
+          if (c == D / 32 - 1) {
+            // dV / dK are in registers: the next item's first MMAs may overwrite them
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_free);
+          }
+          if (key < p.T) {
+            float4* dv4 = reinterpret_cast<float4*>(dv_row + 32 * c);
+            float4* dk4 = reinterpret_cast<float4*>(dk_row + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              dv4[q] = make_float4(__uint_as_float(rv[4 * q]), __uint_as_float(rv[4 * q + 1]),
+                                   __uint_as_float(rv[4 * q + 2]), __uint_as_float(rv[4 * q + 3]));
+              dk4[q] = make_float4(__uint_as_float(rk[4 * q]) * p.scale, __uint_as_float(rk[4 * q + 1]) * p.scale,
+                                   __uint_as_float(rk[4 * q + 2]) * p.scale,
+                                   __uint_as_float(rk[4 * q + 3]) * p.scale);
+            }
+          }
+        }
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_free);
+        if (ok && key < p.T) {
+          // no query of the slice reaches these keys: their contribution is zero
+          float4* dv4 = reinterpret_cast<float4*>(dv_row);
+          float4* dk4 = reinterpret_cast<float4*>(dk_row);
 #pragma unroll 8
-      for (int q = 0; q < D / 4; ++q) {
-        dv4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        dk4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    if (ok && n_items > 0) {
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rv[32], rk[32];
-        tmem_ld32(t_v + 32 * c, rv);
-        tmem_ld32(t_k + 32 * c, rk);
-        tmem_ld_wait(rv);
-        tmem_ld_wait(rk);
-        if (key < p.T) {
-          float4* dv4 = reinterpret_cast<float4*>(p.dv + (static_cast<long long>(key) * p.Hkv + g) * D + 32 * c);
-          float4* dk4 = reinterpret_cast<float4*>(p.dk + (static_cast<long long>(key) * p.Hkv + g) * D + 32 * c);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            dv4[q] = make_float4(__uint_as_float(rv[4 * q]), __uint_as_float(rv[4 * q + 1]),
-                                 __uint_as_float(rv[4 * q + 2]), __uint_as_float(rv[4 * q + 3]));
-            dk4[q] = make_float4(__uint_as_float(rk[4 * q]) * p.scale, __uint_as_float(rk[4 * q + 1]) * p.scale,
-                                 __uint_as_float(rk[4 * q + 2]) * p.scale, __uint_as_float(rk[4 * q + 3]) * p.scale);
+          for (int q = 0; q < D / 4; ++q) {
+            dv4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            dk4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[slot]);  // done with this item's list
     }
   }
 
@@ -700,14 +816,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 static size_t bwd_workspace_bytes(long long ntiles, int Hq) {
   const long long rows_pad = ntiles * kBlockM;
-  return attn_workspace_bytes(ntiles, kBlockM) + 2 * align256(sizeof(float) * rows_pad * Hq);
+  return attn_workspace_bytes(ntiles, kBlockM) + 2 * align256(sizeof(float) * rows_pad * Hq) +
+         align256(sizeof(int32_t) * 8);
 }
 
 template <int D>
 static int launch_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
                       const float* lse, long long t_local, long long T, int Hq, int Hkv, float scale,
-                      const AttnWorkspace& ws, float* lse2, float* dvec, long long ntiles, float* dq, float* dk,
-                      float* dv, int32_t* err, cudaStream_t s) {
+                      const AttnWorkspace& ws, float* lse2, float* dvec, int32_t* work, long long ntiles, float* dq,
+                      float* dk, float* dv, int32_t* err, cudaStream_t s) {
   EncodeTiledFn enc = get_encode_tiled();
   if (enc == nullptr) return CPTHD_ERR_CUDA;
   CUtensorMap mq, mdo, mk, mv;
@@ -718,7 +835,7 @@ static int launch_bwd(const void* q, const void* k, const void* v, const void* o
   const long long warps = static_cast<long long>(rows_pad) * Hq;
   attn_bwd_pre_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, t_local, Hq, rows_pad,
-      lse2, dvec);
+      lse2, dvec, work);
   // The dQ grid runs in decreasing-cost order (the forward's group order
   // over the query tiles) when it needs more than one wave of CTAs.
   const bool ordered = ntiles * Hq > sm_count();
@@ -736,11 +853,13 @@ static int launch_bwd(const void* q, const void* k, const void* v, const void* o
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
+  p.work = work;
   p.t_local = t_local;
   p.T = T;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.ntiles = static_cast<int>(ntiles);
+  p.n_key_tiles = static_cast<int>((T + kBlockN - 1) / kBlockN);
   p.rows_pad = rows_pad;
   p.max_blocks = static_cast<int>((T + kBlockN - 1) / kBlockN + kBlockM);
   p.scale = scale;
@@ -751,8 +870,12 @@ static int launch_bwd(const void* q, const void* k, const void* v, const void* o
   CPTHD_TRY_CUDA(cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_dq));
   CPTHD_TRY_CUDA(cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv));
   attn_bwd_dq_kernel<D><<<static_cast<unsigned>(ntiles * Hq), kBwdThreads, smem_dq, s>>>(mq, mdo, mk, mv, p);
-  const long long kts = (T + kBlockN - 1) / kBlockN;
-  attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(kts * Hkv), kBwdThreads, smem_kv, s>>>(mq, mdo, mk, mv, p);
+  // persistent: one CTA per SM, taking (key tile, KV head) items
+  const long long work_items = static_cast<long long>(p.n_key_tiles) * Hkv;
+  const int sms = sm_count();
+  if (sms < 1) return CPTHD_ERR_CUDA;
+  const long long grid_kv = work_items < sms ? work_items : sms;
+  attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid_kv), kBwdThreads, smem_kv, s>>>(mq, mdo, mk, mv, p);
   CPTHD_TRY_CUDA(cudaGetLastError());
   return CPTHD_OK;
 }
@@ -813,12 +936,13 @@ extern "C" int thd_causal_attn_bwd(const int32_t* q_slice_idx_dev, int64_t t_loc
   char* extra = static_cast<char*>(workspace_dev) + attn_workspace_bytes(ntiles, kBlockM);
   float* lse2 = reinterpret_cast<float*>(extra);
   float* dvec = reinterpret_cast<float*>(extra + align256(sizeof(float) * ntiles * kBlockM * Hq));
+  int32_t* work = reinterpret_cast<int32_t*>(extra + 2 * align256(sizeof(float) * ntiles * kBlockM * Hq));
   attn_group_meta_kernel<kBlockM><<<static_cast<unsigned>(ntiles), kBlockM, 0, s>>>(
       index_list(q_slice_idx_dev), t_local, cu_seqlens_dev, cup, num_docs, T, ws, err_dev);
   CPTHD_TRY_CUDA(cudaGetLastError());
   if (d == 128)
     return launch_bwd<128>(q_dev, k_dev, v_dev, out_dev, dout_dev, lse_dev, t_local, T, Hq, Hkv, scale, ws, lse2,
-                           dvec, ntiles, dq_dev, dk_dev, dv_dev, err_dev, s);
+                           dvec, work, ntiles, dq_dev, dk_dev, dv_dev, err_dev, s);
   return launch_bwd<64>(q_dev, k_dev, v_dev, out_dev, dout_dev, lse_dev, t_local, T, Hq, Hkv, scale, ws, lse2, dvec,
-                        ntiles, dq_dev, dk_dev, dv_dev, err_dev, s);
+                        work, ntiles, dq_dev, dk_dev, dv_dev, err_dev, s);
 }

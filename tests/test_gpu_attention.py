@@ -442,3 +442,32 @@ def test_full_size_rank_every_row(name, strategy, rank):
                              ref_idx)
     assert_attn_matches(out, lse, ro, rl, f"{name}/{strategy}/rank{rank}")
     assert err.cpu().tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("permute", [False, True])
+def test_more_document_runs_than_shared_memory_holds(permute):
+    """About 10,000 one- and two-token documents in one slice (cp_size 1):
+    more document runs than the plan keeps in shared memory (4096), so the
+    group blocks walk the tile cut through the global run list; with the
+    slice's rows permuted, nearly every row is a run of its own. Every row
+    against the oracle, and the planned run bit-identical to the one call."""
+    dev = cuda_or_skip(); cp = load_lib()
+    rng = np.random.default_rng(10000 + int(permute))
+    lengths = rng.integers(1, 3, size=10000).tolist()
+    inp = _custom(lengths, 1, 4, 2, 64, 23)
+    d = DevInputs(inp, dev)
+    lay = inp.layout
+    order = rng.permutation(lay.T) if permute else np.arange(lay.T)
+    idx = torch.from_numpy(order.astype(np.int32)).to(dev)
+    err = new_err(dev)
+    q_loc = cp.cp_reorder(d.q, idx, err=err)
+    out, lse = cp.thd_causal_attn_fwd(idx, q_loc, d.k, d.v, d.cu, d.cup, err=err)
+    ws = cp.thd_causal_attn_plan(idx, lay.T, d.cu, d.cup, 4, 2, err=err)
+    o2, l2 = cp.thd_causal_attn_fwd_planned(q_loc, d.k, d.v, ws, err=err)
+    torch.cuda.synchronize()
+    assert err.cpu().tolist() == [0, 0]
+    assert torch.equal(out, o2) and torch.equal(lse, l2)
+    ref_idx = order.astype(np.int64)
+    ro, rl = A.attention_fwd(inp.q[torch.from_numpy(ref_idx)], inp.k, inp.v, lay.cu_seqlens, lay.cu_seqlens_padded,
+                             ref_idx)
+    assert_attn_matches(out, lse, ro, rl, f"10000 documents, permuted={permute}")
