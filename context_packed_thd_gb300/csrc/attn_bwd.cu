@@ -408,10 +408,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ int item_slot[2], list_n[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ int last_key_tile;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int group = p.Hq / p.Hkv;
-  const int n_work = p.n_key_tiles * p.Hkv;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -444,6 +444,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The last key tile any query of the slice reaches (a tile's intervals
+    // are sorted by document, so its last one ends at its largest slot):
+    // work items stop there, and the tiles past it are zero-filled by the
+    // whole grid after the item loop.
+    int max_end = -1;
+    for (int t = lane; t < p.ntiles; t += 32) {
+      const int n_iv = min(max(p.tile_info[t].n_intervals, 0), kBlockM);
+      if (n_iv > 0) max_end = max(max_end, min(p.intervals[static_cast<long long>(t) * kBlockM + n_iv - 1].y,
+                                              static_cast<int>(p.T) - 1));
+    }
+    max_end = __reduce_max_sync(0xffffffffu, max_end);
+    const int kt_last = (max_end < 0) ? -1 : max_end / kBlockN;
+    if (lane == 0) last_key_tile = kt_last;
+    const int n_work = (kt_last + 1) * p.Hkv;
     int next = blockIdx.x;
     int ig = 0;   // Q/dO items loaded so far, over all work items
     int nkv = 0;  // K/V loads so far
@@ -812,6 +826,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (abort_flag && threadIdx.x == 0) record_error(p.err, CPTHD_ERR_TIMEOUT, blockIdx.x);
   tc_fence_after_sync();
   if (warp == 1) tmem_dealloc(tmem, 512);
+  // keys past the last reached key tile: zeros, spread over the whole grid
+  const long long first = static_cast<long long>(last_key_tile + 1) * kBlockN;
+  if (first < p.T) {
+    const long long n4 = (p.T - first) * p.Hkv * D / 4;
+    float4* dk4 = reinterpret_cast<float4*>(p.dk + first * p.Hkv * D);
+    float4* dv4 = reinterpret_cast<float4*>(p.dv + first * p.Hkv * D);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+      dk4[i] = z;
+      dv4[i] = z;
+    }
+  }
 }
 
 static size_t bwd_workspace_bytes(long long ntiles, int Hq) {
