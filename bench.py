@@ -361,7 +361,8 @@ def _graph_ms(fn, flush, reps=5):
 def other_workloads(cp, current, dev, flush, peak, peak_sustained, hbm_peak):
     """Attention throughput of every other multi-rank workload: all ranks of
     all its strategies in one CUDA graph (L2 flushed before each replay), so
-    that the line also carries the long-context and many-document figures.
+    that the line also carries the long-context and many-document figures;
+    then the backward of every rank slice, each timed alone.
     Fractions are given of the burst and of the sustained bf16 peak: the
     long workload's graph runs tens of milliseconds of tensor work, long
     enough for the power cap to lower the clocks as in the sustained
@@ -394,6 +395,7 @@ def other_workloads(cp, current, dev, flush, peak, peak_sustained, hbm_peak):
                                         "useful_pair_frac": round(sum(st.pairs) / sum(st.kpairs), 4)}
         dcs = [st for st in sts if st.name == W.DUAL_CHUNK_SWAP]
         restore = kv_restore(cp, cfg, dcs[0], flush, hbm_peak) if dcs else None
+        bwd = backward(cp, cfg, sts, range(cfg.cp), flush, peak)
         for st in sts:
             e = st.err.cpu().tolist()
             if e[0] != 0:
@@ -405,7 +407,7 @@ def other_workloads(cp, current, dev, flush, peak, peak_sustained, hbm_peak):
                          "frac_of_sustained_peak": round(tf / peak_sustained, 4), "ms": round(ms, 4),
                          "rank_slices": cfg.cp * len(sts), "strategies": list(cfg.strategies),
                          "useful_pair_frac": round(useful, 4),
-                         "per_strategy": by_strategy or None, "kv_restore": restore}
+                         "per_strategy": by_strategy or None, "kv_restore": restore, "backward": bwd}
         del sts
         torch.cuda.empty_cache()
     return out

@@ -30,6 +30,18 @@ struct BlockCursor {
     start += kBlockN;
     if (start > end && ++k < n_iv) { int2 a = iv[k]; start = a.x; end = a.y; }
   }
+  // Moves on by nb blocks (whole intervals at a time, then within one).
+  __device__ void skip(int nb) {
+    while (nb > 0 && k < n_iv) {
+      const int left = (end >= start) ? (end - start) / kBlockN + 1 : 0;  // blocks left in this interval
+      if (nb < left) {
+        start += nb * kBlockN;
+        return;
+      }
+      nb -= left;
+      if (++k < n_iv) { int2 a = iv[k]; start = a.x; end = a.y; }
+    }
+  }
 };
 
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {

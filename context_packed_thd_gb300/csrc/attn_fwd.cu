@@ -47,10 +47,31 @@
 //                normalises O into the tile's Q buffer in shared memory and
 //                one thread stores the tile with TMA; LSE per row.
 // Key blocks start at the group's interval starts (document starts), so
-// documents the group does not see are never loaded or multiplied. The grid
-// runs the groups in decreasing-cost order. Every wait is bounded; a wait
-// that times out makes the CTA drain its copies and MMAs, free TMEM, record
-// CPTHD_ERR_TIMEOUT and return.
+// documents the group does not see are never loaded or multiplied.
+//
+// Schedule. A work item is a group under one head unit; its work is the
+// group's key blocks. The plan lays the items out in order (costliest groups
+// first when there are more items than SMs). When items are short (fewer
+// than kSharesMinMeanBlocks blocks on average) the CTAs (one per SM) take
+// whole items from a counter in that order, each claiming its next item as
+// the current one's last blocks are loaded: a greedy costliest-first
+// schedule, under which the items running together start together and share
+// their K/V blocks in L2. When items are long, a whole item per CTA leaves
+// SMs idle at the end (256 items on 152 SMs finish in two item lengths, not
+// 1.7), so each CTA instead takes an equal share of the total work (each
+// item's blocks plus a fixed cost per item). An item that crosses a share
+// boundary runs in pieces, one per
+// CTA whose share it touches, each over its own key blocks. The online
+// softmax of a piece is a partial result: its unnormalised O (fp32), the
+// row maxima m and the sums l. Every piece but the last stores those to a
+// slot of the workspace (one per share boundary and tile) and raises a flag;
+// the last piece, which the CTA runs after the rest of its share, waits for
+// the flags and combines all pieces in piece order (the standard rescaling
+// by 2^(m_i - max m)), so that results do not depend on timing. That wait
+// only ever points at CTAs of lower index whose pieces end or fill their
+// shares, and those pieces wait for nothing, so the waits cannot form a
+// cycle. Every wait is bounded; a wait that times out makes the CTA drain its
+// copies and MMAs, free TMEM, record CPTHD_ERR_TIMEOUT and return.
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
@@ -88,7 +109,13 @@ struct AttnParams {
   const FwdGroup* groups;
   const int2* intervals;
   const int32_t* order;  // groups by decreasing cost; null: natural order
-  int32_t* ctrl;         // plan counters: [1] groups, [2] next work item, [3] CTAs finished
+  int32_t* ctrl;         // plan counters: [1] groups, [3] CTAs finished, [5] CTAs with a share of the work
+  const long long* cum;  // work before each position of the order (blocks x head units)
+  const long long* work; // [0]: the total
+  const int32_t* cta_first;  // first and last work item of each CTA's share
+  const int32_t* cta_last;
+  int32_t* flags;        // [2 * (boundary) + tile]: that piece's partial result is stored
+  float* partial;        // the pieces' partial results, one slot per share boundary and tile
   float* lse;
   uint8_t* out;          // bf16 [t_local, Hq, D]: tiles of fewer than 128 rows are stored through it
   long long t_local;
@@ -103,6 +130,26 @@ struct AttnParams {
 };
 
 constexpr int kItemConsumers = 4;  // MMA issuer, data relay, one warp of each softmax warpgroup
+
+// A slot holds one tile's partial result: O as [D / 4][128 rows] float4 (so
+// that a warp's 32 rows are 512 contiguous bytes), then m and l per row.
+template <int D>
+constexpr int slot_floats() { return D * kBlockM + 2 * kBlockM; }
+
+// A work item as the producer hands it to the other roles: the group (a
+// position of the plan's order), the head unit, and the piece of the group's
+// key blocks this CTA runs: blocks [j0, j0 + nb) of the group's walk, piece
+// s of S, the pieces' first share being `first`.
+struct ItemDesc {
+  int group;  // -1: no item left
+  int unit;
+  int j0;
+  int nb;
+  int s;
+  int S;
+  int first;
+  int pad;
+};
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -119,9 +166,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ uint64_t q_full[2], q_free[2], k_full[kStages], v_full[kStages];
   __shared__ uint64_t s_full[2][kStages], p_full[2], o_final[2], o_free[2];
   __shared__ uint64_t item_full[2], item_empty[2], drain[1];
-  __shared__ int item_slot[2];
-  __shared__ int wg_item[2];
+  __shared__ ItemDesc item_desc[2];
+  __shared__ ItemDesc wg_desc[2];
   __shared__ int wg_abort[2];
+  __shared__ int wg_flag_ok[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -162,60 +210,133 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   grid_dependents_launch();
   const int units = p.head_pairs ? (p.Hq >> 1) : p.Hq;
   const int gqa = p.Hq / p.Hkv;
-  // Work item i: group order[i / units] (the plan's decreasing-cost order),
-  // head unit i % units.
-  auto item_group = [&](int item) {
-    const int pos = item / units;
-    return p.order ? __ldg(p.order + pos) : pos;
-  };
-  auto item_head0 = [&](int item) {
-    const int unit = item % units;
-    return p.head_pairs ? 2 * unit : unit;
-  };
-  // The k-th item of this CTA, as the producer published it (-1: none left,
-  // or the CTA aborted). Reading the slot and releasing it are one step.
-  auto take_item = [&](int k) -> int {
-    if (!mbar_wait(&item_full[k & 1], (k >> 1) & 1, &abort_flag)) return -1;
-    const int item = item_slot[k & 1];
+  // The k-th item of this CTA, as the producer published it (false: none
+  // left, or the CTA aborted). Reading the slot and releasing it are one step.
+  auto take_item = [&](int k, ItemDesc& d) -> bool {
+    d.group = -1;
+    if (!mbar_wait(&item_full[k & 1], (k >> 1) & 1, &abort_flag)) return false;
+    d = item_desc[k & 1];
     mbar_arrive(&item_empty[k & 1]);
-    return item;
+    return d.group >= 0;
   };
 
   if (warp < 4) {
    setmaxnreg_dec<kRegsControl>();
    if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Takes work items (the first is blockIdx.x, then one from the plan's
-    // counter per item), publishes each in a two-slot ring, and loads the
-    // item's Q tiles and K/V blocks. Key blocks are numbered across items
-    // (b), so the stage ring and its release through tile B's score barrier
-    // run on without a break between items.
+    // Walks the CTA's share of the work, publishes each item (or piece) in a
+    // two-slot ring, and loads its Q tiles and K/V blocks. Key blocks are
+    // numbered across items (b), so the stage ring and its release through
+    // tile B's score barrier run on without a break between items.
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int n_items = min(max(p.ctrl[1], 0), p.max_groups) * units;
-      int next = blockIdx.x;
+      const int P = min(max(p.ctrl[1], 0), p.max_groups);
+      const int G = min(max(p.ctrl[5], 0), static_cast<int>(gridDim.x));
+      // equal shares, or whole items from the plan's counter (taken only
+      // once the previous item's loads are issued, so that items go to the
+      // CTAs about to be free and the costliest-first order balances the SMs
+      // as a greedy schedule does)
+      const bool shares = (p.ctrl[6] != 0);
+      int next = static_cast<int>(blockIdx.x);
+      const long long W = p.work[0];
+      const int bx = static_cast<int>(blockIdx.x);
+      const int f_share = p.cta_first[bx];
+      const int l_share = p.cta_last[bx];
+      const long long n_total = static_cast<long long>(P) * units;
+      long long R0 = 0, R1 = 0;  // this CTA's share of the work
+      int i_first = 0, n_it = 0;
+      if (shares && bx < G && W > 0) {
+        R0 = bx * W / G;
+        R1 = (bx + 1) * W / G;
+        if (R0 < R1 && f_share >= 0 && l_share >= f_share && l_share < n_total) {
+          i_first = f_share;
+          n_it = l_share - f_share + 1;
+        }
+      }
+      // Item i spans the work [st, st + w) of the running totals: its key
+      // blocks (at least one counted), then its fixed cost; nb_of: the
+      // blocks counted for it.
+      auto item_range = [&](int i, long long& st, long long& nb_of) {
+        const int pos = i / units;
+        const long long c0 = p.cum[pos], c1 = p.cum[pos + 1];
+        const long long w = max(c1 - c0, 0LL) / units;
+        st = c0 + (i - pos * units) * w;
+        nb_of = max(w - kItemCost, 1LL);
+      };
+      // the share holding work index w
+      auto share_of = [&](long long w) -> int { return static_cast<int>(((w + 1) * G - 1) / W); };
+      // whether item i has a block in this share (a share may begin or end
+      // inside an item's fixed cost)
+      auto in_share = [&](int i) {
+        long long st, nb_of;
+        item_range(i, st, nb_of);
+        return st < R1 && st + nb_of > R0;
+      };
+      // An item begun in the share before (this CTA finishes it and combines
+      // its pieces) runs last, after the rest of the share.
+      bool head_last = false;
+      if (n_it > 1) {
+        long long st, nb_of;
+        item_range(i_first, st, nb_of);
+        head_last = (st < R0) && (st + nb_of > R0);
+      }
+      int cand = head_last ? i_first + 1 : i_first;  // next candidate item
+      const int i_end = i_first + n_it;
       int b = 0;       // key blocks of all items so far
       int issued = 0;  // K/V loads issued, in block order: 2b + 1 after K_b, 2b + 2 after V_b
       int nq[2] = {0, 0};
       bool ok = true;
       for (int k = 0; ok; ++k) {
         if (k >= 2 && !mbar_wait(&item_empty[k & 1], ((k >> 1) - 1) & 1, &abort_flag)) break;
-        const int item = (next < n_items) ? next : -1;
-        item_slot[k & 1] = item;
+        int i = -1;
+        if (!shares) {
+          if (next < n_total) i = next;
+        } else {
+          while (cand < i_end && i < 0) {
+            if (in_share(cand)) i = cand;
+            ++cand;
+          }
+          if (i < 0 && head_last) {
+            i = i_first;
+            head_last = false;
+          }
+        }
+        ItemDesc d;
+        d.group = -1;
+        d.unit = d.j0 = d.nb = d.s = d.first = d.pad = 0;
+        d.S = 1;
+        if (i >= 0) {
+          const int pos = i / units;
+          d.unit = i - pos * units;
+          d.group = min(max(p.order ? __ldg(p.order + pos) : pos, 0), p.max_groups - 1);
+          const long long n = min(max(p.groups[d.group].n_blocks, 0), p.max_blocks);
+          if (!shares) {
+            d.nb = static_cast<int>(n);
+          } else {
+            long long st, nb_of;
+            item_range(i, st, nb_of);
+            const long long j0 = max(R0, st) - st, j1 = min(R1, st + nb_of) - st;
+            d.j0 = static_cast<int>(j0);
+            d.nb = static_cast<int>(max(0LL, min(j1, n) - j0));
+            d.first = share_of(st);
+            d.S = share_of(st + nb_of - 1) - d.first + 1;
+            d.s = bx - d.first;
+          }
+        }
+        item_desc[k & 1] = d;
         mbar_arrive(&item_full[k & 1]);
-        if (item < 0) break;
-        const int group = item_group(item);
-        const int head0 = item_head0(item);
-        const int kvh = head0 / gqa;
-        const FwdGroup* gi = p.groups + group;
-        const int n_blocks = min(max(gi->n_blocks, 0), p.max_blocks);
-        if (n_blocks == 0) {
-          next = static_cast<int>(gridDim.x) + atomicAdd(p.ctrl + 2, 1);
+        if (d.group < 0) break;
+        if (d.nb == 0) {  // no key block here: nothing to load
+          if (!shares) next = static_cast<int>(gridDim.x) + atomicAdd(p.ctrl + 2, 1);
           continue;
         }
-        const int2* group_iv = p.intervals + static_cast<long long>(group) * p.group_rows;
+        const int head0 = p.head_pairs ? 2 * d.unit : d.unit;
+        const int kvh = head0 / gqa;
+        const FwdGroup* gi = p.groups + d.group;
+        const int n_blocks = d.nb;
+        const int2* group_iv = p.intervals + static_cast<long long>(d.group) * p.group_rows;
         const int n_iv = min(max(gi->n_intervals, 0), p.group_rows);
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
@@ -231,6 +352,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!ok) break;
         BlockCursor cur;
         cur.init(group_iv, n_iv);
+        cur.skip(d.j0);
         for (int i = 0; i < n_blocks; ++i, ++b) {
           const int st = b & 1;
           // Stages are released through tile B's score barriers, one per
@@ -255,12 +377,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           issued = 2 * b + 2;
           cur.next();
         }
-        // The next item is claimed only now, two key blocks before this one
-        // ends (the ring holds two), so that items go to the CTAs that are
-        // about to be free: the costliest-first order then balances the SMs
-        // as a greedy schedule does. Claiming at the item's start would hand
-        // out items round-robin, whatever their cost.
-        next = static_cast<int>(gridDim.x) + atomicAdd(p.ctrl + 2, 1);
+        if (!shares) next = static_cast<int>(gridDim.x) + atomicAdd(p.ctrl + 2, 1);
       }
       if (abort_flag) {
         // let every copy still in flight land before the CTA exits
@@ -316,9 +433,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int b = 0, nq = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int item = take_item(k);
-        if (item < 0) break;
-        const int n_blocks = min(max(p.groups[item_group(item)].n_blocks, 0), p.max_blocks);
+        ItemDesc d;
+        if (!take_item(k, d)) break;
+        const int n_blocks = d.nb;
         int finals = 0;
         if (n_blocks > 0) {
           ok = mbar_wait(&q_full[0], nq & 1, &abort_flag) && mbar_wait(&q_full[1], nq & 1, &abort_flag) &&
@@ -376,9 +493,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int b = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int item = take_item(k);
-        if (item < 0) break;
-        const int n_blocks = min(max(p.groups[item_group(item)].n_blocks, 0), p.max_blocks);
+        ItemDesc d;
+        if (!take_item(k, d)) break;
+        const int n_blocks = d.nb;
         for (int j = 0; j < n_blocks; ++j) {
           const int bb = b + j;
           if (bb > 0 && !(mbar_wait(&p_full[0], (bb - 1) & 1, &abort_flag) &&
@@ -416,26 +533,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int k = 0;; ++k) {
       // One warp takes the item for the warpgroup, so that its four warps
       // always agree on the item and on stopping.
-      if (quarter == 0) {
-        int item = -1;
-        if (lane == 0) item = take_item(k);
-        item = __shfl_sync(0xffffffffu, item, 0);
-        if (lane == 0) {
-          wg_item[x] = item;
-          wg_abort[x] = 0;
-        }
+      if (quarter == 0 && lane == 0) {
+        ItemDesc d;
+        take_item(k, d);
+        wg_desc[x] = d;
+        wg_abort[x] = 0;
       }
       named_bar_sync(bar_id, 128);
       int n_blocks, lo = 1, hi = 0, tmax_lo, tmin_hi;
       BlockCursor cur;
       {
-        const int item = wg_item[x];
-        if (item < 0) break;
-        const int group = item_group(item);
+        const int group = wg_desc[x].group;
+        if (group < 0) break;
         const FwdGroup* gi = p.groups + group;
-        n_blocks = min(max(gi->n_blocks, 0), p.max_blocks);
+        n_blocks = wg_desc[x].nb;
         cur.init(p.intervals + static_cast<long long>(group) * p.group_rows,
                  min(max(gi->n_intervals, 0), p.group_rows));
+        cur.skip(wg_desc[x].j0);
         tmax_lo = gi->max_lo[x];
         tmin_hi = gi->min_hi[x];
         if (r < min(max(gi->h[x], 0), kBlockM)) {
@@ -573,14 +687,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       b += n_blocks;
       // The tile's rows and head are read again here rather than kept
       // through the block loop, whose registers the scores fill.
-      const int item = wg_item[x];
-      const FwdGroup* gi = p.groups + item_group(item);
-      const int qh = p.head_pairs ? item_head0(item) + x : item_head0(item);
+      const int d_s = wg_desc[x].s, d_S = wg_desc[x].S;
+      const FwdGroup* gi = p.groups + wg_desc[x].group;
+      const int qh = p.head_pairs ? 2 * wg_desc[x].unit + x : wg_desc[x].unit;
       const int row0 = gi->row0[x];
       const int h = min(max(gi->h[x], 0), kBlockM);
       const bool in_tile = r < h;
       const long long grow = static_cast<long long>(row0) + r;
       const bool valid = in_tile && (lo <= hi);
+      // a piece of an item cut at share boundaries: every piece but the last
+      // publishes its partial result, the last combines them all
+      const bool split = d_S > 1;
+      const bool publisher = split && d_s != d_S - 1;
+      const bool combiner = split && !publisher;
+      constexpr int kSlot = slot_floats<D>();
+      // piece t (< S - 1) of this tile: the slot of the boundary it ends at,
+      // and its flag
+      const int slot0 = 2 * wg_desc[x].first + x;
+      float* const slot_base = p.partial + static_cast<long long>(slot0) * kSlot;
+      auto slot_of = [slot_base](int t) { return slot_base + static_cast<long long>(2 * t) * kSlot; };
       // ---------------------------------------------------------- epilogue
       // O / l in bf16 goes into this tile's Q buffer (free once o_final[x] is
       // reported: the last MMA reading it is done) in the 128-byte swizzle of
@@ -592,13 +717,87 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (ok) ok = warp_wait(&o_final[x], k & 1, &abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after_sync();
-      if (ok && n_blocks > 0) {
+      if (publisher) {
+        // O (unnormalised), m and l of this row into the piece's slot; the
+        // flag goes up after the warpgroup's barrier below
+        float* so = slot_of(d_s);
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            if (n_blocks > 0) {
+              tmem_ld32(t_o + c * 32, rr);
+              tmem_ld_wait(rr);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 32; ++q) rr[q] = 0u;
+            }
+            float4* dst = reinterpret_cast<float4*>(so) + (c * 8) * kBlockM + r;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q * kBlockM] = make_float4(__uint_as_float(rr[4 * q]), __uint_as_float(rr[4 * q + 1]),
+                                             __uint_as_float(rr[4 * q + 2]), __uint_as_float(rr[4 * q + 3]));
+          }
+          so[D * kBlockM + r] = (n_blocks > 0) ? m : -INFINITY;
+          so[D * kBlockM + kBlockM + r] = (n_blocks > 0) ? l : 0.f;
+        }
+        __threadfence();
+      }
+      float w_own = 1.f;  // the combiner's weight of its own piece
+      if (combiner) {
+        // every other piece of this tile has published (their CTAs have lower
+        // indices and their pieces wait for nothing)
+        bool got = ok && n_blocks > 0;
+        if (ok && n_blocks == 0) record_error(p.err, CPTHD_ERR_INDEX_RANGE, wg_desc[x].group);
+        if (got && r == 0)
+          for (int t = 0; t < d_S - 1 && got; ++t) got = flag_wait(p.flags + slot0 + 2 * t, &abort_flag);
+        if (r == 0) wg_flag_ok[x] = got ? 1 : 0;
+        named_bar_sync(bar_id, 128);
+        ok = ok && (wg_flag_ok[x] != 0);
+        fence_acq_rel_gpu();
+        if (ok) {
+          // the combined maximum and sum, pieces in order (own piece last)
+          float ms = m;
+          for (int t = 0; t < d_S - 1; ++t) ms = fmaxf(ms, __ldcg(slot_of(t) + D * kBlockM + r));
+          float ls = 0.f;
+          for (int t = 0; t < d_S - 1; ++t) {
+            const float mt = __ldcg(slot_of(t) + D * kBlockM + r);
+            if (mt != -INFINITY) ls += ex2(mt - ms) * __ldcg(slot_of(t) + D * kBlockM + kBlockM + r);
+          }
+          w_own = (m != -INFINITY) ? ex2(m - ms) : 0.f;
+          ls += w_own * l;
+          m = ms;
+          l = ls;
+        }
+      }
+      if (ok && n_blocks > 0 && !publisher) {
         const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
           tmem_ld32(t_o + c * 32, rr);
           tmem_ld_wait(rr);
+          if (combiner) {
+            float acc[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+            for (int t = 0; t < d_S - 1; ++t) {
+              const float* so = slot_of(t);
+              const float mt = __ldcg(so + D * kBlockM + r);
+              const float wt = (mt != -INFINITY) ? ex2(mt - m) : 0.f;
+              const float4* src = reinterpret_cast<const float4*>(so) + (c * 8) * kBlockM + r;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 v = __ldcg(src + q * kBlockM);
+                acc[4 * q] += wt * v.x;
+                acc[4 * q + 1] += wt * v.y;
+                acc[4 * q + 2] += wt * v.z;
+                acc[4 * q + 3] += wt * v.w;
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < 32; ++q) rr[q] = __float_as_uint(acc[q] + w_own * __uint_as_float(rr[q]));
+          }
           uint32_t ob[16];
 #pragma unroll
           for (int q = 0; q < 16; ++q)
@@ -615,10 +814,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[x]);
-      if (ok && in_tile) {
+      if (ok && in_tile && !publisher) {
         p.lse[static_cast<long long>(qh) * p.t_local + grow] =
             (valid && l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-        if (n_blocks == 0) {
+        if (n_blocks == 0 && !split) {
           // no key in the whole group (only pad rows): zeros, stored directly
           uint4* dst = reinterpret_cast<uint4*>(p.out + (grow * p.Hq + qh) * static_cast<long long>(D) * 2);
 #pragma unroll
@@ -631,7 +830,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // read once, between the two barriers: the warpgroup's first warp
       // clears the flag for the next item only after the second one
       const bool stop = (wg_abort[x] != 0);
-      if (!stop && n_blocks > 0 && h > 0) {
+      // every thread's partial is written and fenced: raise the piece's flag
+      if (publisher && !stop && r == 0) st_release_gpu(p.flags + slot0 + 2 * d_s, 1);
+      if (!stop && !publisher && n_blocks > 0 && h > 0) {
         if (h == kBlockM) {
           if (r == 0) {
 #pragma unroll
@@ -666,6 +867,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // launch on this plan.
     __threadfence();
     if (atomicAdd(p.ctrl + 3, 1) == static_cast<int>(gridDim.x) - 1) {
+      // every CTA is done with the hand-off flags: lower them for the next launch
+      for (int f = 0; f < 2 * static_cast<int>(gridDim.x); ++f) p.flags[f] = 0;
       atomicExch(p.ctrl + 2, 0);
       atomicExch(p.ctrl + 3, 0);
     }
@@ -674,10 +877,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// The attention grid, which the plan's schedule is made for: one CTA per SM,
+// at most kMaxCtas.
+static int attn_grid() {
+  const int sms = sm_count();
+  return sms < kMaxCtas ? sms : kMaxCtas;
+}
+
 template <int D>
 static int launch_attn(const void* q, const void* k, const void* v, long long t_local, long long T, int Hq, int Hkv,
-                       float scale_log2, const FwdPlan& plan, const FwdShape& shape, bool ordered, void* out,
-                       float* lse, int32_t* err, cudaStream_t s) {
+                       float scale_log2, const FwdPlan& plan, const FwdShape& shape, bool ordered, float* partial,
+                       void* out, float* lse, int32_t* err, cudaStream_t s) {
   EncodeTiledFn enc = get_encode_tiled();
   if (enc == nullptr) return CPTHD_ERR_CUDA;
   CUtensorMap mq, mk, mv, mo;
@@ -691,6 +901,12 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
   p.intervals = plan.intervals;
   p.order = ordered ? plan.order : nullptr;
   p.ctrl = plan.ctrl;
+  p.cum = plan.cum;
+  p.work = plan.work;
+  p.cta_first = plan.cta_first;
+  p.cta_last = plan.cta_last;
+  p.flags = plan.flags;
+  p.partial = partial;
   p.lse = lse;
   p.out = static_cast<uint8_t*>(out);
   p.t_local = t_local;
@@ -706,22 +922,27 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
   CPTHD_TRY_CUDA(cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   const long long items = shape.max_groups * (shape.head_pairs ? Hq / 2 : Hq);
   if (items > INT32_MAX) return CPTHD_ERR_UNSUPPORTED;
-  const int sms = sm_count();
-  if (sms < 1) return CPTHD_ERR_CUDA;
   // one CTA per SM (one fits: shared memory and TMEM are taken whole), each
-  // taking work items until none is left
-  const int grid = static_cast<int>(items < sms ? items : sms);
+  // running its share of the plan's work; the plan was made for this grid
+  const int grid = attn_grid();
+  if (grid < 1) return CPTHD_ERR_CUDA;
   CPTHD_TRY_CUDA(launch_pdl(attn_fwd_tc_kernel<D>, dim3(static_cast<unsigned>(grid)), dim3(kAttnThreads), smem, s,
                             mq, mk, mv, mo, p));
   return CPTHD_OK;
 }
 
-// Whether the plan orders the groups: when there are more work items than
-// SMs (the attention grid's CTAs take items in that order) and the groups
-// fit the sort.
+// Whether the plan orders the groups (costliest first): when there are more
+// work items than SMs and the groups fit the sort.
 static bool plan_ordered(const FwdShape& shape, int Hq) {
   const long long items = shape.max_groups * (shape.head_pairs ? Hq / 2 : Hq);
   return items > sm_count() && shape.max_groups <= kMaxSortGroups;
+}
+
+// The partial results of cut items: one slot per share boundary and tile,
+// after the plan in the workspace.
+static size_t split_bytes(int d) {
+  return align256(sizeof(float) * static_cast<size_t>(2 * (kMaxCtas - 1)) * (d == 64 ? slot_floats<64>()
+                                                                                       : slot_floats<128>()));
 }
 
 }  // namespace cpthd
@@ -729,16 +950,18 @@ static bool plan_ordered(const FwdShape& shape, int Hq) {
 extern "C" int thd_causal_attn_workspace_size(int64_t t_local, int Hq, int Hkv, int d, size_t* bytes_host) {
   if (bytes_host == nullptr || t_local < 0 || Hq < 1 || Hkv < 1) return CPTHD_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return CPTHD_ERR_UNSUPPORTED;
-  (void)d;
-  *bytes_host = cpthd::fwd_plan_bytes(cpthd::fwd_shape(t_local, Hq, Hkv));
+  if (d != 64 && d != 128) return CPTHD_ERR_UNSUPPORTED;
+  *bytes_host = cpthd::fwd_plan_bytes(cpthd::fwd_shape(t_local, Hq, Hkv)) + cpthd::split_bytes(d);
   return CPTHD_OK;
 }
 
 namespace cpthd {
 
-static int check_workspace(int64_t t_local, int Hq, int Hkv, const void* workspace_dev, size_t workspace_bytes) {
-  if (workspace_dev == nullptr || workspace_bytes < fwd_plan_bytes(fwd_shape(t_local, Hq, Hkv)) ||
-      (reinterpret_cast<uintptr_t>(workspace_dev) & 255))
+// d = 0: the plan alone (thd_causal_attn_plan, which does not know d)
+static int check_workspace(int64_t t_local, int Hq, int Hkv, int d, const void* workspace_dev,
+                           size_t workspace_bytes) {
+  const size_t need = fwd_plan_bytes(fwd_shape(t_local, Hq, Hkv)) + (d > 0 ? split_bytes(d) : 0);
+  if (workspace_dev == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace_dev) & 255))
     return CPTHD_ERR_WORKSPACE;
   return CPTHD_OK;
 }
@@ -765,13 +988,17 @@ static int launch_plan(const IndexGen& slots, long long t_local, long long T, co
     while (sort_n < shape.max_groups) sort_n <<= 1;
   }
   const size_t sort_bytes = sizeof(unsigned) * static_cast<size_t>(sort_n);
+  const int units = shape.head_pairs ? Hq / 2 : Hq;
+  const int grid = attn_grid();
+  if (grid < 1) return CPTHD_ERR_CUDA;
   if (shape.head_pairs) {
     CPTHD_TRY_CUDA(launch_pdl(attn_fwd_group_kernel<kBlockM>, dim3(static_cast<unsigned>(shape.max_groups)),
-                              dim3(kBlockM), sort_bytes, s, t_local, shape.max_tiles, 1, cup, plan, sort_n, err));
+                              dim3(kBlockM), sort_bytes, s, t_local, shape.max_tiles, 1, cup, plan, sort_n, units,
+                              grid, err));
   } else {
     CPTHD_TRY_CUDA(launch_pdl(attn_fwd_group_kernel<2 * kBlockM>, dim3(static_cast<unsigned>(shape.max_groups)),
                               dim3(2 * kBlockM), sort_bytes, s, t_local, shape.max_tiles, 0, cup, plan, sort_n,
-                              err));
+                              units, grid, err));
   }
   return CPTHD_OK;
 }
@@ -787,7 +1014,7 @@ extern "C" int thd_causal_attn_plan(const int32_t* q_slice_idx_dev, int64_t t_lo
   if (st != CPTHD_OK) return st;
   if (t_local == 0) return CPTHD_OK;
   if (q_slice_idx_dev == nullptr || cu_seqlens_dev == nullptr || num_docs < 1 || T < 1) return CPTHD_ERR_INVALID_ARG;
-  st = check_workspace(t_local, Hq, Hkv, workspace_dev, workspace_bytes);
+  st = check_workspace(t_local, Hq, Hkv, 0, workspace_dev, workspace_bytes);
   if (st != CPTHD_OK) return st;
   const int32_t* cup = cu_seqlens_padded_dev ? cu_seqlens_padded_dev : cu_seqlens_dev;
   return launch_plan(index_list(q_slice_idx_dev), t_local, T, cu_seqlens_dev, cup, num_docs, Hq, Hkv, workspace_dev,
@@ -807,7 +1034,7 @@ extern "C" int thd_causal_attn_plan_partition(int strategy, int64_t T, const int
   if (st != CPTHD_OK) return st;
   if (t_local == 0) return CPTHD_OK;
   if (cu_seqlens_dev == nullptr || num_docs < 1) return CPTHD_ERR_INVALID_ARG;
-  st = check_workspace(t_local, Hq, Hkv, workspace_dev, workspace_bytes);
+  st = check_workspace(t_local, Hq, Hkv, 0, workspace_dev, workspace_bytes);
   if (st != CPTHD_OK) return st;
   const int32_t* cup = cu_seqlens_padded_dev ? cu_seqlens_padded_dev : cu_seqlens_dev;
   return launch_plan(index_formula(strategy, cup, num_docs, T, cp_size, rank, t_local), t_local, T, cu_seqlens_dev,
@@ -828,20 +1055,22 @@ extern "C" int thd_causal_attn_fwd_planned(int64_t t_local, const void* q_dev, c
   const uintptr_t align = reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(k_dev) |
                           reinterpret_cast<uintptr_t>(v_dev) | reinterpret_cast<uintptr_t>(out_dev);
   if (align & 15) return CPTHD_ERR_UNSUPPORTED;
-  st = check_workspace(t_local, Hq, Hkv, workspace_dev, workspace_bytes);
+  st = check_workspace(t_local, Hq, Hkv, d, workspace_dev, workspace_bytes);
   if (st != CPTHD_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
   const float scale_log2 = scale * 1.4426950408889634f;
   const FwdShape shape = fwd_shape(t_local, Hq, Hkv);
   const FwdPlan plan = carve_fwd_plan(const_cast<void*>(workspace_dev), shape);
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(workspace_dev)) +
+                                            fwd_plan_bytes(shape));
   // the plan ordered its groups exactly when there are more items than SMs
   const bool ordered = plan_ordered(shape, Hq);
   if (d == 128)
-    return launch_attn<128>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, plan, shape, ordered, out_dev,
-                            lse_dev, err_dev, s);
-  return launch_attn<64>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, plan, shape, ordered, out_dev,
-                         lse_dev, err_dev, s);
+    return launch_attn<128>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, plan, shape, ordered, partial,
+                            out_dev, lse_dev, err_dev, s);
+  return launch_attn<64>(q_dev, k_dev, v_dev, t_local, T, Hq, Hkv, scale_log2, plan, shape, ordered, partial,
+                         out_dev, lse_dev, err_dev, s);
 }
 
 extern "C" int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_local, const void* q_dev,
@@ -861,7 +1090,7 @@ extern "C" int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loc
   const uintptr_t align = reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(k_dev) |
                           reinterpret_cast<uintptr_t>(v_dev) | reinterpret_cast<uintptr_t>(out_dev);
   if (align & 15) return CPTHD_ERR_UNSUPPORTED;
-  st = check_workspace(t_local, Hq, Hkv, workspace_dev, workspace_bytes);
+  st = check_workspace(t_local, Hq, Hkv, d, workspace_dev, workspace_bytes);
   if (st != CPTHD_OK) return st;
   st = thd_causal_attn_plan(q_slice_idx_dev, t_local, T, cu_seqlens_dev, cu_seqlens_padded_dev, num_docs, Hq, Hkv,
                             workspace_dev, workspace_bytes, err_dev, stream);

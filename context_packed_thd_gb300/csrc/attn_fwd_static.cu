@@ -5,8 +5,8 @@
 // plugins that must not call cudaMalloc (it synchronises the device and can
 // fail or fragment memory mid-step), or hot paths that must never enter the
 // allocator at all. For them this file keeps the attention's scratch
-// (per-row key bounds, the query tiles, per-group key intervals, the group
-// schedule) in a
+// (per-row key bounds, the query tiles, per-group key intervals, the
+// schedule, the partial results of cut items) in a
 // fixed-size array that lives in device memory for as long as the library is
 // loaded, so the call itself allocates nothing.
 //
@@ -25,11 +25,13 @@
 
 namespace cpthd {
 
-// 8 MiB: the scratch of a slice of up to about 255,000 query rows (the plan
-// takes about 33 bytes per row: per-row bounds and document, the document
-// runs, and per tile and group its key intervals). Every GPU that loads the
-// library holds this array until the process exits.
-constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+// 32 MiB: the attention's fixed part (about 20 MiB at d = 128: the partial
+// results of the items that the schedule cuts at CTA share boundaries, one
+// slot per boundary and tile) and the plan of a slice of up to about 350,000
+// query rows (about 33 bytes per row: per-row bounds and document, the
+// document runs, and per tile and group its key intervals). Every GPU that
+// loads the library holds this array until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kStaticScratchBytes];
 

@@ -28,9 +28,13 @@
 //     the GQA group size is even, else two consecutive tiles under one head)
 //     the union of its rows' intervals, one per document, sorted; its cost
 //     in 128-key blocks; and per tile the bounds inside which a key block
-//     needs no mask. When the attention grid has more work items than SMs,
-//     the block that finishes last also writes the groups' order by
-//     decreasing cost (a greedy schedule of the costliest first).
+//     needs no mask. The block that finishes last writes the attention
+//     kernel's schedule: when there are more work items than SMs, the
+//     groups' order by decreasing cost; always, the running total of the
+//     work (128-key blocks, at least one per item, plus a fixed cost per
+//     item) over the items in that order, and for every attention CTA the
+//     first and last item of its equal share of the total (see the
+//     attention kernel for how a share that cuts an item is handled).
 #pragma once
 
 #include "attn_meta.cuh"
@@ -46,6 +50,20 @@ struct FwdGroup {
   int h[2];       // rows of each tile (0: no tile)
 };
 
+// Attention CTAs the schedule is made for (at most; the grid is the smaller
+// of this and the SM count), and the least work a CTA is given.
+constexpr int kMaxCtas = 160;
+constexpr int kMinCtaBlocks = 4;
+// The fixed cost of a work item in key blocks (its Q load, first scores and
+// epilogue take about as long as three key blocks): the schedule counts an
+// item as max(blocks, 1) + kItemCost, its blocks first.
+constexpr int kItemCost = 3;
+// Equal shares pay off when items are long: below this mean number of key
+// blocks per item, the CTAs instead take whole items from a counter in the
+// plan's order (their fixed costs and cache reuse then balance better than
+// cut pieces do).
+constexpr int kSharesMinMeanBlocks = 64;
+
 // Device arrays of a plan, carved from the caller's workspace.
 struct FwdPlan {
   int32_t* row_lo;     // [n] first allowed key slot of each local row (empty: lo > hi)
@@ -53,11 +71,18 @@ struct FwdPlan {
   int32_t* row_doc;    // [n] document of the row's slot, -1 when the slot is out of range
   int32_t* seg;        // [n] run starts past the group blocks' shared copy (scratch)
   uint32_t* run_bits;  // [ceil(n / 32)] bit r of word w: row 32 w + r starts a run
-  int32_t* ctrl;       // [0] tiles, [1] groups, [2] next work item, [3] attention CTAs finished,
-                       // [4] group blocks finished (cleared by the rows kernel)
+  int32_t* ctrl;       // [0] tiles, [1] groups, [2] next work item (taken from a counter), [3] attention
+                       // CTAs finished, [4] group blocks finished (cleared by the rows kernel), [5]
+                       // attention CTAs with work, [6] 1: equal shares, 0: items from the counter
   FwdGroup* groups;    // [max_groups]
   int2* intervals;     // [max_groups * group_rows] (start, end) inclusive, per group
   int32_t* order;      // [max_groups]
+  long long* cum;      // [max_groups + 1] work before each position of the order (blocks x head units)
+  long long* work;     // [1] the total
+  int32_t* cta_first;  // [kMaxCtas] first work item of each CTA's share
+  int32_t* cta_last;   // [kMaxCtas] last work item of each CTA's share
+  int32_t* flags;      // [2 * kMaxCtas] hand-off flags of the pieces of cut items (cleared by the rows
+                       // kernel and by the attention kernel's last CTA)
 };
 
 struct FwdShape {
@@ -86,6 +111,9 @@ inline size_t fwd_plan_bytes(const FwdShape& s) {
   b += align256(sizeof(FwdGroup) * s.max_groups);
   b += align256(sizeof(int2) * s.max_groups * s.group_rows);
   b += align256(sizeof(int32_t) * s.max_groups);
+  b += align256(sizeof(long long) * (s.max_groups + 1));
+  b += align256(sizeof(long long));
+  b += 3 * align256(sizeof(int32_t) * 2 * kMaxCtas);
   return b;
 }
 
@@ -100,7 +128,12 @@ inline FwdPlan carve_fwd_plan(void* base, const FwdShape& s) {
   w.ctrl = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * 8);
   w.groups = reinterpret_cast<FwdGroup*>(p); p += align256(sizeof(FwdGroup) * s.max_groups);
   w.intervals = reinterpret_cast<int2*>(p); p += align256(sizeof(int2) * s.max_groups * s.group_rows);
-  w.order = reinterpret_cast<int32_t*>(p);
+  w.order = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * s.max_groups);
+  w.cum = reinterpret_cast<long long*>(p); p += align256(sizeof(long long) * (s.max_groups + 1));
+  w.work = reinterpret_cast<long long*>(p); p += align256(sizeof(long long));
+  w.cta_first = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * 2 * kMaxCtas);
+  w.cta_last = reinterpret_cast<int32_t*>(p); p += align256(sizeof(int32_t) * 2 * kMaxCtas);
+  w.flags = reinterpret_cast<int32_t*>(p);
   return w;
 }
 
@@ -146,8 +179,10 @@ static __global__ void __launch_bounds__(256) attn_rows_kernel(IndexGen slots, l
     }
   }
   // the group kernel's completion count starts at zero (it counts blocks
-  // only after this kernel has finished)
+  // only after this kernel has finished), and so do the attention kernel's
+  // hand-off flags
   if (i == 0) plan.ctrl[4] = 0;
+  for (long long j = i; j < 2 * kMaxCtas; j += static_cast<long long>(gridDim.x) * 256) plan.flags[j] = 0;
   int lo = 1, hi = 0, doc = -1;  // empty interval
   if (in) {
     if (p < 0 || p >= T) {
@@ -278,38 +313,118 @@ static __device__ __forceinline__ void group_intervals(const int32_t* __restrict
 }
 
 
-// The block that finishes last then writes the LPT order of the groups
-// (decreasing cost, ties by index, so unused groups come last) when
-// sort_n > 0: a bitonic sort of sort_n (a power of two >= the grid) keys in
-// dynamic shared memory.
+// The block that finishes last then writes the attention kernel's schedule.
+// When sort_n > 0: the LPT order of the groups (decreasing cost, ties by
+// index, so unused groups come last) by a bitonic sort of sort_n (a power of
+// two >= the grid) keys in dynamic shared memory. Always: the running total
+// of the work over the positions of the order (each group's blocks, at least
+// one, plus kItemCost, times the head units), and for each of the G attention
+// CTAs (G: the
+// grid, fewer when the work is small) the first and last work item of its
+// share [c W / G, (c + 1) W / G). cum_sh (cum_cap entries) keeps the running
+// totals for the searches when they fit.
 template <int ROWS>
-static __device__ void order_groups_last_block(const FwdPlan& plan, int ngroups_total, int sort_n) {
+static __device__ void schedule_last_block(const FwdPlan& plan, int ngroups_total, int sort_n, int units, int grid,
+                                           long long* cum_sh, int cum_cap, long long* scan_sh) {
   extern __shared__ unsigned sort_keys[];
   const int t = threadIdx.x;
-  for (int i = t; i < sort_n; i += ROWS) {
-    if (i < ngroups_total) {
-      const int c = __ldcg(&plan.groups[i].n_blocks);  // written by other blocks: read past L1
-      const unsigned cost = static_cast<unsigned>(min(max(c, 0), (1 << 18) - 1));
-      sort_keys[i] = ((cost ^ 0x3ffffu) << 13) | static_cast<unsigned>(i);
-    } else {
-      sort_keys[i] = 0xffffffffu;
+  if (sort_n > 0) {
+    for (int i = t; i < sort_n; i += ROWS) {
+      if (i < ngroups_total) {
+        const int c = __ldcg(&plan.groups[i].n_blocks);  // written by other blocks: read past L1
+        const unsigned cost = static_cast<unsigned>(min(max(c, 0), (1 << 18) - 1));
+        sort_keys[i] = ((cost ^ 0x3ffffu) << 13) | static_cast<unsigned>(i);
+      } else {
+        sort_keys[i] = 0xffffffffu;
+      }
     }
+    __syncthreads();
+    for (int k = 2; k <= sort_n; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = t; i < sort_n; i += ROWS) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const unsigned a = sort_keys[i], b = sort_keys[ixj];
+            const bool up = ((i & k) == 0);
+            if ((a > b) == up) { sort_keys[i] = b; sort_keys[ixj] = a; }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = t; i < ngroups_total; i += ROWS) plan.order[i] = static_cast<int>(sort_keys[i] & 0x1fffu);
+  }
+  // running totals: each thread sums a contiguous run of positions, then a
+  // scan over the threads places the runs
+  const int P = min(max(__ldcg(plan.ctrl + 1), 0), ngroups_total);
+  const int per = (P + ROWS - 1) / ROWS;
+  const int a = min(P, t * per);
+  const int b = min(P, a + per);
+  auto work_at = [&](int pos) -> long long {
+    const int g = (sort_n > 0) ? static_cast<int>(sort_keys[pos] & 0x1fffu) : pos;
+    return static_cast<long long>(max(__ldcg(&plan.groups[g].n_blocks), 1) + kItemCost) * units;
+  };
+  long long sum = 0, blocks = 0;
+  for (int i = a; i < b; ++i) {
+    const long long w = work_at(i);
+    sum += w;
+    blocks += w - static_cast<long long>(kItemCost) * units;
+  }
+  scan_sh[t] = sum;
+  // the mean item length decides between equal shares and the counter
+  __shared__ unsigned long long blocks_sh;
+  if (t == 0) blocks_sh = 0;
+  __syncthreads();
+  atomicAdd(&blocks_sh, static_cast<unsigned long long>(blocks));
+  __syncthreads();
+  if (t == 0) {
+    long long acc = 0;
+    for (int u = 0; u < ROWS; ++u) {
+      const long long x = scan_sh[u];
+      scan_sh[u] = acc;
+      acc += x;
+    }
+    scan_sh[ROWS] = acc;
   }
   __syncthreads();
-  for (int k = 2; k <= sort_n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = t; i < sort_n; i += ROWS) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned a = sort_keys[i], b = sort_keys[ixj];
-          const bool up = ((i & k) == 0);
-          if ((a > b) == up) { sort_keys[i] = b; sort_keys[ixj] = a; }
-        }
-      }
-      __syncthreads();
-    }
+  long long run = scan_sh[t];
+  for (int i = a; i < b; ++i) {
+    plan.cum[i] = run;
+    if (i < cum_cap) cum_sh[i] = run;
+    run += work_at(i);
   }
-  for (int i = t; i < ngroups_total; i += ROWS) plan.order[i] = static_cast<int>(sort_keys[i] & 0x1fffu);
+  const long long W = scan_sh[ROWS];
+  if (t == 0) {
+    plan.cum[P] = W;
+    if (P < cum_cap) cum_sh[P] = W;
+    plan.work[0] = W;
+  }
+  __syncthreads();
+  const long long G = max(1LL, min(static_cast<long long>(grid), W / kMinCtaBlocks));
+  const bool shares = static_cast<long long>(blocks_sh) >= static_cast<long long>(kSharesMinMeanBlocks) * P * units;
+  if (t == 0) {
+    plan.ctrl[5] = static_cast<int>(G);
+    plan.ctrl[6] = shares ? 1 : 0;
+  }
+  // the work item holding work index w: the last position whose running total
+  // is <= w, then the head unit inside it
+  const bool in_shared = (P < cum_cap);
+  auto cum_at = [&](int pos) -> long long { return in_shared ? cum_sh[pos] : __ldcg(plan.cum + pos); };
+  auto item_at = [&](long long w) -> int {
+    int lo = 0, hi = P - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cum_at(mid) <= w) lo = mid; else hi = mid - 1;
+    }
+    const long long per_unit = (cum_at(lo + 1) - cum_at(lo)) / units;
+    const long long u = per_unit > 0 ? (w - cum_at(lo)) / per_unit : 0;
+    return lo * units + static_cast<int>(min(u, static_cast<long long>(units - 1)));
+  };
+  for (int c = t; c < G && P > 0; c += ROWS) {
+    const long long r0 = c * W / G, r1 = (c + 1) * W / G;
+    plan.cta_first[c] = item_at(r0);
+    plan.cta_last[c] = item_at(r1 - 1);
+  }
 }
 
 constexpr int kRunsInShared = 4096;  // run starts a group block keeps in shared memory for the greedy walk
@@ -435,13 +550,14 @@ static __device__ void find_group_tiles(long long n, long long max_tiles, int he
 template <int ROWS>
 static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(long long n, long long max_tiles, int head_pairs,
                                                                      const int32_t* __restrict__ cup, FwdPlan plan,
-                                                                     int sort_n, int32_t* err) {
+                                                                     int sort_n, int units, int grid, int32_t* err) {
   __shared__ unsigned long long xbuf[2][ROWS];
   __shared__ int warp_sum[ROWS / 32];
   __shared__ int red_blocks[ROWS / 32];
   __shared__ int red_lo[ROWS / 32];
   __shared__ int red_hi[ROWS / 32];
-  __shared__ int run_start[kRunsInShared];
+  __shared__ __align__(8) int run_start[kRunsInShared];  // later the running totals (kRunsInShared / 2 of them)
+  __shared__ long long scan_sh[ROWS + 1];
   __shared__ int2 tiles[2];
   __shared__ int sh[2];
   __shared__ int is_last;
@@ -461,8 +577,7 @@ static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(long long n
   } else {
     group_intervals<ROWS>(cup, plan, g, tiles[0], tiles[1], xbuf, warp_sum, red_blocks, red_lo, red_hi);
   }
-  if (sort_n == 0) return;
-  // every block counts itself done; the last one orders the groups
+  // every block counts itself done; the last one writes the schedule
   __syncthreads();
   if (t == 0) {
     __threadfence();
@@ -471,7 +586,8 @@ static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(long long n
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  order_groups_last_block<ROWS>(plan, static_cast<int>(gridDim.x), sort_n);
+  schedule_last_block<ROWS>(plan, static_cast<int>(gridDim.x), sort_n, units, grid,
+                            reinterpret_cast<long long*>(run_start), kRunsInShared / 2, scan_sh);
 }
 
 }  // namespace cpthd

@@ -13,7 +13,7 @@ extern "C" const char* cpthd_status_string(int status) {
     case CPTHD_ERR_INDEX_RANGE: return "index out of range";
     case CPTHD_ERR_PAD_LENGTH: return "actual document length exceeds padded length";
     case CPTHD_ERR_TIMEOUT: return "pipeline wait timed out; kernel returned early";
-    case CPTHD_ERR_SCRATCH_LIMIT: return "query slice too large for the built-in 8 MiB attention scratch";
+    case CPTHD_ERR_SCRATCH_LIMIT: return "query slice too large for the built-in 32 MiB attention scratch";
     default: return "unknown status";
   }
 }

@@ -164,9 +164,13 @@ CPTHD_API int cp_partition_reorder_multi(int strategy, const int32_t* cu_seqlens
                                          const int64_t* row_bytes_host, int32_t* idx_out_dev, int32_t* err_dev,
                                          cpthd_stream_t stream);
 
-/* Device workspace thd_causal_attn_fwd needs for a slice of t_local rows
- * (per-row key bounds, per-tile key intervals and the tile schedule).
- * Host only. */
+/* Device workspace thd_causal_attn_fwd needs for a slice of t_local rows:
+ * the plan (per-row key bounds, per-tile key intervals, the schedule of the
+ * attention CTAs, about 33 bytes per row) and one fp32 partial-result slot
+ * per boundary between two CTAs' shares of the work and per query tile (a
+ * work item that a boundary cuts runs in pieces whose partial softmax
+ * results are combined; about 20 MiB at d = 128, 10 MiB at d = 64, whatever
+ * t_local). d must be 64 or 128 (else CPTHD_ERR_UNSUPPORTED). Host only. */
 CPTHD_API int thd_causal_attn_workspace_size(int64_t t_local, int Hq, int Hkv, int d, size_t* bytes_host);
 
 /* Causal packed-THD attention forward for one rank's query slice.
@@ -188,6 +192,8 @@ CPTHD_API int thd_causal_attn_workspace_size(int64_t t_local, int Hq, int Hkv, i
  *   workspace_dev: at least thd_causal_attn_workspace_size() bytes, 256-byte
  *     aligned, device; contents need no initialisation and are scratch.
  * Supported: d in {64, 128}; Hq % Hkv == 0; Hq, Hkv >= 1.
+ * The result is deterministic: the same inputs on the same GPU give the
+ * same bits (the pieces of a cut work item are combined in a fixed order).
  * Host errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  * Device checks (err_dev): BAD_OFFSETS, PAD_LENGTH, INDEX_RANGE, TIMEOUT. */
 CPTHD_API int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_local, const void* q_dev,
@@ -199,14 +205,19 @@ CPTHD_API int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loca
 
 /* The forward in two parts, for callers that run several attentions over
  * the same slice (every layer of a model step shares q_slice_idx and the
- * offsets): thd_causal_attn_plan writes the row-group metadata (per-row key
- * bounds, per-group key intervals and, when the grid needs more CTAs than
- * the GPU has SMs, the group order) into the workspace once;
- * thd_causal_attn_fwd_planned runs the attention kernel against it as often
- * as needed. thd_causal_attn_fwd is the two in sequence. The planned call
- * must get the same t_local, T, Hq, Hkv and the workspace the plan wrote
- * (caller's contract; the workspace is read only); q, k, v, d and the scale
- * may differ between planned calls.
+ * offsets): thd_causal_attn_plan writes the plan (per-row key bounds,
+ * per-group key intervals, the group order when there are more work items
+ * than SMs, and every attention CTA's equal share of the work) into the
+ * workspace once; thd_causal_attn_fwd_planned runs the attention kernel
+ * against it as often as needed. thd_causal_attn_fwd is the two in
+ * sequence. The planned call must get the same t_local, T, Hq, Hkv and the
+ * workspace the plan wrote, on the same GPU (caller's contract); q, k, v, d
+ * and the scale may differ between planned calls. A planned call writes only
+ * the workspace's partial-result slots and its counters and flags, which it
+ * returns to their initial state before it ends, so planned calls on one
+ * workspace must not overlap on the GPU. thd_causal_attn_plan alone checks
+ * the workspace against the plan part only (it does not know d); the
+ * planned call needs the full thd_causal_attn_workspace_size().
  * Arguments, layouts, errors: as thd_causal_attn_fwd. */
 CPTHD_API int thd_causal_attn_plan(const int32_t* q_slice_idx_dev, int64_t t_local, int64_t T,
                                    const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_padded_dev, int num_docs,
@@ -268,10 +279,10 @@ CPTHD_API int thd_causal_attn_bwd(const int32_t* q_slice_idx_dev, int64_t t_loca
  * device memory (a host framework that owns all allocations, a plugin that
  * must not call cudaMalloc mid-step, a path that may never enter an
  * allocator). The pages have no counterpart: this is a deployment variant.
- * Instead of a caller workspace it uses a fixed 8 MiB device array built into
- * the library, which every GPU that loads the library holds until the
+ * Instead of a caller workspace it uses a fixed 32 MiB device array built
+ * into the library, which every GPU that loads the library holds until the
  * process exits; the call allocates nothing. That is enough for slices of at
- * least 250,000 query rows; a larger slice is rejected with
+ * least 350,000 query rows; a larger slice is rejected with
  * CPTHD_ERR_SCRATCH_LIMIT before anything is launched.
  * Every call whose stream is not capturing looks up the array's device
  * address on the current device (so a device reset, or another context

@@ -12,6 +12,8 @@ Tolerances: max |out - ref| <= 1e-2 + 1e-2 |ref| (bf16 output) and
   row of one rank of the lognormal (both strategies) and padded packs.
 * DualChunkSwap as two launches per rank (one per owned chunk, the pages'
   two attention steps): every row against the oracle and the one launch.
+* long work items cut into pieces at the CTAs' share boundaries (one long
+  document, few heads): every row, and bit-identical repeated runs.
 * edge cases: ragged tails, empty and one-token documents, pad rows, GQA
   group sizes, custom scale, arbitrary row order of the query slice, and
   device-checked malformed offsets.
@@ -471,3 +473,32 @@ def test_more_document_runs_than_shared_memory_holds(permute):
     ro, rl = A.attention_fwd(inp.q[torch.from_numpy(ref_idx)], inp.k, inp.v, lay.cu_seqlens, lay.cu_seqlens_padded,
                              ref_idx)
     assert_attn_matches(out, lse, ro, rl, f"10000 documents, permuted={permute}")
+
+
+@pytest.mark.parametrize("hq,hkv,dd", [(1, 1, 64), (2, 1, 128)])
+def test_long_items_cut_into_pieces_every_row(hq, hkv, dd):
+    """One 16384-token document as a single slice (cp_size 1) under one or two
+    query heads: the work items (one per 128- or 256-row group) are long
+    (65 key blocks on average), so the CTAs take equal shares of the work
+    and most items are cut into pieces whose partial results one CTA
+    combines (up to five pieces here). Every row against the oracle, and one
+    plan run three times: bit-identical results each time (the pieces are
+    combined in a fixed order, and the hand-off flags are lowered again
+    after every launch)."""
+    dev = cuda_or_skip(); cp = load_lib()
+    inp = _custom([16384], 1, hq, hkv, dd, 31 + dd)
+    d = DevInputs(inp, dev)
+    lay = inp.layout
+    err = new_err(dev)
+    idx = cp.cp_partition_index("nlb", d.cup, lay.T, 1, 0, err=err)
+    ws = cp.thd_causal_attn_plan(idx, lay.T, d.cu, d.cup, hq, hkv, err=err)
+    q_loc = cp.cp_reorder(d.q, idx, err=err)
+    outs = [cp.thd_causal_attn_fwd_planned(q_loc, d.k, d.v, ws, err=err) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert err.cpu().tolist() == [0, 0]
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    ref_idx = np.arange(lay.T, dtype=np.int64)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    ro, rl = A.attention_fwd(inp.q, inp.k, inp.v, lay.cu_seqlens, lay.cu_seqlens_padded, ref_idx)
+    assert_attn_matches(outs[0][0], outs[0][1], ro, rl, f"one document, Hq {hq}, d {dd}")
