@@ -61,8 +61,8 @@ L2_FLUSH_BYTES = 256 << 20
 # change, the line reports null until it is captured again.
 ATTN_SOURCES = ("csrc/attn_fwd.cu", "csrc/attn_plan.cuh", "csrc/attn_common.cuh", "csrc/attn_meta.cuh",
                 "csrc/sm100.cuh", "csrc/common.cuh")
-ATTN_TRAFFIC = {"workload": "long131072_h8", "bytes_per_launch": 670035640,
-                "source_sha256": "ca5af1c3f59ec2a5eeeb5f18d315b6f4e67a2137f91fb4e7748486a721276f1b"}
+ATTN_TRAFFIC = {"workload": "long131072_h8", "bytes_per_launch": 1029514616,
+                "source_sha256": "b1077cb310cc3367656c911c2ec31445fdcbb55c5fc4674c443041c1859ed416"}
 
 
 def load_peaks():

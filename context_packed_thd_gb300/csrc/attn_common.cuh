@@ -74,12 +74,12 @@ static inline EncodeTiledFn get_encode_tiled() {
   return fn;
 }
 
-// [rows, heads, d] bf16 tensor, boxes of 64 columns x 1 head x 128 rows, 128-byte swizzle.
+// [rows, heads, d] bf16 tensor, boxes of 64 columns x 1 head x box_rows rows, 128-byte swizzle.
 static inline bool make_rows_heads_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, long long rows, int heads,
-                                int d) {
+                                int d, int box_rows = 128) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(heads) * d * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

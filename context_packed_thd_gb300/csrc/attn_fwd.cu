@@ -12,12 +12,14 @@
 // head. Twelve warps in three warpgroups; warpgroup 0 gives registers to the
 // softmax warpgroups (setmaxnreg: 96 vs 192 per thread; 96*128 + 192*256 stays
 // within the 168 * 384 the launch allocates):
-//  * warp 0      TMA producer: both Q tiles once, then K and V 128-key blocks
-//                into a two-stage shared-memory ring (128-byte swizzle, the
-//                layout the UMMA shared-memory descriptors read). A stage is
-//                refilled once tile B's score barrier reports that the MMAs
-//                reading it are done, so the issuer commits only to the two
-//                score barriers inside its loop.
+//  * warp 0      TMA producer: both Q tiles once per item, then K and V
+//                128-key blocks into a two-stage shared-memory ring (128-byte
+//                swizzle, the layout the UMMA shared-memory descriptors
+//                read). A stage is refilled once tile B's score barrier
+//                reports that the MMAs reading it are done. A Q tile is
+//                replaced by the next item's as soon as the item's last
+//                scores are done (the issuer commits to q_free after the
+//                last S), so the next item's Q loads while this one ends.
 //  * warp 1      one lane issues all tcgen05 MMAs: S_A(0), S_B(0), then per
 //                block j and tile x = A, B: O_x += P_x(j) V_j, S_x(j+1).
 //                Issuing tile A's batch before tile B's from one thread keeps
@@ -43,9 +45,9 @@
 //                interval (only on blocks the tile's bounds do not cover
 //                fully), keeps the fp32 running max / sum in base 2, rescales
 //                O in TMEM only when the max grows by more than 2^8 (exact
-//                either way), and writes P back into TMEM. At the end it
-//                normalises O into the tile's Q buffer in shared memory and
-//                one thread stores the tile with TMA; LSE per row.
+//                either way), and writes P back into TMEM. At the end each
+//                thread normalises its row of O and writes it (bf16, 16-byte
+//                stores) straight to the output, and its LSE.
 // Key blocks start at the group's interval starts (document starts), so
 // documents the group does not see are never loaded or multiplied.
 //
@@ -98,7 +100,10 @@ struct AttnSmem {
   static constexpr int kQOff = 0;                  // Q_A, Q_B
   static constexpr int kKOff = 2 * kQ;
   static constexpr int kVOff = kKOff + kStages * kKV;
-  static constexpr int kBytes = kVOff + kStages * kKV;
+  // per softmax warp: its 32 rows x 64 output columns, staged for a TMA store
+  static constexpr int kOutSlice = 32 * 128;
+  static constexpr int kOutOff = kVOff + kStages * kKV;
+  static constexpr int kBytes = kOutOff + 8 * kOutSlice;
   // request at least this much so that one CTA holds an SM (TMEM is taken whole)
   static constexpr int kLaunchBytes = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
 };
@@ -162,6 +167,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sQ = smem + L::kQOff;
   uint8_t* sK = smem + L::kKOff;
   uint8_t* sV = smem + L::kVOff;
+  uint8_t* sOut = smem + L::kOutOff;
 
   __shared__ uint64_t q_full[2], q_free[2], k_full[kStages], v_full[kStages];
   __shared__ uint64_t s_full[2][kStages], p_full[2], o_final[2], o_free[2];
@@ -170,6 +176,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ ItemDesc wg_desc[2];
   __shared__ int wg_abort[2];
   __shared__ int wg_flag_ok[2];
+  __shared__ int wg_bounds[2][2];  // per tile: the bounds inside which a key block needs no mask
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     abort_flag = 0;
     for (int x = 0; x < 2; ++x) {
       mbar_init(&q_full[x], 1);
-      mbar_init(&q_free[x], 1);   // the thread that stores tile x's output
+      mbar_init(&q_free[x], 1);   // the commit after the item's last S_x
       for (int s = 0; s < kStages; ++s) mbar_init(&s_full[x][s], 1);  // scores of tile x, key blocks of stage s
       mbar_init(&p_full[x], 5);   // four softmax warps and the data relay
       mbar_init(&o_final[x], 1);
@@ -340,7 +347,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int n_iv = min(max(gi->n_intervals, 0), p.group_rows);
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          // tile x's buffer holds the previous item's output until its store has read it
+          // the previous item's last S_x has read tile x's buffer
           if (nq[x] > 0 && !mbar_wait(&q_free[x], (nq[x] - 1) & 1, &abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&q_full[x], L::kQ);
           const int qh = p.head_pairs ? head0 + x : head0;
@@ -445,8 +452,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after_sync();
             issue_s(b, 0);
             umma_commit(&s_full[0][b & 1]);
+            if (n_blocks == 1) umma_commit(&q_free[0]);  // the item's last read of Q_A
             issue_s(b, 1);
             umma_commit(&s_full[1][b & 1]);
+            if (n_blocks == 1) umma_commit(&q_free[1]);
           }
           for (int j = 0; ok && j < n_blocks; ++j) {
             const int bb = b + j;
@@ -462,6 +471,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               if (more) {
                 issue_s(bb + 1, x);
                 umma_commit(&s_full[x][(bb + 1) & 1]);  // also reports O_x += P_x(bb) V_bb done
+                // the item's last scores: once they are done, Q_x may be
+                // replaced by the next item's while this one finishes
+                if (j + 2 == n_blocks) umma_commit(&q_free[x]);
               } else {
                 umma_commit(&o_final[x]);  // tile x's epilogue need not wait for the other tile
                 finals |= 1 << x;
@@ -528,7 +540,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t t_s = tmem + lane_off + x * kBlockN;
     const uint32_t t_o = tmem + lane_off + 256 + x * D;
     const float sl2 = p.scale_log2;
-    uint8_t* stile = sQ + x * L::kQ;
     int b = 0;
     for (int k = 0;; ++k) {
       // One warp takes the item for the warpgroup, so that its four warps
@@ -538,9 +549,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         take_item(k, d);
         wg_desc[x] = d;
         wg_abort[x] = 0;
+        // kept in shared memory: the block loop has no registers to spare
+        if (d.group >= 0) {
+          wg_bounds[x][0] = p.groups[d.group].max_lo[x];
+          wg_bounds[x][1] = p.groups[d.group].min_hi[x];
+        }
       }
       named_bar_sync(bar_id, 128);
-      int n_blocks, lo = 1, hi = 0, tmax_lo, tmin_hi;
+      int n_blocks, lo = 1, hi = 0;
       BlockCursor cur;
       {
         const int group = wg_desc[x].group;
@@ -550,8 +566,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         cur.init(p.intervals + static_cast<long long>(group) * p.group_rows,
                  min(max(gi->n_intervals, 0), p.group_rows));
         cur.skip(wg_desc[x].j0);
-        tmax_lo = gi->max_lo[x];
-        tmin_hi = gi->min_hi[x];
         if (r < min(max(gi->h[x], 0), kBlockM)) {
           lo = p.row_lo[static_cast<long long>(gi->row0[x]) + r];
           hi = p.row_hi[static_cast<long long>(gi->row0[x]) + r];
@@ -572,7 +586,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t sr[kBlockN];
         tmem_ld128(t_s, sr);
         tmem_ld_wait128(sr);
-        const bool full = (kstart >= tmax_lo) && (kstart + kBlockN - 1 <= min(tmin_hi, kend));
+        const bool full = (kstart >= wg_bounds[x][0]) && (kstart + kBlockN - 1 <= min(wg_bounds[x][1], kend));
         // 16-column groups of this block that no row of the warp may use
         uint32_t dead_groups = 0;
         bool row_dead = false;  // this row has no key in this block
@@ -707,13 +721,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float* const slot_base = p.partial + static_cast<long long>(slot0) * kSlot;
       auto slot_of = [slot_base](int t) { return slot_base + static_cast<long long>(2 * t) * kSlot; };
       // ---------------------------------------------------------- epilogue
-      // O / l in bf16 goes into this tile's Q buffer (free once o_final[x] is
-      // reported: the last MMA reading it is done) in the 128-byte swizzle of
-      // the output's tensor map. A full tile is stored by one thread with
-      // TMA; a shorter one by the warpgroup's threads, 16 bytes each, from
-      // the same staging (a TMA box would write the next tile's rows). Then
-      // the buffer is released for the next item's Q. Every warp reaches the
-      // barriers of every item it took; an aborted one only marks the tile.
+      // Once o_final[x] reports the last P V done, each thread reads its row
+      // of O from TMEM, merges or publishes pieces of a cut item, and writes
+      // O / l in bf16 straight to the output (no staging: the Q buffer is
+      // already the next item's). Every warp reaches the barriers of every
+      // item it took; an aborted one only marks the tile.
       if (ok) ok = warp_wait(&o_final[x], k & 1, &abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after_sync();
@@ -743,7 +755,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         __threadfence();
       }
-      float w_own = 1.f;  // the combiner's weight of its own piece
       if (combiner) {
         // every other piece of this tile has published (their CTAs have lower
         // indices and their pieces wait for nothing)
@@ -764,20 +775,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const float mt = __ldcg(slot_of(t) + D * kBlockM + r);
             if (mt != -INFINITY) ls += ex2(mt - ms) * __ldcg(slot_of(t) + D * kBlockM + kBlockM + r);
           }
-          w_own = (m != -INFINITY) ? ex2(m - ms) : 0.f;
+          const float w_own = (m != -INFINITY) ? ex2(m - ms) : 0.f;
           ls += w_own * l;
           m = ms;
           l = ls;
-        }
-      }
-      if (ok && n_blocks > 0 && !publisher) {
-        const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(t_o + c * 32, rr);
-          tmem_ld_wait(rr);
-          if (combiner) {
+          // O of all pieces, in piece order (own piece last), back into TMEM
+          for (int c = 0; c < D / 32; ++c) {
             float acc[32];
 #pragma unroll
             for (int q = 0; q < 32; ++q) acc[q] = 0.f;
@@ -795,25 +798,77 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 acc[4 * q + 3] += wt * v.w;
               }
             }
+            uint32_t rr[32];
+            tmem_ld32(t_o + c * 32, rr);
+            tmem_ld_wait(rr);
 #pragma unroll
             for (int q = 0; q < 32; ++q) rr[q] = __float_as_uint(acc[q] + w_own * __uint_as_float(rr[q]));
+            tmem_st32(t_o + c * 32, rr);
           }
-          uint32_t ob[16];
+          tmem_st_wait();
+        }
+      }
+      // O / l in bf16, 64 columns at a time: each warp packs its 32 rows into
+      // its slice of shared memory (128-byte swizzle) and one lane stores the
+      // slice with TMA; a warp whose rows cross the end of a short tile
+      // stores its rows directly instead (a TMA box would write the next
+      // tile's rows). O_x is released to the next item's first P V right
+      // after the warp's last TMEM read, before the stores.
+      bool freed = false;
+      if (ok && n_blocks > 0 && !publisher) {
+        const float inv = (valid && l > 0.f) ? 1.f / l : 0.f;
+        const int wrow = quarter * 32;  // the warp's first row in the tile
+        const bool tma_rows = (wrow + 32 <= h);
+        uint8_t* slice = sOut + (warp - 4) * L::kOutSlice;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (grow * p.Hq + qh) * static_cast<long long>(D) * 2);
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            ob[q] = valid ? pack_bf16x2(__uint_as_float(rr[2 * q]) * inv, __uint_as_float(rr[2 * q + 1]) * inv) : 0u;
+        for (int hh = 0; hh < D / 64; ++hh) {
+          uint32_t ob[32];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int u = 4 * c + q4;  // 16-byte unit of the row; 8 units per 64-column panel
-            uint8_t* dst = stile + (u >> 3) * L::kChunk + r * 128 + (((u & 7) ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(dst) = make_uint4(ob[4 * q4], ob[4 * q4 + 1], ob[4 * q4 + 2], ob[4 * q4 + 3]);
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t rr[32];
+            tmem_ld32(t_o + (2 * hh + cc) * 32, rr);
+            tmem_ld_wait(rr);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              ob[16 * cc + q] =
+                  valid ? pack_bf16x2(__uint_as_float(rr[2 * q]) * inv, __uint_as_float(rr[2 * q + 1]) * inv) : 0u;
+          }
+          if (hh == D / 64 - 1) {
+            // O_x is read: the next item's first P V may overwrite it
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[x]);
+            freed = true;
+          }
+          if (tma_rows) {
+            // the slice's previous store (this item's last round, or the
+            // previous item's) has been read
+            if (lane == 0) bulk_wait_group_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4*>(slice + lane * 128 + ((u ^ (lane & 7)) << 4)) =
+                  make_uint4(ob[4 * u], ob[4 * u + 1], ob[4 * u + 2], ob[4 * u + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tm_o, slice, hh * 64, qh, row0 + wrow);
+              bulk_commit_group();
+            }
+          } else if (in_tile) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              dst[8 * hh + u] = make_uint4(ob[4 * u], ob[4 * u + 1], ob[4 * u + 2], ob[4 * u + 3]);
           }
         }
       }
-      // O_x is read: the next item's first P V may overwrite it
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[x]);
+      if (!freed) {
+        // O_x is read: the next item's first P V may overwrite it
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_free[x]);
+      }
       if (ok && in_tile && !publisher) {
         p.lse[static_cast<long long>(qh) * p.t_local + grow] =
             (valid && l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
@@ -825,38 +880,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
       if (!ok) wg_abort[x] = 1;
-      fence_proxy_async_smem();
       named_bar_sync(bar_id, 128);
       // read once, between the two barriers: the warpgroup's first warp
       // clears the flag for the next item only after the second one
       const bool stop = (wg_abort[x] != 0);
       // every thread's partial is written and fenced: raise the piece's flag
       if (publisher && !stop && r == 0) st_release_gpu(p.flags + slot0 + 2 * d_s, 1);
-      if (!stop && !publisher && n_blocks > 0 && h > 0) {
-        if (h == kBlockM) {
-          if (r == 0) {
-#pragma unroll
-            for (int c = 0; c < L::kChunks; ++c) tma_store_3d(&tm_o, stile + c * L::kChunk, c * 64, qh, row0);
-            bulk_commit_group();
-            bulk_wait_group_read_all();
-          }
-        } else {
-          constexpr int kUnitsPerRow = D / 8;  // 16-byte units of one output row
-          for (int u = r; u < h * kUnitsPerRow; u += kBlockM) {
-            const int rr = u / kUnitsPerRow;
-            const int cu = u - rr * kUnitsPerRow;
-            const uint8_t* src = stile + (cu >> 3) * L::kChunk + rr * 128 + (((cu & 7) ^ (rr & 7)) << 4);
-            uint8_t* dst = p.out + ((static_cast<long long>(row0) + rr) * p.Hq + qh) * static_cast<long long>(D) * 2 +
-                           cu * 16;
-            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-          }
-        }
-      }
       named_bar_sync(bar_id, 128);
-      if (n_blocks > 0 && r == 0) mbar_arrive(&q_free[x]);
       if (stop) break;
     }
-    if (r == 0) bulk_wait_group_all();  // this tile's last output store has landed
+    if (lane == 0) bulk_wait_group_all();  // this warp's last output store has landed
   }
 
   tc_fence_before_sync();
@@ -868,7 +901,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __threadfence();
     if (atomicAdd(p.ctrl + 3, 1) == static_cast<int>(gridDim.x) - 1) {
       // every CTA is done with the hand-off flags: lower them for the next launch
-      for (int f = 0; f < 2 * static_cast<int>(gridDim.x); ++f) p.flags[f] = 0;
+      if (p.ctrl[6] != 0)
+        for (int f = 0; f < 2 * static_cast<int>(gridDim.x); ++f) p.flags[f] = 0;
       atomicExch(p.ctrl + 2, 0);
       atomicExch(p.ctrl + 3, 0);
     }
@@ -892,7 +926,7 @@ static int launch_attn(const void* q, const void* k, const void* v, long long t_
   if (enc == nullptr) return CPTHD_ERR_CUDA;
   CUtensorMap mq, mk, mv, mo;
   if (!make_rows_heads_map(enc, &mq, q, t_local, Hq, D) || !make_rows_heads_map(enc, &mk, k, T, Hkv, D) ||
-      !make_rows_heads_map(enc, &mv, v, T, Hkv, D) || !make_rows_heads_map(enc, &mo, out, t_local, Hq, D))
+      !make_rows_heads_map(enc, &mv, v, T, Hkv, D) || !make_rows_heads_map(enc, &mo, out, t_local, Hq, D, 32))
     return CPTHD_ERR_UNSUPPORTED;
   AttnParams p;
   p.row_lo = plan.row_lo;

@@ -354,61 +354,67 @@ static __device__ void schedule_last_block(const FwdPlan& plan, int ngroups_tota
     }
     for (int i = t; i < ngroups_total; i += ROWS) plan.order[i] = static_cast<int>(sort_keys[i] & 0x1fffu);
   }
-  // running totals: each thread sums a contiguous run of positions, then a
-  // scan over the threads places the runs
+  // running totals: each thread sums a contiguous run of positions (keeping
+  // the terms in cum_sh when they fit), a shuffle scan over the threads
+  // places the runs
   const int P = min(max(__ldcg(plan.ctrl + 1), 0), ngroups_total);
   const int per = (P + ROWS - 1) / ROWS;
   const int a = min(P, t * per);
   const int b = min(P, a + per);
+  const bool in_shared = (P < cum_cap);
   auto work_at = [&](int pos) -> long long {
     const int g = (sort_n > 0) ? static_cast<int>(sort_keys[pos] & 0x1fffu) : pos;
     return static_cast<long long>(max(__ldcg(&plan.groups[g].n_blocks), 1) + kItemCost) * units;
   };
-  long long sum = 0, blocks = 0;
+  long long sum = 0;
   for (int i = a; i < b; ++i) {
     const long long w = work_at(i);
+    if (in_shared) cum_sh[i] = w;
     sum += w;
-    blocks += w - static_cast<long long>(kItemCost) * units;
   }
-  scan_sh[t] = sum;
-  // the mean item length decides between equal shares and the counter
-  __shared__ unsigned long long blocks_sh;
-  if (t == 0) blocks_sh = 0;
-  __syncthreads();
-  atomicAdd(&blocks_sh, static_cast<unsigned long long>(blocks));
-  __syncthreads();
-  if (t == 0) {
-    long long acc = 0;
-    for (int u = 0; u < ROWS; ++u) {
-      const long long x = scan_sh[u];
-      scan_sh[u] = acc;
-      acc += x;
-    }
-    scan_sh[ROWS] = acc;
+  // inclusive scan of the per-thread sums: within each warp by shuffles,
+  // then over the warp totals
+  constexpr int kWarps = ROWS / 32;
+  const int lane = t & 31, wid = t >> 5;
+  long long incl = sum;
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
   }
+  if (lane == 31) scan_sh[wid] = incl;
   __syncthreads();
-  long long run = scan_sh[t];
-  for (int i = a; i < b; ++i) {
-    plan.cum[i] = run;
-    if (i < cum_cap) cum_sh[i] = run;
-    run += work_at(i);
+  long long warp_base = 0, W = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    const long long x = scan_sh[w];
+    if (w < wid) warp_base += x;
+    W += x;
   }
-  const long long W = scan_sh[ROWS];
-  if (t == 0) {
-    plan.cum[P] = W;
-    if (P < cum_cap) cum_sh[P] = W;
-    plan.work[0] = W;
-  }
-  __syncthreads();
+  // Each position counts max(blocks, 1) + kItemCost per head unit, so the
+  // blocks alone are the total less the fixed costs; their mean per item
+  // decides between equal shares and the counter.
+  const long long blocks = W - static_cast<long long>(kItemCost) * units * P;
+  const bool shares = (P > 0) && blocks >= static_cast<long long>(kSharesMinMeanBlocks) * P * units;
   const long long G = max(1LL, min(static_cast<long long>(grid), W / kMinCtaBlocks));
-  const bool shares = static_cast<long long>(blocks_sh) >= static_cast<long long>(kSharesMinMeanBlocks) * P * units;
   if (t == 0) {
+    plan.work[0] = W;
     plan.ctrl[5] = static_cast<int>(G);
     plan.ctrl[6] = shares ? 1 : 0;
   }
+  if (!shares) return;  // the counter needs neither the totals nor the shares
+  long long run = warp_base + incl - sum;
+  for (int i = a; i < b; ++i) {
+    const long long w = in_shared ? cum_sh[i] : work_at(i);
+    plan.cum[i] = run;
+    if (in_shared) cum_sh[i] = run;
+    run += w;
+  }
+  if (t == 0) {
+    plan.cum[P] = W;
+    if (in_shared) cum_sh[P] = W;
+  }
+  __syncthreads();
   // the work item holding work index w: the last position whose running total
   // is <= w, then the head unit inside it
-  const bool in_shared = (P < cum_cap);
   auto cum_at = [&](int pos) -> long long { return in_shared ? cum_sh[pos] : __ldcg(plan.cum + pos); };
   auto item_at = [&](long long w) -> int {
     int lo = 0, hi = P - 1;
@@ -420,7 +426,7 @@ static __device__ void schedule_last_block(const FwdPlan& plan, int ngroups_tota
     const long long u = per_unit > 0 ? (w - cum_at(lo)) / per_unit : 0;
     return lo * units + static_cast<int>(min(u, static_cast<long long>(units - 1)));
   };
-  for (int c = t; c < G && P > 0; c += ROWS) {
+  for (int c = t; c < G; c += ROWS) {
     const long long r0 = c * W / G, r1 = (c + 1) * W / G;
     plan.cta_first[c] = item_at(r0);
     plan.cta_last[c] = item_at(r1 - 1);
@@ -557,7 +563,7 @@ static __global__ void __launch_bounds__(ROWS) attn_fwd_group_kernel(long long n
   __shared__ int red_lo[ROWS / 32];
   __shared__ int red_hi[ROWS / 32];
   __shared__ __align__(8) int run_start[kRunsInShared];  // later the running totals (kRunsInShared / 2 of them)
-  __shared__ long long scan_sh[ROWS + 1];
+  __shared__ long long scan_sh[ROWS / 32];
   __shared__ int2 tiles[2];
   __shared__ int sh[2];
   __shared__ int is_last;
