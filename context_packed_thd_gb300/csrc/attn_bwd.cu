@@ -135,6 +135,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
+  // The dK/dV pass depends on none of this pass's results: it may start as
+  // soon as every CTA of this grid has started, and fill the SMs this grid's
+  // last wave leaves idle.
+  grid_dependents_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // with more CTAs than SMs the costliest query tiles go first
   const int tile = p.order ? __ldg(p.order + blockIdx.x / p.Hq) : static_cast<int>(blockIdx.x / p.Hq);
@@ -839,6 +843,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       dv4[i] = z;
     }
   }
+  // This grid may have started beside the dQ pass (it reads nothing the dQ
+  // pass writes); it ends only after that pass has, so that the backward
+  // call's completion covers both.
+  grid_dependency_wait();
 }
 
 static size_t bwd_workspace_bytes(long long ntiles, int Hq) {
@@ -902,8 +910,10 @@ static int launch_bwd(const void* q, const void* k, const void* v, const void* o
   const int sms = sm_count();
   if (sms < 1) return CPTHD_ERR_CUDA;
   const long long grid_kv = work_items < sms ? work_items : sms;
-  attn_bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid_kv), kBwdThreads, smem_kv, s>>>(mq, mdo, mk, mv, p);
+  // launched to overlap the dQ pass's last wave (see the two kernels)
   CPTHD_TRY_CUDA(cudaGetLastError());
+  CPTHD_TRY_CUDA(launch_pdl(attn_bwd_dkdv_kernel<D>, dim3(static_cast<unsigned>(grid_kv)), dim3(kBwdThreads),
+                            static_cast<size_t>(smem_kv), s, mq, mdo, mk, mv, p));
   return CPTHD_OK;
 }
 
