@@ -17,13 +17,18 @@
 //    dP = dO V^T into TMEM, the elementwise warps turn them into dS (bf16,
 //    written back over S), then dQ += dS K with dS read from TMEM. Two S
 //    buffers let S(j+1) and dQ(j) run while the elementwise warps work.
-//  * dK/dV pass, one CTA per (128-key tile, KV head), over every query tile
-//    whose key intervals reach the key tile and every query head of the
-//    group (a key tile no query reaches gets zeros, so dK/dV need no
-//    clearing pass): S^T = K Q^T and dP^T = V dO^T into TMEM, the elementwise warps
-//    write P^T and then dS^T (bf16) back over them in two phases, and
-//    dV += P^T dO and dK += dS^T Q, both accumulated in TMEM and written
-//    once, run during the other phase.
+//  * dK/dV pass, persistent: one CTA per SM takes (128-key tile, KV head)
+//    items from a counter; an item runs over every query tile whose key
+//    intervals reach the key tile and every query head of the group (keys no
+//    query reaches get zeros, so dK/dV need no clearing pass): S^T = K Q^T
+//    and dP^T = V dO^T into TMEM, the elementwise warps write P^T and then
+//    dS^T (bf16) back over them in two phases, and dV += P^T dO and
+//    dK += dS^T Q, both accumulated in TMEM and written once per item, run
+//    during the other phase.
+// The dK/dV pass reads nothing the dQ pass writes: it is launched as a
+// programmatic dependent of the dQ pass and starts once every dQ CTA has
+// started, taking the SMs the dQ pass's last wave leaves idle; it waits for
+// the dQ grid only before it exits.
 // Rows without keys get lse2 = +inf in the pre-pass (p = 0 without a mask);
 // blocks and items the query tile's bounds cover fully skip the mask.
 // Warp roles as in the forward: warp 0 TMA producer, warp 1 MMA issuer
