@@ -362,7 +362,9 @@ def other_workloads(cp, current, dev, flush, peak, peak_sustained, hbm_peak):
     """Attention throughput of every other multi-rank workload: all ranks of
     all its strategies in one CUDA graph (L2 flushed before each replay), so
     that the line also carries the long-context and many-document figures;
-    then the backward of every rank slice, each timed alone.
+    the attention kernel alone per slice (plan written first, as for the
+    headline's roofline); then the backward of every rank slice, each timed
+    alone.
     Fractions are given of the burst and of the sustained bf16 peak: the
     long workload's graph runs tens of milliseconds of tensor work, long
     enough for the power cap to lower the clocks as in the sustained
@@ -382,6 +384,14 @@ def other_workloads(cp, current, dev, flush, peak, peak_sustained, hbm_peak):
                     st.run_attn(cp, r)
 
         ms = _graph_ms(attn_all, flush, reps=3)
+        # the attention kernel alone per slice (its plan written beforehand,
+        # outside the timed graph), as the headline's roofline figure is
+        kern_ms = {}
+        for st in sts:
+            kern_ms[st.name] = []
+            for r in range(cfg.cp):
+                st.run_plan(cp, r)
+                kern_ms[st.name].append(_graph_ms(lambda st=st, r=r: st.run_kernel(cp, r), flush, reps=3))
         # each strategy's slices alone as well: DualChunkSwap balances the
         # ranks, NO_LOAD_BALANCE leaves them as uneven as the pack makes them
         by_strategy = {}
@@ -389,9 +399,13 @@ def other_workloads(cp, current, dev, flush, peak, peak_sustained, hbm_peak):
             for st in sts:
                 ms_s = _graph_ms(lambda st=st: [st.run_attn(cp, r) for r in range(cfg.cp)], flush, reps=3)
                 tf_s = sum(st.flops) / (ms_s * 1e-3) / 1e12
+                tk_s = sum(st.flops) / (sum(kern_ms[st.name]) * 1e-3) / 1e12
                 by_strategy[st.name] = {"attn_tflops": round(tf_s, 3), "frac_of_peak": round(tf_s / peak, 4),
                                         "frac_of_sustained_peak": round(tf_s / peak_sustained, 4),
-                                        "ms": round(ms_s, 4),
+                                        "ms": round(ms_s, 4), "kernel_tflops": round(tk_s, 3),
+                                        "kernel_frac_of_peak": round(tk_s / peak, 4),
+                                        "kernel_ms_per_rank_max": round(max(kern_ms[st.name]), 5),
+                                        "kernel_ms_per_rank_min": round(min(kern_ms[st.name]), 5),
                                         "useful_pair_frac": round(sum(st.pairs) / sum(st.kpairs), 4)}
         dcs = [st for st in sts if st.name == W.DUAL_CHUNK_SWAP]
         restore = kv_restore(cp, cfg, dcs[0], flush, hbm_peak) if dcs else None
@@ -402,9 +416,11 @@ def other_workloads(cp, current, dev, flush, peak, peak_sustained, hbm_peak):
                 raise RuntimeError(f"device check failed on {cfg.name}: {cp.cpthd_status_string(e[0])} ({e})")
         flops = sum(sum(st.flops) for st in sts)
         tf = flops / (ms * 1e-3) / 1e12
+        tk = flops / (sum(sum(v) for v in kern_ms.values()) * 1e-3) / 1e12
         useful = sum(sum(st.pairs) for st in sts) / sum(sum(st.kpairs) for st in sts)
         out[cfg.name] = {"attn_tflops": round(tf, 3), "frac_of_peak": round(tf / peak, 4),
                          "frac_of_sustained_peak": round(tf / peak_sustained, 4), "ms": round(ms, 4),
+                         "kernel_tflops": round(tk, 3), "kernel_frac_of_peak": round(tk / peak, 4),
                          "rank_slices": cfg.cp * len(sts), "strategies": list(cfg.strategies),
                          "useful_pair_frac": round(useful, 4),
                          "per_strategy": by_strategy or None, "kv_restore": restore, "backward": bwd}
