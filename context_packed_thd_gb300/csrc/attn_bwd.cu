@@ -490,9 +490,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const GroupInfo ti = p.tile_info[t];
             const int n_iv = min(max(ti.n_intervals, 0), kBlockM);
             const int2* iv = p.intervals + static_cast<long long>(t) * kBlockM;
-            for (int q = 0; q < n_iv && !rel; ++q) {
-              const int2 a = iv[q];
-              rel = (a.x <= K0 + kBlockN - 1) && (a.y >= K0);
+            // the intervals are disjoint and in key order: the first start and
+            // the last end bound them, which rejects most tiles at once
+            if (n_iv > 0 && iv[0].x <= K0 + kBlockN - 1 && iv[n_iv - 1].y >= K0) {
+              for (int q = 0; q < n_iv && !rel; ++q) {
+                const int2 a = iv[q];
+                rel = (a.x <= K0 + kBlockN - 1) && (a.y >= K0);
+              }
             }
             full = (ti.max_lo[0] <= K0 && ti.min_hi[0] >= K0 + kBlockN - 1);
           }
