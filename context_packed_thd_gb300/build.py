@@ -94,11 +94,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), build_dir:
 
 def build_wait_test() -> str:
     """A test-only variant of the library, built with CPTHD_WAIT_TEST: its
-    pipeline waits give up after 5 ms instead of 2 s, and the attention
-    forward's data-relay warp withholds its arrivals for key block 1, so every
-    CTA with more than one key block must leave through the timeout path
-    (CPTHD_ERR_TIMEOUT). Kept apart from libcpthd.so under _build/; only the
-    timeout test loads it."""
+    waits give up after 5 ms instead of 2 s, and the attention forward
+    withholds one signal so that a wait must run out (CPTHD_ERR_TIMEOUT):
+    by default the data-relay warp's arrivals for key block 1, or, after
+    cpthd_wait_test_mode(2), the hand-off flags of the pieces of cut items.
+    Kept apart from libcpthd.so under _build/; only the timeout tests load
+    it."""
     d = os.path.join(BUILD, "wait_test")
     return build(extra_flags=("-DCPTHD_WAIT_TEST",), build_dir=d, lib=os.path.join(d, "libcpthd_wait_test.so"))
 

@@ -136,6 +136,13 @@ struct AttnParams {
 
 constexpr int kItemConsumers = 4;  // MMA issuer, data relay, one warp of each softmax warpgroup
 
+#ifdef CPTHD_WAIT_TEST
+// Test build only: which wait is made to run out. 1: the data relay withholds
+// its arrivals for key block 1; 2: the pieces of cut items never raise their
+// hand-off flags, so the merging pieces' flag waits run out.
+__device__ int g_wait_test_mode = 1;
+#endif
+
 // A slot holds one tile's partial result: O as [D / 4][128 rows] float4 (so
 // that a warp's 32 rows are 512 contiguous bytes), then m and l per row.
 template <int D>
@@ -520,7 +527,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #ifdef CPTHD_WAIT_TEST
           // Test build only: key block 1's arrivals are withheld, so the waits
           // for P(1) can never complete and must run out into the abort path.
-          if (bb == 1) continue;
+          if (g_wait_test_mode == 1 && bb == 1) continue;
 #endif
           mbar_arrive(&p_full[0]);
           mbar_arrive(&p_full[1]);
@@ -885,7 +892,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // clears the flag for the next item only after the second one
       const bool stop = (wg_abort[x] != 0);
       // every thread's partial is written and fenced: raise the piece's flag
-      if (publisher && !stop && r == 0) st_release_gpu(p.flags + slot0 + 2 * d_s, 1);
+#ifdef CPTHD_WAIT_TEST
+      const bool raise_flag = (g_wait_test_mode != 2);  // test build: mode 2 withholds the flags
+#else
+      const bool raise_flag = true;
+#endif
+      if (publisher && !stop && r == 0 && raise_flag) st_release_gpu(p.flags + slot0 + 2 * d_s, 1);
       named_bar_sync(bar_id, 128);
       if (stop) break;
     }
@@ -1132,3 +1144,10 @@ extern "C" int thd_causal_attn_fwd(const int32_t* q_slice_idx_dev, int64_t t_loc
   return thd_causal_attn_fwd_planned(t_local, q_dev, k_dev, v_dev, T, Hq, Hkv, d, softmax_scale, out_dev, lse_dev,
                                      workspace_dev, workspace_bytes, err_dev, stream);
 }
+
+#ifdef CPTHD_WAIT_TEST
+// Test build only: selects the wait the kernel makes run out (see g_wait_test_mode).
+extern "C" CPTHD_API int cpthd_wait_test_mode(int mode) {
+  return cudaMemcpyToSymbol(cpthd::g_wait_test_mode, &mode, sizeof(int)) == cudaSuccess ? CPTHD_OK : CPTHD_ERR_CUDA;
+}
+#endif
