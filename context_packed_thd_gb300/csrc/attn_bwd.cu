@@ -21,10 +21,14 @@
 //    items from a counter; an item runs over every query tile whose key
 //    intervals reach the key tile and every query head of the group (keys no
 //    query reaches get zeros, so dK/dV need no clearing pass): S^T = K Q^T
-//    and dP^T = V dO^T into TMEM, the elementwise warps write P^T and then
-//    dS^T (bf16) back over them in two phases, and dV += P^T dO and
-//    dK += dS^T Q, both accumulated in TMEM and written once per item, run
-//    during the other phase.
+//    and dP^T = V dO^T into TMEM, each with one more K step that subtracts
+//    the per-query term (lse2 / (scale log2(e)), resp. D: a ones operand
+//    times a per-query operand the pre-pass writes), the elementwise warps
+//    write P^T and then dS^T (bf16) back over them in two phases, and
+//    dV += P^T dO and dK += dS^T Q, both accumulated in TMEM and written
+//    once per item, run during the other phase. With the per-query terms in
+//    the scores, the elementwise loops read no shared memory (the SS-form
+//    MMAs keep its bandwidth busy).
 // The dK/dV pass reads nothing the dQ pass writes: it is launched as a
 // programmatic dependent of the dQ pass and starts once every dQ CTA has
 // started, taking the SMs the dQ pass's last wave leaves idle; it waits for
@@ -40,17 +44,28 @@ namespace cpthd {
 
 constexpr int kBwdThreads = 192;
 constexpr int kBwdMaxTiles = 2048;  // query tiles of one slice the dK/dV pass can list
+// The dK/dV pass lets the tensor core add the per-query terms of
+// x = s scale log2(e) - lse2 and of dP - D: one more K = 16 step of S^T and of
+// dP^T multiplies a "ones" operand (128 keys x 16, ones in columns 0-2) by a
+// per-query operand (128 queries x 16) that holds -lse2 / (scale log2(e)),
+// resp. -D, as the sum of three bf16 terms in columns 0-2 (about 24
+// significant bits). Both are K-major without swizzle: core matrices of 8
+// rows x 16 bytes, row group g and K half c at byte g * 256 + c * 128.
+constexpr int kBwdAugOperand = kBlockM * 16 * 2;     // one 128 x 16 bf16 operand
+constexpr int kBwdAugBytes = 2 * kBwdAugOperand;     // per (query tile, head): the lse2 terms, then the D terms
+constexpr int kBwdOnesBytes = kBlockN * 16 * 2;
 
 template <int D>
 struct BwdSmem {
   static constexpr int kChunk = kBlockM * 64 * 2;
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = kChunks * kChunk;  // one 128-row bf16 tile of Q, dO, K or V
-  static constexpr int kCol = 4 * kBlockM * 4;    // row_lo, row_hi, lse2, D of 128 query rows
+  static constexpr int kCol = 2 * kBlockM * 4;    // row_lo, row_hi of 128 query rows
   // dQ pass: Q, dO, K[3], V[2]
   static constexpr int kDqBytes = 7 * kTile;
-  // dK/dV pass: K, V, Q[2], dO[2], column info[2], two tile lists
-  static constexpr int kDkvBytes = 6 * kTile + 2 * kCol + 2 * kBwdMaxTiles * 4;
+  // dK/dV pass: K, V, Q[2], dO[2], column terms[2], the ones operand,
+  // row bounds[2], two tile lists
+  static constexpr int kDkvBytes = 6 * kTile + 2 * kBwdAugBytes + kBwdOnesBytes + 2 * kCol + 2 * kBwdMaxTiles * 2;
   static constexpr int launch(int b) { return (b + 1024 > 120 * 1024) ? b + 1024 : 120 * 1024; }
 };
 
@@ -62,6 +77,7 @@ struct BwdParams {
   const int32_t* order;  // dQ grid: query tiles by decreasing block count; null = natural order
   const float* lse2;  // [Hq, rows_pad]: lse * log2(e)
   const float* dvec;  // [Hq, rows_pad]: rowsum(dO * O)
+  const uint8_t* aug;  // [Hq, ntiles] blocks of kBwdAugBytes: the dK/dV pass's per-query MMA operands
   float* dq;
   float* dk;
   float* dv;
@@ -79,15 +95,29 @@ struct BwdParams {
   int32_t* err;
 };
 
+// Three bf16 terms whose sum is v to about 24 significant bits, in the low
+// halves of a (element 0), then b (element 1), c (element 2).
+__device__ __forceinline__ void split_bf16x3(float v, uint32_t& w01, uint32_t& w2) {
+  const __nv_bfloat16 t0 = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(t0);
+  const __nv_bfloat16 t1 = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 t2 = __float2bfloat16_rn(r1 - __bfloat162float(t1));
+  w01 = static_cast<uint32_t>(__bfloat16_as_ushort(t0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(t1)) << 16);
+  w2 = static_cast<uint32_t>(__bfloat16_as_ushort(t2));
+}
+
 // D = rowsum(dO * O) and lse * log2(e), laid out [Hq, rows_pad]; one warp per (row, head).
 // A row with no key (a pad row, LSE = -inf) or past the slice gets +inf, so
 // that 2^(s*scale*log2(e) - lse2) is exactly 0 for it without any mask.
+// Also the row's entries of the dK/dV pass's per-query operands: -lse2 /
+// (scale log2(e)) (-2^120 for a row without keys, so that its scores end far
+// below any exponent that ex2 keeps) and -D, each split into three bf16 terms.
 template <int D>
 static __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
                                                                   const __nv_bfloat16* __restrict__ dout,
                                                                   const float* __restrict__ lse, long long t_local,
-                                                                  int Hq, int rows_pad, float* lse2, float* dvec,
-                                                                  int32_t* work) {
+                                                                  int Hq, int rows_pad, float scale_log2, float* lse2,
+                                                                  float* dvec, uint8_t* aug, int32_t* work) {
   if (blockIdx.x == 0 && threadIdx.x == 0) work[0] = 0;  // the dK/dV pass's work counter
   const long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -108,6 +138,16 @@ static __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __nv_bfl
   if (lane == 0) {
     dvec[(long long)h * rows_pad + row] = acc;
     lse2[(long long)h * rows_pad + row] = l2;
+  }
+  if (lane < 2) {
+    const float val = (lane == 1) ? -acc : (l2 == INFINITY ? -0x1p120f : -l2 / scale_log2);
+    uint32_t w01, w2;
+    split_bf16x3(val, w01, w2);
+    const int ntiles = rows_pad / kBlockM, rr = static_cast<int>(row % kBlockM);
+    uint8_t* blk = aug + (static_cast<long long>(h) * ntiles + row / kBlockM) * kBwdAugBytes + lane * kBwdAugOperand;
+    uint4* dst = reinterpret_cast<uint4*>(blk + (rr >> 3) * 256 + (rr & 7) * 16);
+    dst[0] = make_uint4(w01, w2, 0u, 0u);  // elements 0-7 of the row
+    dst[8] = make_uint4(0u, 0u, 0u, 0u);    // elements 8-15, one core matrix further along K
   }
 }
 
@@ -408,9 +448,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sV = smem + L::kTile;
   uint8_t* sQ = smem + 2 * L::kTile;   // two stages
   uint8_t* sDO = smem + 4 * L::kTile;  // two stages
-  uint8_t* sCol = smem + 6 * L::kTile; // two stages of {row_lo, row_hi, lse2, D} x 128
-  int* sList = reinterpret_cast<int*>(sCol + 2 * L::kCol);  // two lists of kBwdMaxTiles
-  __shared__ uint8_t sFull[2][kBwdMaxTiles];  // every real row of the listed tile sees all 128 keys
+  uint8_t* sAug = smem + 6 * L::kTile;  // two stages of the per-query operands (lse2 terms, D terms)
+  uint8_t* sOnes = sAug + 2 * kBwdAugBytes;
+  uint8_t* sCol = sOnes + kBwdOnesBytes;  // two stages of {row_lo, row_hi} x 128
+  // two lists of kBwdMaxTiles query tiles: the tile in bits 0-14, and bit 15
+  // set when every real row of the tile sees all 128 keys
+  uint16_t* sList = reinterpret_cast<uint16_t*>(sCol + 2 * L::kCol);
 
   __shared__ uint64_t kv_full, kv_empty, qdo_full[2], qdo_empty[2], sdp_full[2], pds_full[2], kv_final, acc_free;
   __shared__ uint64_t item_full[2], item_empty[2], drain;
@@ -443,6 +486,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
+  // the ones operand: 1 in columns 0-2 of every row (the first core matrix
+  // along K of each row group), 0 elsewhere
+  for (int i = threadIdx.x; i < kBwdOnesBytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(sOnes)[i] = ((i & 15) < 8) ? make_uint4(0x3f803f80u, 0x3f80u, 0u, 0u)
+                                                        : make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -502,10 +551,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           const unsigned ballot = __ballot_sync(0xffffffffu, rel);
           const int pos = count + __popc(ballot & ((1u << lane) - 1u));
-          if (rel && pos < kBwdMaxTiles) {
-            sList[slot * kBwdMaxTiles + pos] = t;
-            sFull[slot][pos] = full ? 1 : 0;
-          }
+          if (rel && pos < kBwdMaxTiles)
+            sList[slot * kBwdMaxTiles + pos] = static_cast<uint16_t>(t | (full ? 0x8000 : 0));
           count += __popc(ballot);
         }
       }
@@ -533,24 +580,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         for (int i = 0; ok && i < n_items; ++i, ++ig) {
           const int st = ig & 1;
-          const int t = sList[slot * kBwdMaxTiles + i / group];
+          const int t = sList[slot * kBwdMaxTiles + i / group] & 0x7fff;
           const int h = g * group + i % group;
           // Q / dO stage st is free once dK of the item two before is done;
           // that barrier's next phase needs this load, so the parity is
           // unambiguous however far behind this thread runs
           if (ig >= 2 && !mbar_wait(&qdo_empty[st], ((ig >> 1) - 1) & 1, &abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&qdo_full[st], 2 * L::kTile + L::kCol);
+          mbar_arrive_expect_tx(&qdo_full[st], 2 * L::kTile + kBwdAugBytes + L::kCol);
           for (int c = 0; c < L::kChunks; ++c) {
             tma_load_3d(sQ + st * L::kTile + c * L::kChunk, &tm_q, &qdo_full[st], c * 64, h, t * kBlockM);
             tma_load_3d(sDO + st * L::kTile + c * L::kChunk, &tm_do, &qdo_full[st], c * 64, h, t * kBlockM);
           }
           uint8_t* col = sCol + st * L::kCol;
           const long long r0 = static_cast<long long>(t) * kBlockM;
-          const long long hr = static_cast<long long>(h) * p.rows_pad + r0;
           bulk_load(col, p.row_lo + r0, kBlockM * 4, &qdo_full[st]);
           bulk_load(col + kBlockM * 4, p.row_hi + r0, kBlockM * 4, &qdo_full[st]);
-          bulk_load(col + 2 * kBlockM * 4, p.lse2 + hr, kBlockM * 4, &qdo_full[st]);
-          bulk_load(col + 3 * kBlockM * 4, p.dvec + hr, kBlockM * 4, &qdo_full[st]);
+          bulk_load(sAug + st * kBwdAugBytes, p.aug + (static_cast<long long>(h) * p.ntiles + t) * kBwdAugBytes,
+                    kBwdAugBytes, &qdo_full[st]);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -577,21 +623,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       umma_desc_words(smem_desc_sw128(smem_u32(sDO), 16, 1024), do_lo, do_hi);
       umma_desc_words(smem_desc_sw128(smem_u32(sQ), L::kChunk, 1024), qmn_lo, qmn_hi);
       umma_desc_words(smem_desc_sw128(smem_u32(sDO), L::kChunk, 1024), domn_lo, domn_hi);
-      auto issue_s = [&](int i) {  // S^T = K Q^T into [0, 128)
+      uint32_t one_lo, one_hi, aug_lo, aug_hi;
+      umma_desc_words(smem_desc_noswizzle(smem_u32(sOnes), 128, 256), one_lo, one_hi);
+      umma_desc_words(smem_desc_noswizzle(smem_u32(sAug), 128, 256), aug_lo, aug_hi);
+      auto issue_s = [&](int i) {  // S^T = K Q^T - lse2 / (scale log2(e)) into [0, 128)
         const uint32_t so = ((i & 1) * L::kTile) >> 4;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
           umma_ss_w(tmem, k_lo + off, k_hi, q_lo + so + off, q_hi, kIdS, kk > 0);
         }
+        umma_ss_w(tmem, one_lo, one_hi, aug_lo + (((i & 1) * kBwdAugBytes) >> 4), aug_hi, kIdS, 1u);
       };
-      auto issue_dp = [&](int i) {  // dP^T = V dO^T into [128, 256)
+      auto issue_dp = [&](int i) {  // dP^T = V dO^T - D into [128, 256)
         const uint32_t so = ((i & 1) * L::kTile) >> 4;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4;
           umma_ss_w(tmem + 128, v_lo + off, v_hi, do_lo + so + off, do_hi, kIdS, kk > 0);
         }
+        umma_ss_w(tmem + 128, one_lo, one_hi, aug_lo + (((i & 1) * kBwdAugBytes + kBwdAugOperand) >> 4), aug_hi, kIdS,
+                  1u);
       };
       auto issue_dv = [&](int i, uint32_t acc0) {  // dV (+)= P^T dO, P^T (bf16) in [0, 64)
         const uint32_t so = ((i & 1) * L::kTile) >> 4;
@@ -701,11 +753,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!warp_wait(&qdo_full[st], (gi >> 1) & 1, &abort_flag)) { ok = false; break; }
         const int* c_lo = reinterpret_cast<const int*>(sCol + st * L::kCol);
         const int* c_hi = c_lo + kBlockM;
-        const float* c_l2 = reinterpret_cast<const float*>(c_lo + 2 * kBlockM);
-        const float* c_d = c_l2 + kBlockM;
-        const bool item_full_keys = sFull[slot][i / group] != 0;
+        const bool item_full_keys = (sList[slot * kBwdMaxTiles + i / group] & 0x8000) != 0;
         uint32_t pp[64];  // P of the 128 queries, bf16 pairs
-        // ---- phase 1: P = 2^(S scale log2(e) - lse2), masked
+        // ---- phase 1: P = 2^(S scale log2(e) - lse2), masked; S^T already
+        // holds S - lse2 / (scale log2(e)), so no per-query value is read here
+        // (unless a mask is needed)
         if (!warp_wait(&sdp_full[0], gi & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after_sync();
 #pragma unroll
@@ -716,14 +768,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
             const int col = 64 * c2 + 4 * q4;
-            const float4 l24 = *reinterpret_cast<const float4*>(c_l2 + col);
-            const float l2s[4] = {l24.x, l24.y, l24.z, l24.w};
             float pv[4];
 #pragma unroll
             for (int u = 0; u < 4; u += 2) {
               float a0, a1;
-              fma2(a0, a1, __uint_as_float(sv[4 * q4 + u]), __uint_as_float(sv[4 * q4 + u + 1]), sl2, -l2s[u],
-                   -l2s[u + 1]);
+              mul2(a0, a1, __uint_as_float(sv[4 * q4 + u]), __uint_as_float(sv[4 * q4 + u + 1]), sl2, sl2);
               pv[u] = ex2(a0);
               pv[u + 1] = ex2(a1);
             }
@@ -746,7 +795,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&pds_full[0]);
-        // ---- phase 2: dS = P (dP - D)
+        // ---- phase 2: dS = P (dP - D); dP^T already holds dP - D
         if (!warp_wait(&sdp_full[1], gi & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after_sync();
 #pragma unroll
@@ -757,20 +806,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t pd[32];
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
-            const int col = 64 * c2 + 4 * q4;
-            const float4 d4 = *reinterpret_cast<const float4*>(c_d + col);
-            const float ds[4] = {d4.x, d4.y, d4.z, d4.w};
             const uint32_t w0 = pp[32 * c2 + 2 * q4], w1 = pp[32 * c2 + 2 * q4 + 1];
             const float pv[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u),
                                  __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u)};
             float dsv[4];
 #pragma unroll
-            for (int u = 0; u < 4; u += 2) {
-              float t0, t1;
-              fma2(t0, t1, __uint_as_float(dp[4 * q4 + u]), __uint_as_float(dp[4 * q4 + u + 1]), 1.f, -ds[u],
-                   -ds[u + 1]);
-              mul2(dsv[u], dsv[u + 1], pv[u], pv[u + 1], t0, t1);
-            }
+            for (int u = 0; u < 4; u += 2)
+              mul2(dsv[u], dsv[u + 1], pv[u], pv[u + 1], __uint_as_float(dp[4 * q4 + u]),
+                   __uint_as_float(dp[4 * q4 + u + 1]));
             pd[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
             pd[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
           }
@@ -861,13 +904,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 static size_t bwd_workspace_bytes(long long ntiles, int Hq) {
   const long long rows_pad = ntiles * kBlockM;
   return attn_workspace_bytes(ntiles, kBlockM) + 2 * align256(sizeof(float) * rows_pad * Hq) +
-         align256(sizeof(int32_t) * 8);
+         align256(sizeof(int32_t) * 8) + align256(static_cast<size_t>(kBwdAugBytes) * ntiles * Hq);
 }
 
 template <int D>
 static int launch_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
                       const float* lse, long long t_local, long long T, int Hq, int Hkv, float scale,
-                      const AttnWorkspace& ws, float* lse2, float* dvec, int32_t* work, long long ntiles, float* dq,
+                      const AttnWorkspace& ws, float* lse2, float* dvec, uint8_t* aug, int32_t* work, long long ntiles,
+                      float* dq,
                       float* dk, float* dv, int32_t* err, cudaStream_t s) {
   EncodeTiledFn enc = get_encode_tiled();
   if (enc == nullptr) return CPTHD_ERR_CUDA;
@@ -879,7 +923,7 @@ static int launch_bwd(const void* q, const void* k, const void* v, const void* o
   const long long warps = static_cast<long long>(rows_pad) * Hq;
   attn_bwd_pre_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, t_local, Hq, rows_pad,
-      lse2, dvec, work);
+      scale * 1.4426950408889634f, lse2, dvec, aug, work);
   // The dQ grid runs in decreasing-cost order (the forward's group order
   // over the query tiles) when it needs more than one wave of CTAs.
   const bool ordered = ntiles * Hq > sm_count();
@@ -894,6 +938,7 @@ static int launch_bwd(const void* q, const void* k, const void* v, const void* o
   p.order = ordered ? ws.order : nullptr;
   p.lse2 = lse2;
   p.dvec = dvec;
+  p.aug = aug;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
@@ -983,12 +1028,14 @@ extern "C" int thd_causal_attn_bwd(const int32_t* q_slice_idx_dev, int64_t t_loc
   float* lse2 = reinterpret_cast<float*>(extra);
   float* dvec = reinterpret_cast<float*>(extra + align256(sizeof(float) * ntiles * kBlockM * Hq));
   int32_t* work = reinterpret_cast<int32_t*>(extra + 2 * align256(sizeof(float) * ntiles * kBlockM * Hq));
+  uint8_t* aug = reinterpret_cast<uint8_t*>(extra + 2 * align256(sizeof(float) * ntiles * kBlockM * Hq) +
+                                            align256(sizeof(int32_t) * 8));
   attn_group_meta_kernel<kBlockM><<<static_cast<unsigned>(ntiles), kBlockM, 0, s>>>(
       index_list(q_slice_idx_dev), t_local, cu_seqlens_dev, cup, num_docs, T, ws, err_dev);
   CPTHD_TRY_CUDA(cudaGetLastError());
   if (d == 128)
     return launch_bwd<128>(q_dev, k_dev, v_dev, out_dev, dout_dev, lse_dev, t_local, T, Hq, Hkv, scale, ws, lse2,
-                           dvec, work, ntiles, dq_dev, dk_dev, dv_dev, err_dev, s);
+                           dvec, aug, work, ntiles, dq_dev, dk_dev, dv_dev, err_dev, s);
   return launch_bwd<64>(q_dev, k_dev, v_dev, out_dev, dout_dev, lse_dev, t_local, T, Hq, Hkv, scale, ws, lse2, dvec,
-                        work, ntiles, dq_dev, dk_dev, dv_dev, err_dev, s);
+                        aug, work, ntiles, dq_dev, dk_dev, dv_dev, err_dev, s);
 }
