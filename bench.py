@@ -62,7 +62,7 @@ L2_FLUSH_BYTES = 256 << 20
 ATTN_SOURCES = ("csrc/attn_fwd.cu", "csrc/attn_plan.cuh", "csrc/attn_common.cuh", "csrc/attn_meta.cuh",
                 "csrc/sm100.cuh", "csrc/common.cuh")
 ATTN_TRAFFIC = {"workload": "long131072_h8", "bytes_per_launch": 1029514616,
-                "source_sha256": "9d84fbcb6b5d8eba2b30c247f8fae28bda24af03716397c5c71a3a5d11bbd483"}
+                "source_sha256": "76e50bff4976ddc28e8cafa94c61d8f4f9e5287438dbfdcc69f36cde80dd6098"}
 
 
 def load_peaks():
