@@ -248,7 +248,9 @@ CPTHD_API int thd_causal_attn_plan_partition(int strategy, int64_t T, const int3
                                              int32_t* err_dev, cpthd_stream_t stream);
 
 /* Device workspace thd_causal_attn_bwd needs (per-row key bounds, per-tile key
- * intervals, lse * log2(e) and rowsum(dO * O) per row and query head). Host only. */
+ * intervals, lse * log2(e) and rowsum(dO * O) per row and query head, and
+ * 64 bytes per row and query head of per-query MMA operands for the dK/dV
+ * pass). Host only. */
 CPTHD_API int thd_causal_attn_bwd_workspace_size(int64_t t_local, int Hq, int Hkv, int d, size_t* bytes_host);
 
 /* Causal packed-THD attention backward for one rank's query slice: the
