@@ -177,7 +177,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sOut = smem + L::kOutOff;
 
   __shared__ uint64_t q_full[2], q_free[2], k_full[kStages], v_full[kStages];
-  __shared__ uint64_t s_full[2][kStages], p_full[2], o_final[2], o_free[2];
+  // p_half[x]: P_x of the block's first 64 keys is in TMEM (and V_b has
+  // landed); p_full[x]: all of P_x (and K_{b+1} has landed)
+  __shared__ uint64_t s_full[2][kStages], p_half[2], p_full[2], o_final[2], o_free[2];
   __shared__ uint64_t item_full[2], item_empty[2], drain[1];
   __shared__ ItemDesc item_desc[2];
   __shared__ ItemDesc wg_desc[2];
@@ -197,6 +199,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&q_full[x], 1);
       mbar_init(&q_free[x], 1);   // the commit after the item's last S_x
       for (int s = 0; s < kStages; ++s) mbar_init(&s_full[x][s], 1);  // scores of tile x, key blocks of stage s
+      mbar_init(&p_half[x], 5);   // four softmax warps and the data relay
       mbar_init(&p_full[x], 5);   // four softmax warps and the data relay
       mbar_init(&o_final[x], 1);
       mbar_init(&o_free[x], 4);   // the four softmax warps of tile x
@@ -436,12 +439,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           umma_ss_w(t_s, qb + off, q_hi, kb + off, k_hi, kIdescS, kk > 0);
         }
       };
-      auto issue_pv = [&](int j, int x, uint32_t acc0) {  // O_x (+)= P_x V_j, P_x read from TMEM
+      // O_x (+)= P_x V_j over keys [64 h, 64 h + 64) of the block, P_x read from TMEM
+      auto issue_pv = [&](int j, int x, int h, uint32_t acc0) {
         const uint32_t t_s = tmem + x * kBlockN;
         const uint32_t t_o = tmem + 256 + x * D;
         const uint32_t vb = v_lo + (((j & 1) * L::kKV) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
+        for (int kk = 4 * h; kk < 4 * h + kBlockN / 32; ++kk)
           umma_ts_w(t_o, t_s + kk * 8, vb + ((kk * 16 * 128) >> 4), v_hi, kIdescO, kk > 0 ? 1u : acc0);
       };
       int b = 0, nq = 0;
@@ -471,10 +475,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int x = 0; x < 2; ++x) {
               // the previous item's O_x has been read by its epilogue
               if (j == 0 && k > 0 && !mbar_wait(&o_free[x], (k - 1) & 1, &abort_flag)) { ok = false; break; }
-              // P_x(bb) is ready, and (through the relay's arrival) V_bb and K_{bb+1} have landed
+              // P_x(bb) over the first 64 keys is ready (and, through the
+              // relay's arrival, V_bb has landed): the first half of P V
+              // runs while the softmax warps finish the other 64 keys
+              if (!mbar_wait(&p_half[x], bb & 1, &abort_flag)) { ok = false; break; }
+              tc_fence_after_sync();
+              issue_pv(bb, x, 0, j > 0 ? 1u : 0u);
+              // all of P_x(bb) is ready, and K_{bb+1} has landed
               if (!mbar_wait(&p_full[x], bb & 1, &abort_flag)) { ok = false; break; }
               tc_fence_after_sync();
-              issue_pv(bb, x, j > 0 ? 1u : 0u);
+              issue_pv(bb, x, 1, 1u);
               if (more) {
                 issue_s(bb + 1, x);
                 umma_commit(&s_full[x][(bb + 1) & 1]);  // also reports O_x += P_x(bb) V_bb done
@@ -502,12 +512,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
    } else if (warp == 2) {
     // ------------------------------------------------------------ data relay
-    // Waits, per key block, until V_b and (when the item has a next block)
-    // K_{b+1} have landed and then arrives on both tiles' p_full, so that the
-    // MMA issuer (the busiest thread of the CTA) needs a single wait per tile
-    // and block. Before arriving for block b it waits for both p_full phases
-    // of block b - 1 to complete, so that an early arrival never counts
-    // toward the previous phase.
+    // Waits, per key block, until V_b has landed and arrives on both tiles'
+    // p_half, then until (when the item has a next block) K_{b+1} has landed
+    // and arrives on both tiles' p_full, so that the MMA issuer (the busiest
+    // thread of the CTA) waits on one barrier per half of P V. Before
+    // arriving for block b it waits for both p_full phases of block b - 1 to
+    // complete (which implies the p_half phases: the softmax warps arrive on
+    // p_half first), so that an early arrival never counts toward the
+    // previous phase.
     if (lane == 0) {
       int b = 0;
       bool ok = true;
@@ -520,15 +532,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (bb > 0 && !(mbar_wait(&p_full[0], (bb - 1) & 1, &abort_flag) &&
                           mbar_wait(&p_full[1], (bb - 1) & 1, &abort_flag))) { ok = false; break; }
           if (!mbar_wait(&v_full[bb & 1], (bb >> 1) & 1, &abort_flag)) { ok = false; break; }
-          if (j + 1 < n_blocks && !mbar_wait(&k_full[(bb + 1) & 1], ((bb + 1) >> 1) & 1, &abort_flag)) {
-            ok = false;
-            break;
-          }
 #ifdef CPTHD_WAIT_TEST
           // Test build only: key block 1's arrivals are withheld, so the waits
           // for P(1) can never complete and must run out into the abort path.
           if (g_wait_test_mode == 1 && bb == 1) continue;
 #endif
+          mbar_arrive(&p_half[0]);
+          mbar_arrive(&p_half[1]);
+          if (j + 1 < n_blocks && !mbar_wait(&k_full[(bb + 1) & 1], ((bb + 1) >> 1) & 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
           mbar_arrive(&p_full[0]);
           mbar_arrive(&p_full[1]);
         }
@@ -665,6 +679,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // p = 2^(scale*log2(e)*s - m): one packed FMA per pair, ex2 per element,
         // row sum in two packed accumulators. A 64-column half no row may use
         // stores zeros without exponentials; elsewhere masked columns give 0.
+        // Each half is released to the MMA issuer as soon as it is stored, so
+        // that P V over the first 64 keys runs during the second half.
         float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -685,25 +701,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
           }
           tmem_st32(t_s + 32 * h2, pk);
+          if (h2 == 0 && __any_sync(0xffffffffu, grow_o)) {
+            // O_x holds P_x V up to the previous block (complete before S_x(bb)
+            // was reported) and nothing newer: rescale it before this block's
+            // first half of P V, which p_half releases (here, once the first
+            // half's scores no longer hold registers)
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t orr[32];
+              tmem_ld32(t_o + c * 32, orr);
+              tmem_ld_wait(orr);
+#pragma unroll
+              for (int q = 0; q < 32; ++q) orr[q] = __float_as_uint(__uint_as_float(orr[q]) * alpha);
+              tmem_st32(t_o + c * 32, orr);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(h2 == 0 ? &p_half[x] : &p_full[x]);
         }
         l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-        if (__any_sync(0xffffffffu, grow_o)) {
-          // O_x holds P_x V up to the previous block (complete before S_x(bb)
-          // was reported) and nothing newer: rescale it before the next P V
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t orr[32];
-            tmem_ld32(t_o + c * 32, orr);
-            tmem_ld_wait(orr);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) orr[q] = __float_as_uint(__uint_as_float(orr[q]) * alpha);
-            tmem_st32(t_o + c * 32, orr);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[x]);
       }
       b += n_blocks;
       // The tile's rows and head are read again here rather than kept
