@@ -62,7 +62,7 @@ L2_FLUSH_BYTES = 256 << 20
 ATTN_SOURCES = ("csrc/attn_fwd.cu", "csrc/attn_plan.cuh", "csrc/attn_common.cuh", "csrc/attn_meta.cuh",
                 "csrc/sm100.cuh", "csrc/common.cuh")
 ATTN_TRAFFIC = {"workload": "long131072_h8", "bytes_per_launch": 1061359112,
-                "source_sha256": "2ebe729913ef1c3d1f4250b21071cbdaf9c4c1fdf61612aafd82e17d0743eebb"}
+                "source_sha256": "2641be9ab235f1febf48f65e008aaf9a7e39d82ae703fb56cb015a130604a122"}
 
 
 def load_peaks():

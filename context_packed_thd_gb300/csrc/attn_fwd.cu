@@ -21,7 +21,10 @@
 //                scores are done (the issuer commits to q_free after the
 //                last S), so the next item's Q loads while this one ends.
 //  * warp 1      one lane issues all tcgen05 MMAs: S_A(0), S_B(0), then per
-//                block j and tile x = A, B: O_x += P_x(j) V_j, S_x(j+1).
+//                block j and tile x = A, B: O_x += P_x(j) V_j in two halves
+//                of 64 keys (the first as soon as the softmax has stored
+//                P_x for those keys, so that it runs while the softmax
+//                computes the other 64), then S_x(j+1).
 //                Issuing tile A's batch before tile B's from one thread keeps
 //                the two tiles half a period apart, so that each tile's
 //                softmax runs while the tensor pipe works on the other tile.
@@ -34,9 +37,11 @@
 //                order, the commit that reports S_x(j+1) also reports that
 //                O_x += P_x(j) V_j is done, so the softmax may then rescale
 //                O_x and overwrite P_x without further waits.
-//  * warp 2      data relay: per block j, waits until V_j and K_{j+1} have
-//                landed and arrives on both tiles' P-ready barriers, so that
-//                the issuer waits once per tile and block.
+//  * warp 2      data relay: per block j, waits until V_j has landed and
+//                arrives on both tiles' first-half barriers (p_half), then
+//                until K_{j+1} has landed and arrives on both tiles' P-ready
+//                barriers (p_full), so that the issuer waits once per half
+//                of P V.
 //  * warp 3      idle.
 //  * warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: each thread
 //                owns one query row (its TMEM lane). It reads S with one
@@ -45,7 +50,8 @@
 //                interval (only on blocks the tile's bounds do not cover
 //                fully), keeps the fp32 running max / sum in base 2, rescales
 //                O in TMEM only when the max grows by more than 2^8 (exact
-//                either way), and writes P back into TMEM. At the end each
+//                either way; before the block's first half of P is
+//                released), and writes P back into TMEM, 64 keys at a time. At the end each
 //                thread normalises its row of O and writes it (bf16, 16-byte
 //                stores) straight to the output, and its LSE.
 // Key blocks start at the group's interval starts (document starts), so
