@@ -409,7 +409,7 @@ def other_workloads(cp, current, dev, flush, peak, peak_sustained, hbm_peak):
                                         "useful_pair_frac": round(sum(st.pairs) / sum(st.kpairs), 4)}
         dcs = [st for st in sts if st.name == W.DUAL_CHUNK_SWAP]
         restore = kv_restore(cp, cfg, dcs[0], flush, hbm_peak) if dcs else None
-        bwd = backward(cp, cfg, sts, range(cfg.cp), flush, peak)
+        bwd = backward(cp, cfg, sts, range(cfg.cp), flush, peak, peak_sustained)
         for st in sts:
             e = st.err.cpu().tolist()
             if e[0] != 0:
@@ -500,11 +500,13 @@ def dcs_two_launch(cp, cfg, st, ranks, flush):
             "max_abs_diff_vs_one_launch": max_diff, "bit_identical_to_one_launch": bool(identical)}
 
 
-def backward(cp, cfg, strategies, ranks, flush, peak):
+def backward(cp, cfg, strategies, ranks, flush, peak, peak_sustained=None):
     """The attention backward of every (strategy, rank) slice of the step,
     timed alone (graph replays, L2 flushed before each). Algorithmic work is
     the usual 2.5x the forward: 10 * d * pairs * Hq (the S recompute, dP, dS V,
-    dQ, dK, dV products counted once)."""
+    dQ, dK, dV products counted once). It runs after the timed step, for tens
+    of milliseconds of tensor work, so it is given as a fraction of both the
+    burst and the sustained peak."""
     res = {}
     tot_f, tot_ms = 0.0, 0.0
     for st in strategies:
@@ -532,6 +534,8 @@ def backward(cp, cfg, strategies, ranks, flush, peak):
     tf = tot_f / (tot_ms * 1e-3) / 1e12
     res["all"] = {"tflops": round(tf, 3), "frac_of_peak": round(tf / peak, 4),
                   "flops": "10 * d * unmasked pairs * Hq per slice"}
+    if peak_sustained:
+        res["all"]["frac_of_sustained_peak"] = round(tf / peak_sustained, 4)
     return res
 
 
@@ -777,7 +781,7 @@ def run_cuda(args):
     extras = set() if args.no_extras else set(args.extras.split(","))
     restore = kv_restore(cp, cfg, dcs_st[0], flush, hbm_peak) if dcs_st and "restore" in extras else None
     two = dcs_two_launch(cp, cfg, dcs_st[0], ranks, flush) if dcs_st and "two_launch" in extras else None
-    bwd = backward(cp, cfg, strategies, ranks, flush, peak) if "backward" in extras else None
+    bwd = backward(cp, cfg, strategies, ranks, flush, peak, peak_sustained) if "backward" in extras else None
     others = other_workloads(cp, cfg.name, dev, flush, peak, peak_sustained, hbm_peak) if "others" in extras else None
 
 
