@@ -11,9 +11,10 @@ smaller). Pad query rows of dQ and keys no
 query of the slice reaches (dK, dV) must be exactly zero.
 
 Cases: every element of the tiny, T=8192 and lognormal slices listed below,
-edge cases, seeded random packs, and one query head (all its dQ rows and all
+edge cases, seeded random packs, one query head (all its dQ rows and all
 its dK/dV keys) of the 131072-token DualChunkSwap rank 3 computed with all
-eight heads, the slice the backward is benchmarked on.
+eight heads, the slice the backward is benchmarked on, and a pack with
+sharp scores and a large dO (large per-query terms).
 """
 import numpy as np
 import pytest
@@ -179,3 +180,27 @@ def test_backward_long_context_rank_one_head():
     assert err.cpu().tolist() == [0, 0]
     _compare("long131072_h8/dcs/rank3/head0", (dq, dk, dv), inp.q[torch.from_numpy(idx)], inp.k, inp.v, lay, idx,
              dout, heads=[0])
+
+
+def test_backward_sharp_scores_and_large_dout():
+    """Scores six times sharper than the N(0,1) inputs give (Q scaled by 6
+    before its bf16 rounding) and dO twenty times larger, so |s| reaches the
+    hundreds and |LSE| and |D| the tens. The dK/dV pass takes the per-query
+    terms lse * log2(e) / (scale log2(e)) and D into its score MMAs as sums of
+    three bf16 terms; a split that kept fewer bits, or a wrong sign, breaks
+    the element bound here. Both partitions, both ranks, GQA 2/1, d = 128,
+    two documents."""
+    dev = cuda_or_skip(); cp = load_lib()
+    lengths = (700, 1300)
+    lay = W.make_layout(list(lengths), 1)
+    q, k, v = W.make_qkv_logical(91, sum(lengths), 2, 1, 128)
+    q = (q.float() * 6).to(torch.bfloat16)
+    cfg = W.Config("sharp", 91, lengths, 2, 1, 128, 2, ("dcs",), 1)
+    inp = W.AttnInputs(cfg, "dcs", lay, q, k, v)
+    dout_phys = (W.randn_bf16(91, 6, (lay.T, 2, 128)).float() * 20).to(torch.bfloat16)
+    err = new_err(dev)
+    for s in ("dcs", "nlb"):
+        for r in range(2):
+            idx, dq, dk, dv, dout = _rank_bwd(cp, inp, s, 2, r, dev, dout_phys, err)
+            _compare(f"sharp/{s}/r{r}", (dq, dk, dv), q[torch.from_numpy(idx)], k, v, lay, idx, dout)
+    assert err.cpu().tolist() == [0, 0]
