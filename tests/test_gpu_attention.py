@@ -502,3 +502,39 @@ def test_long_items_cut_into_pieces_every_row(hq, hkv, dd):
     assert np.array_equal(idx.cpu().numpy(), ref_idx)
     ro, rl = A.attention_fwd(inp.q, inp.k, inp.v, lay.cu_seqlens, lay.cu_seqlens_padded, ref_idx)
     assert_attn_matches(outs[0][0], outs[0][1], ro, rl, f"one document, Hq {hq}, d {dd}")
+
+
+@pytest.mark.parametrize("total", [1024, 16384])
+def test_running_max_jumps_every_block(total):
+    """Scores that rise by about 10 (in units of log2) from one key block to
+    the next: the keys of block b are b * gamma times a direction every
+    query shares, plus small N(0,1) noise. Each new block then raises every
+    row's running max by more than the softmax's rescale threshold (8), so
+    O is rescaled in TMEM at every block (the path the two-half P V release
+    has to order before the block's first P V). 1024 tokens run as whole items
+    from the counter; 16384 tokens make the plan cut items into pieces, whose
+    merge combines partial results of very different maxima. One head,
+    d = 128, cp_size 1, every row against the oracle."""
+    dev = cuda_or_skip(); cp = load_lib()
+    d_ = 128
+    lay = W.make_layout([total], 1)
+    q0, k0, v = W.make_qkv_logical(55, total, 1, 1, d_)
+    scale = 1.0 / np.sqrt(d_)
+    gamma = 10.0 / (scale * d_ * 0.25 * np.log2(np.e))  # log2 step per block with directions of 0.5
+    blk = torch.arange(total, dtype=torch.float32) // 128
+    q = (0.5 + 0.05 * q0.float()).to(torch.bfloat16)
+    k = (0.5 * gamma * blk[:, None, None] + 0.05 * k0.float()).to(torch.bfloat16)
+    cfg = W.Config("jumps", 55, (total,), 1, 1, d_, 1, ("nlb",), 1)
+    inp = W.AttnInputs(cfg, "nlb", lay, q, k, v)
+    d = DevInputs(inp, dev)
+    err = new_err(dev)
+    idx = cp.cp_partition_index("nlb", d.cup, lay.T, 1, 0, err=err)
+    q_loc = cp.cp_reorder(d.q, idx, err=err)
+    out, lse = cp.thd_causal_attn_fwd(idx, q_loc, d.k, d.v, d.cu, d.cup, err=err)
+    torch.cuda.synchronize()
+    assert err.cpu().tolist() == [0, 0]
+    ref_idx = np.arange(lay.T, dtype=np.int64)
+    ro, rl = A.attention_fwd(q, k, v, lay.cu_seqlens, lay.cu_seqlens_padded, ref_idx)
+    # the premise: the rows' maxima rise by more than the threshold per block
+    assert float(rl[0, -1] - rl[0, 127]) * np.log2(np.e) > 8.0 * (total // 128 - 1)
+    assert_attn_matches(out, lse, ro, rl, f"running max jumps, {total} tokens")
