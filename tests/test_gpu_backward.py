@@ -13,8 +13,8 @@ query of the slice reaches (dK, dV) must be exactly zero.
 Cases: every element of the tiny, T=8192 and lognormal slices listed below,
 edge cases, seeded random packs, one query head (all its dQ rows and all
 its dK/dV keys) of the 131072-token DualChunkSwap rank 3 computed with all
-eight heads, the slice the backward is benchmarked on, and a pack with
-sharp scores and a large dO (large per-query terms).
+eight heads, the slice the backward is benchmarked on, a pack with sharp
+scores and a large dO (large per-query terms), and an empty slice.
 """
 import numpy as np
 import pytest
@@ -204,3 +204,29 @@ def test_backward_sharp_scores_and_large_dout():
             idx, dq, dk, dv, dout = _rank_bwd(cp, inp, s, 2, r, dev, dout_phys, err)
             _compare(f"sharp/{s}/r{r}", (dq, dk, dv), q[torch.from_numpy(idx)], k, v, lay, idx, dout)
     assert err.cpu().tolist() == [0, 0]
+
+
+def test_empty_slice():
+    """A rank slice of no rows (t_local = 0) against a nonempty K/V buffer:
+    the forward returns empty outputs without error, and the backward's
+    contribution to dK and dV is all zeros (the buffers are pre-filled with
+    garbage to see that every entry is written)."""
+    dev = cuda_or_skip(); cp = load_lib()
+    lay = W.make_layout([300], 1)
+    _, k, v = W.make_qkv_logical(5, 300, 2, 2, 64)
+    k, v = k.to(dev), v.to(dev)
+    cu = torch.from_numpy(lay.cu_seqlens).to(dev)
+    cup = torch.from_numpy(lay.cu_seqlens_padded).to(dev)
+    idx = torch.empty(0, dtype=torch.int32, device=dev)
+    q_loc = torch.empty((0, 2, 64), dtype=torch.bfloat16, device=dev)
+    err = new_err(dev)
+    out, lse = cp.thd_causal_attn_fwd(idx, q_loc, k, v, cu, cup, err=err)
+    assert tuple(out.shape) == (0, 2, 64) and tuple(lse.shape) == (2, 0)
+    dk = torch.full((300, 2, 64), 7.0, dtype=torch.float32, device=dev)
+    dv = torch.full((300, 2, 64), -3.0, dtype=torch.float32, device=dev)
+    dq, dk, dv = cp.thd_causal_attn_bwd(idx, q_loc, k, v, out, torch.empty_like(q_loc), lse, cu, cup, dk=dk, dv=dv,
+                                        err=err)
+    torch.cuda.synchronize()
+    assert err.cpu().tolist() == [0, 0]
+    assert tuple(dq.shape) == (0, 2, 64)
+    assert bool((dk == 0).all()) and bool((dv == 0).all())
