@@ -14,7 +14,8 @@ Cases: every element of the tiny, T=8192 and lognormal slices listed below,
 edge cases, seeded random packs, one query head (all its dQ rows and all
 its dK/dV keys) of the 131072-token DualChunkSwap rank 3 computed with all
 eight heads, the slice the backward is benchmarked on, a pack with sharp
-scores and a large dO (large per-query terms), and an empty slice.
+scores and a large dO (large per-query terms), an empty slice, and the
+largest slice the backward takes (2048 query tiles).
 """
 import numpy as np
 import pytest
@@ -230,3 +231,33 @@ def test_empty_slice():
     assert err.cpu().tolist() == [0, 0]
     assert tuple(dq.shape) == (0, 2, 64)
     assert bool((dk == 0).all()) and bool((dv == 0).all())
+
+
+def test_backward_largest_slice():
+    """The largest slice the backward takes: 2048 query tiles (t_local =
+    262,144 rows), the capacity of the dK/dV pass's per-item tile lists
+    (16-bit entries: tile index and a full-tile bit). 512 documents of 512
+    tokens, one head, d = 64, cp_size 1; every element of dQ, dK and dV
+    against the oracle. One more tile is refused on the host."""
+    dev = cuda_or_skip(); cp = load_lib()
+    lengths = [512] * 512
+    lay = W.make_layout(lengths, 1)
+    q, k, v = W.make_qkv_logical(303, lay.T, 1, 1, 64)
+    cfg = W.Config("max_tiles", 303, tuple(lengths), 1, 1, 64, 1, ("nlb",), 1)
+    inp = W.AttnInputs(cfg, "nlb", lay, q, k, v)
+    dout_phys = W.randn_bf16(303, 6, (lay.T, 1, 64))
+    err = new_err(dev)
+    idx, dq, dk, dv, dout = _rank_bwd(cp, inp, "nlb", 1, 0, dev, dout_phys, err)
+    assert idx.shape[0] == 2048 * 128
+    assert err.cpu().tolist() == [0, 0]
+    _compare("largest slice", (dq, dk, dv), q[torch.from_numpy(idx)], k, v, lay, idx, dout)
+    too_many = 2048 * 128 + 1
+    with pytest.raises(cp.CpthdError, match="status -"):
+        cp.thd_causal_attn_bwd(torch.zeros(too_many, dtype=torch.int32, device=dev),
+                               torch.zeros((too_many, 1, 64), dtype=torch.bfloat16, device=dev),
+                               torch.zeros((too_many, 1, 64), dtype=torch.bfloat16, device=dev),
+                               torch.zeros((too_many, 1, 64), dtype=torch.bfloat16, device=dev),
+                               torch.zeros((too_many, 1, 64), dtype=torch.bfloat16, device=dev),
+                               torch.zeros((too_many, 1, 64), dtype=torch.bfloat16, device=dev),
+                               torch.zeros((1, too_many), dtype=torch.float32, device=dev),
+                               torch.tensor([0, too_many], dtype=torch.int32, device=dev))
