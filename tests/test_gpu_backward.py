@@ -110,6 +110,7 @@ def test_backward_matches_oracle(name, strategy, ranks):
     dict(lengths=[300], pad=1, hq=2, hkv=2, d=128, cp=1),                  # ragged tail
     dict(lengths=[1, 0, 5, 0, 130, 1, 2], pad=1, hq=4, hkv=1, d=64, cp=1),  # empty, one-token docs, GQA 4
     dict(lengths=[37, 91, 250, 3], pad=8, hq=6, hkv=2, d=128, cp=4),       # pads, GQA 3
+    dict(lengths=[517, 1, 260, 900], pad=4, hq=16, hkv=1, d=64, cp=2),     # 16 query heads per KV head
 ])
 def test_backward_edge_cases(case):
     dev = cuda_or_skip(); cp = load_lib()
